@@ -1,0 +1,395 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: hand-worked
+cases from the pages' rules (tests/golden/), brute force on tiny inputs, a
+special case that reduces to a library routine, an identity stated on the
+pages, or an fp64 dense restatement.  None of them needs a GPU.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _sig64(v):
+    return 1.0 / (1.0 + np.exp(-np.asarray(v, np.float64)))
+
+
+def _route_from_logits(ref, logits, bias, K, norm, scale, top_p, H=64):
+    """Run the oracle router on inputs whose logits are exactly ``logits`` (per token rows)."""
+    logits = np.atleast_2d(np.asarray(logits, np.float32))
+    T, E = logits.shape
+    x = np.zeros((T, H), np.float32)
+    wr = np.zeros((E, H), np.float32)
+    # token t is the one-hot vector e_t (t < H), expert e's row holds its logit for each token
+    assert T <= H
+    for t in range(T):
+        x[t, t] = 1.0
+        wr[:, t] = logits[t]
+    cfg = ref.make_config(H, E, K, 64, 0, 0, norm, scale, top_p)
+    return ref.route(cfg, x, wr, np.asarray(bias, np.float32), with_logits=True)
+
+
+# ---------------------------------------------------------------- router
+
+@pytest.mark.parametrize("case", _load("router_cases.json")["cases"], ids=lambda c: c["name"])
+def test_router_hand_cases(ref, case):
+    out = _route_from_logits(ref, case["logits"], case["bias"], case["top_k"], case["norm"],
+                             case["scale"], case["top_p"])
+    np.testing.assert_array_equal(out["logits"][0], np.float32(case["logits"]))
+    assert out["ids"][0].tolist() == case["ids"]
+    assert int(out["keff"][0]) == case["keff"]
+    np.testing.assert_allclose(out["w"][0], case["w"], rtol=1e-6, atol=1e-7)
+
+
+def _random_layer(E, H, T, seed, bias_std=0.1):
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((T, H)).astype(np.float32)
+    wr = (g.standard_normal((E, H)) / math.sqrt(H)).astype(np.float32)
+    bias = (g.standard_normal(E) * bias_std).astype(np.float32)
+    return x, wr, bias
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_router_brute_force_topk(ref, K):
+    """E = 8: the chosen set maximises the summed choice over all C(8, K) subsets and is
+    listed in descending choice order.  Logits come from an fp64 matmul (independent)."""
+    E, H, T = 8, 64, 64
+    x, wr, bias = _random_layer(E, H, T, 11 + K, bias_std=0.3)
+    cfg = ref.make_config(H, E, K, 64, 0, 0, 1, 1.0, 0.0)
+    out = ref.route(cfg, x, wr, bias)
+    logit = x.astype(np.float64) @ wr.astype(np.float64).T
+    choice = _sig64(logit) + bias.astype(np.float64)
+    checked = 0
+    for t in range(T):
+        srt = np.sort(choice[t])[::-1]
+        if np.min(np.abs(np.diff(srt))) < 1e-5:
+            continue  # near tie: fp32 vs fp64 may legitimately differ
+        best = max(itertools.combinations(range(E), K), key=lambda s: sum(choice[t, list(s)]))
+        assert sorted(out["ids"][t].tolist()) == sorted(best)
+        assert out["ids"][t].tolist() == sorted(best, key=lambda e: -choice[t, e])
+        checked += 1
+    assert checked > T // 2
+
+
+def test_router_bias_changes_choice_not_weights(ref):
+    """noaux_tc: perturbing the bias changes which experts are picked, but the weight of every
+    picked expert stays its unbiased sigmoid renormalised over the picked set."""
+    E, H, T, K = 16, 64, 64, 4
+    x, wr, bias = _random_layer(E, H, T, 5)
+    cfg = ref.make_config(H, E, K, 64, 0, 0, 1, 2.5, 0.0)
+    logit = x.astype(np.float64) @ wr.astype(np.float64).T
+    changed = 0
+    base = ref.route(cfg, x, wr, bias)
+    for trial, b in enumerate([bias, bias + np.linspace(-0.5, 0.5, E, dtype=np.float32),
+                               -3 * bias]):
+        out = ref.route(cfg, x, wr, b.astype(np.float32))
+        for t in range(T):
+            ids = out["ids"][t]
+            g = _sig64(logit[t, ids])
+            np.testing.assert_allclose(out["w"][t], 2.5 * g / g.sum(), rtol=2e-5)
+        changed += int((out["ids"] != base["ids"]).any(axis=1).sum())
+    assert changed > 0
+
+
+def test_router_bias_shift_invariance(ref):
+    """Adding the same constant to every bias leaves the selection unchanged."""
+    E, H, T, K = 32, 128, 64, 8
+    x, wr, bias = _random_layer(E, H, T, 7)
+    cfg = ref.make_config(H, E, K, 64, 0, 0, 1, 1.0, 0.0)
+    a = ref.route(cfg, x, wr, bias)
+    b = ref.route(cfg, x, wr, bias + np.float32(0.25))
+    logit = x.astype(np.float64) @ wr.astype(np.float64).T
+    choice = _sig64(logit) + bias
+    for t in range(T):
+        srt = np.sort(choice[t])[::-1][:K + 1]
+        if np.min(np.abs(np.diff(srt))) < 1e-5:
+            continue
+        assert a["ids"][t].tolist() == b["ids"][t].tolist()
+
+
+def test_router_full_k_is_normalised_sigmoid(ref):
+    """K = E, no bias, norm on, scale 1: weights = sigmoid / sum(sigmoid) over all experts
+    (the normalised-sigmoid router of "colibrì 深度拆解" §3.4), checked with scipy's expit."""
+    scipy_special = pytest.importorskip("scipy.special")
+    E, H, T = 16, 64, 32
+    x, wr, _ = _random_layer(E, H, T, 3)
+    cfg = ref.make_config(H, E, E, 64, 0, 0, 1, 1.0, 0.0)
+    out = ref.route(cfg, x, wr, np.zeros(E, np.float32))
+    s = scipy_special.expit(x.astype(np.float64) @ wr.astype(np.float64).T)
+    p = s / s.sum(axis=1, keepdims=True)
+    for t in range(T):
+        np.testing.assert_allclose(out["w"][t], p[t, out["ids"][t]], rtol=2e-5)
+        assert sorted(out["ids"][t].tolist()) == list(range(E))
+        assert np.all(np.diff(p[t, out["ids"][t]]) <= 1e-6)  # descending sigmoid order
+
+
+def test_router_norm_sums_to_scale(ref):
+    E, H, T, K = 64, 128, 128, 8
+    x, wr, bias = _random_layer(E, H, T, 9)
+    for scale in (1.0, 2.5):
+        for top_p in (0.0, 0.7):
+            cfg = ref.make_config(H, E, K, 64, 0, 0, 1, scale, top_p)
+            out = ref.route(cfg, x, wr, bias)
+            s = out["w"].astype(np.float64).sum(axis=1)
+            np.testing.assert_allclose(s, scale, rtol=K * 1.2e-7)
+            for t in range(T):
+                k = out["keff"][t]
+                assert 1 <= k <= K
+                assert np.all(out["ids"][t, :k] >= 0) and np.all(out["ids"][t, k:] == -1)
+                assert np.all(out["w"][t, k:] == 0)
+                assert len(set(out["ids"][t, :k].tolist())) == k
+
+
+def test_top_p_equal_gates(ref):
+    """Equal gates g: the running sum m*g first reaches p*K*g at m = ceil(p*K)."""
+    K = 8
+    for p, m in ((0.3, 3), (0.55, 5), (0.8, 7), (0.99, 8)):
+        out = _route_from_logits(ref, [0.25] * K, [0.0] * K, K, 1, 1.0, p)
+        assert int(out["keff"][0]) == m
+        assert out["ids"][0, :m].tolist() == list(range(m))  # stable: selection order kept
+        np.testing.assert_allclose(out["w"][0, :m], 1.0 / m, rtol=1e-6)
+
+
+def test_top_p_near_one_keeps_all(ref):
+    E, H, T, K = 32, 64, 64, 8
+    x, wr, bias = _random_layer(E, H, T, 13)
+    cfg = ref.make_config(H, E, K, 64, 0, 0, 1, 1.0, 0.9999999)
+    out = ref.route(cfg, x, wr, bias)
+    assert np.all(out["keff"] == K)
+
+
+# ---------------------------------------------------------------- permute
+
+def _brute_lists(ids, keff, E):
+    lists = {e: [] for e in range(E)}
+    T, K = ids.shape
+    for t in range(T):
+        for i in range(keff[t]):
+            lists[int(ids[t, i])].append((t, t * K + i))
+    return lists
+
+
+@pytest.mark.parametrize("T,E,K,top_p", [(0, 8, 2, 0.0), (1, 8, 2, 0.0), (37, 16, 4, 0.0),
+                                         (64, 256, 8, 0.7), (200, 8, 8, 0.0)])
+def test_permute_against_brute_force(ref, T, E, K, top_p):
+    H = 64
+    x, wr, bias = _random_layer(E, H, max(T, 1), 21 + T)
+    x = x[:T]
+    cfg = ref.make_config(H, E, K, 64, 0, 0, 1, 1.0, top_p)
+    r = ref.route(cfg, x, wr, bias)
+    out = ref.permute(cfg, r["ids"], r["keff"])
+    lists = _brute_lists(r["ids"], r["keff"], E)
+    assert out["counts"].tolist() == [len(lists[e]) for e in range(E)]
+    assert out["offsets"].tolist() == [0] + list(itertools.accumulate(len(lists[e]) for e in range(E)))
+    assert int(out["counts"].sum()) == int(r["keff"].sum())
+    for e in range(E):
+        a, b = out["offsets"][e], out["offsets"][e + 1]
+        assert list(zip(out["tok"][a:b].tolist(), out["slot"][a:b].tolist())) == lists[e]
+    assert out["uniq"].tolist() == [e for e in range(E) if lists[e]]
+    # each (t, i) pair appears exactly once
+    assert sorted(out["slot"].tolist()) == sorted(s for e in range(E) for _, s in lists[e])
+
+
+def test_permute_all_on_one_expert(ref):
+    T, E, K = 50, 8, 1
+    cfg = ref.make_config(64, E, K, 64)
+    ids = np.full((T, K), 5, np.int32)
+    keff = np.ones(T, np.int32)
+    out = ref.permute(cfg, ids, keff)
+    assert out["uniq"].tolist() == [5] and out["n_uniq"] == 1
+    assert out["tok"].tolist() == list(range(T))
+
+
+# ---------------------------------------------------------------- int4 / int8 arithmetic
+
+@pytest.mark.parametrize("case", _load("nibble_cases.json")["cases"])
+def test_nibble_order_and_zero_point(ref, case):
+    row = np.zeros(32, np.uint8)
+    row[:len(case["bytes"])] = case["bytes"]
+    for k, v in enumerate(case["values"]):
+        q = np.zeros(64, np.int8)
+        q[k] = 1
+        assert ref.group_dot(row, q, 0) == v
+
+
+def test_nibble_all_byte_values(ref):
+    """Every byte value: element 2j = low nibble - 8, element 2j+1 = high nibble - 8."""
+    for b in range(256):
+        row = np.full(32, b, np.uint8)
+        lo, hi = (b & 15) - 8, (b >> 4) - 8
+        q = np.zeros(64, np.int8); q[0] = 1
+        assert ref.group_dot(row, q, 0) == lo
+        q = np.zeros(64, np.int8); q[1] = 1
+        assert ref.group_dot(row, q, 0) == hi
+        q = np.ones(64, np.int8)
+        assert ref.group_dot(row, q, 0) == 32 * (lo + hi)
+
+
+def test_idot_identity(ref):
+    """dot(u - 8, q) = dot(u, q) - 8 * sum(q) ("colibri 开发演进实录" §2.2), exactly, per group."""
+    g = np.random.default_rng(1)
+    for _ in range(200):
+        row = g.integers(0, 256, 96, dtype=np.uint8)
+        q = g.integers(-127, 128, 192).astype(np.int8)
+        u = np.empty(192, np.int64)
+        u[0::2] = row & 15
+        u[1::2] = row >> 4
+        for grp in range(3):
+            s = slice(64 * grp, 64 * grp + 64)
+            expect = int((u[s] * q[s]).sum()) - 8 * int(q[s].astype(np.int64).sum())
+            assert ref.group_dot(row, q, grp) == expect
+    # extreme: |A| reaches 64 * 8 * 127
+    assert ref.group_dot(np.zeros(32, np.uint8), np.full(64, 127, np.int8), 0) == -64 * 8 * 127
+
+
+@pytest.mark.parametrize("case", _load("quant_cases.json")["cases"])
+def test_quant_hand_cases(ref, case):
+    q, s = ref.quant_row(np.asarray(case["v"], np.float32))
+    assert q.tolist() == case["q"]
+    assert np.float32(s) == np.float32(case["scale"])
+
+
+def test_quant_amax_maps_to_127(ref):
+    g = np.random.default_rng(2)
+    for _ in range(50):
+        v = g.standard_normal(256).astype(np.float32)
+        q, s = ref.quant_row(v)
+        i = int(np.argmax(np.abs(v)))
+        assert int(q[i]) == (127 if v[i] > 0 else -127)
+        assert np.all(np.abs(q.astype(np.int32)) <= 127)
+        # every code is within half a step of v / s
+        assert np.all(np.abs(q - v.astype(np.float64) / s) <= 0.5 + 1e-4)
+
+
+def _unpack(w):
+    w = np.asarray(w)
+    u = np.empty(w.shape[:-1] + (w.shape[-1] * 2,), np.int64)
+    u[..., 0::2] = w & 15
+    u[..., 1::2] = w >> 4
+    return u - 8
+
+
+def test_group_accumulators_brute_force(ref):
+    """Oracle per-group accumulators equal an int64 matmul of the unpacked weights."""
+    wl = synth.Workload("t", 256, 4, 2, 128, 0, 0, (8,))
+    cfg = ref.config_of(wl)
+    x = synth.gen_x(wl, 8).numpy()
+    R = synth.gen_experts(wl)
+    offsets = np.array([0, 3, 5, 8, 8], np.int32)
+    tok = np.array([0, 2, 5, 1, 7, 3, 4, 6], np.int32)
+    out = ref.expert_ffn(cfg, x, R, offsets, tok, probes=True)
+    xq, sx = ref.quant_rows(x)
+    pe = np.repeat(np.arange(4), np.diff(offsets))
+    for p in range(8):
+        e, t = pe[p], tok[p]
+        for name, key in (("w_gate", "acc_gate"), ("w_up", "acc_up")):
+            W = _unpack(R[name][e].numpy())                      # [F, H]
+            prod = W.reshape(128, 4, 64) * xq[t].astype(np.int64).reshape(1, 4, 64)
+            np.testing.assert_array_equal(out[key][p], prod.sum(-1))
+        Wd = _unpack(R["w_down"][e].numpy())                     # [H, F]
+        prod = Wd.reshape(256, 2, 64) * out["hq"][p].astype(np.int64).reshape(1, 2, 64)
+        np.testing.assert_array_equal(out["acc_down"][p], prod.sum(-1))
+        assert np.abs(out["acc_gate"][p]).max() <= 64 * 8 * 127
+
+
+def test_group_scale_indexing(ref):
+    """A distinct scale per (row, group): the result weights group g of row r by s[r, g],
+    never by a per-row scale (the fmt=4 per-group/per-row mix-up of "colibri 开发演进实录" §8.4)."""
+    H, F = 256, 64
+    expert = {
+        "w_gate": np.full((F, H // 2), 0x99, np.uint8),   # every weight = +1
+        "w_up": np.full((F, H // 2), 0x99, np.uint8),
+        "w_down": np.full((H, F // 2), 0x99, np.uint8),
+        "s_gate": (np.arange(F * 4, dtype=np.float32).reshape(F, 4) + 1) * np.float32(1e-3),
+        "s_up": np.ones((F, 4), np.float32),
+        "s_down": np.ones((H, 1), np.float32),
+    }
+    xq = np.zeros(H, np.int8)
+    xq[0:64] = 1        # group 0 sums to 64
+    xq[128:192] = 2     # group 2 sums to 128
+    out = ref.expert_apply(H, F, expert, xq, 1.0, probes=True)
+    g = expert["s_gate"].astype(np.float64)
+    gate = g[:, 0] * 64 + g[:, 2] * 128
+    up = np.full(F, 64 + 128, np.float64)
+    assert np.all(out["acc_gate"][:, 0] == 64) and np.all(out["acc_gate"][:, 2] == 128)
+    assert np.all(out["acc_gate"][:, 1] == 0) and np.all(out["acc_gate"][:, 3] == 0)
+    h = gate / (1 + np.exp(-gate)) * up
+    hq, hs = ref.quant_row(h.astype(np.float32))
+    assert out["hq"].tolist() == hq.tolist()
+    np.testing.assert_allclose(out["y"], np.full(H, hs * int(hq.astype(np.int64).sum())), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- whole layer vs dense fp64
+
+def _dequant(w, s):
+    u = _unpack(w).astype(np.float64)
+    rows, cols = u.shape
+    return (u.reshape(rows, cols // 64, 64) * s.astype(np.float64)[:, :, None]).reshape(rows, cols)
+
+
+def _np_quant(v):
+    v = np.asarray(v, np.float32)
+    amax = np.float32(np.abs(v).max())
+    if amax == 0:
+        return np.zeros(v.shape, np.int8), np.float32(0)
+    inv = np.float32(127) / amax
+    q = np.clip(np.rint(v * inv), -127, 127).astype(np.int8)
+    return q, np.float32(amax / np.float32(127))
+
+
+def _dense_expert(ex, xq, sx):
+    gate = float(sx) * (_dequant(ex["w_gate"], ex["s_gate"]) @ xq.astype(np.float64))
+    up = float(sx) * (_dequant(ex["w_up"], ex["s_up"]) @ xq.astype(np.float64))
+    h = gate / (1 + np.exp(-gate)) * up
+    hq, hs = _np_quant(h.astype(np.float32))
+    return float(hs) * (_dequant(ex["w_down"], ex["s_down"]) @ hq.astype(np.float64))
+
+
+@pytest.mark.parametrize("wname", ["tiny", "tiny_topp_noscale"])
+def test_layer_matches_dense_fp64(ref, wname):
+    """Whole layer vs an fp64 dense restatement: dequantised weights (u - 8) * s expanded per
+    group, activations quantised the same way, gated sum plus shared expert."""
+    wl = synth.WORKLOADS["tiny"]
+    if wname == "tiny_topp_noscale":
+        from dataclasses import replace
+        wl = replace(wl, top_p=0.6, norm_topk_prob=0, routed_scaling_factor=2.5, top_k=4)
+    cfg = ref.config_of(wl)
+    x = synth.gen_x(wl, 16).numpy()
+    wr, bias = synth.gen_router(wl)
+    R = {k: v.numpy() for k, v in synth.gen_experts(wl).items()}
+    S = {k: v[0].numpy() for k, v in synth.gen_experts(wl, shared=True).items()}
+    out = ref.layer_forward(cfg, x, wr, bias, R, S)
+    y = np.zeros((16, wl.hidden))
+    for t in range(16):
+        xq, sx = _np_quant(x[t])
+        for i in range(int(out["keff"][t])):
+            e = int(out["ids"][t, i])
+            y[t] += float(out["w"][t, i]) * _dense_expert({k: v[e] for k, v in R.items()}, xq, sx)
+        y[t] += _dense_expert(S, xq, sx)
+    rms = np.sqrt((y ** 2).mean())
+    assert np.abs(out["y"] - y).max() <= 1e-9 * rms
+
+
+def test_tiny_layer_regression(ref):
+    """The oracle still gives what tests/golden/make_golden.py recorded on the tiny workload."""
+    doc = _load("tiny_layer.json")
+    wl = synth.WORKLOADS["tiny"]
+    out = ref.layer_forward(ref.config_of(wl), synth.gen_x(wl, 16), *synth.gen_router(wl),
+                            synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
+    assert out["ids"].tolist() == doc["ids"] and out["keff"].tolist() == doc["keff"]
+    np.testing.assert_allclose(out["w"], doc["w"], rtol=1e-6)
+    np.testing.assert_allclose(out["y"][:, :8], doc["y_first8"], rtol=1e-9, atol=1e-9 * doc["y_rms"])
