@@ -1,0 +1,179 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse MoE FFN layer library, libmoe.so.
+ *
+ * The layer ["MoE 路由与专家流式加载" §1 (moe: DeepSeek-V3-style sparse routing)]:
+ *   1. router: logit = x . W_router[e]; sig = sigmoid(logit); the selection
+ *      bias steers which experts are chosen but the applied gate is the
+ *      unbiased sig (noaux_tc); top-k by iterated argmax; optional adaptive
+ *      top-p; norm_topk_prob; routed_scaling_factor            (§1.1, §1.2)
+ *   2. batch-union: the experts chosen by all tokens of the batch are
+ *      deduplicated; each unique expert's weights are read once and applied
+ *      to every token routed to it                              (§1.3)
+ *   3. expert FFN: gate/up/SiLU/down on int4 group-quantised weights (64 per
+ *      group, fp32 scale per group, unsigned nibble with zero point 8) against
+ *      per-token int8 activations; int32 dot per group, then the group scale
+ *      ["colibri 开发演进实录" §2.1 (int4-gs64), §2.2 (K1/K1b integer dot)]
+ *   4. combine: gated sum of the kept experts plus the always-on shared
+ *      expert                                                   (§1.4)
+ *
+ * Conventions (every entry point):
+ *   - Tensor pointers are DEVICE pointers, allocated and owned by the caller,
+ *     16-byte aligned, row major.  The library never allocates: scratch comes
+ *     from a caller-provided device workspace of at least
+ *     moe_workspace_size(cfg, max_tokens) bytes (256-byte aligned).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work on it and return; they never
+ *     synchronise, except moe_layer_forward with MOE_FLAG_SYNC_CHECK.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns a negative MOE_ERR_* code and enqueues nothing.
+ *     moe_last_error_string() (thread-local) describes the last failure.
+ *   - Weight layout, canonical (the one a checkpoint converter writes):
+ *       w_gate, w_up [E][F][H/2] u8    s_gate, s_up [E][F][H/64] fp32
+ *       w_down       [E][H][F/2] u8    s_down       [E][H][F/64] fp32
+ *     byte j of a row holds element 2j in its low nibble and element 2j+1 in
+ *     its high nibble ["colibrì 深度拆解" §5.2 pack order]; a code u in 0..15
+ *     stands for (u - 8) * scale ["colibri 开发演进实录" §2.2].
+ *     The shared expert uses the same layout with E = 1 and F = d_ff_shared.
+ *   - Limits: H, F and Fs multiples of 64 in [64, 8192]; 1 <= E <= 512;
+ *     1 <= K <= min(E, 16); 0 <= T <= 1,000,000, and (T*(K+1) + 513) *
+ *     max(F, Fs)/16 and (T*(K+1) + 513) * H/64 below 1e9.  Inputs must be finite.
+ *   - Alignment: weight, activation and output tensors 16 bytes; index arrays,
+ *     bias and routing weights 4 bytes; the workspace 256 bytes.
+ *   - The workspace's first 256 bytes hold a device error word: zero them
+ *     once before the workspace is first used (e.g. allocate it zeroed).
+ *   - Determinism: every output is a deterministic function of the inputs
+ *     (no floating-point atomics; reductions run in a fixed order).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define MOE_OK               0
+#define MOE_ERR_ARG         -1  /* null pointer, negative count, bad flag */
+#define MOE_ERR_SHAPE       -2  /* config or size outside the limits above */
+#define MOE_ERR_ALIGN       -3  /* a pointer is not 16-byte aligned */
+#define MOE_ERR_CUDA        -4  /* a CUDA launch or runtime call failed */
+#define MOE_ERR_TIMEOUT     -5  /* a bounded device-side wait gave up */
+#define MOE_ERR_UNSUPPORTED -6  /* no device of compute capability 10.3 */
+#define MOE_ERR_WORKSPACE   -7  /* workspace missing or smaller than required */
+#define MOE_ERR_DEVICE      -8  /* a kernel found invalid data (e.g. an expert id out of range) */
+
+/* flags of moe_layer_forward */
+#define MOE_FLAG_SYNC_CHECK  1  /* synchronise the stream and report device-side errors */
+
+typedef struct moe_config {
+    int32_t hidden;                /* H */
+    int32_t n_experts;             /* E, routed experts */
+    int32_t top_k;                 /* K, experts per token (the g_topk override is a smaller K) */
+    int32_t d_ff;                  /* F, routed expert width */
+    int32_t n_shared;              /* 0 or 1 shared expert */
+    int32_t d_ff_shared;           /* Fs, shared expert width */
+    int32_t group_size;            /* must be 64 */
+    int32_t norm_topk_prob;        /* 1: renormalise the kept gates to sum 1 */
+    float routed_scaling_factor;   /* multiplies the applied gates */
+    float top_p;                   /* in (0,1): adaptive top-p; otherwise off (keff = K) */
+} moe_config;
+
+typedef struct moe_expert_weights {
+    const uint8_t *w_gate; const float *s_gate;
+    const uint8_t *w_up;   const float *s_up;
+    const uint8_t *w_down; const float *s_down;
+} moe_expert_weights;
+
+/* Optional probes of moe_expert_ffn (device pointers, each nullable), indexed
+ * by pair p in permuted order (p < offsets[E]):
+ *   acc_gate, acc_up [P][F][H/64] int32: per-group sum (u - 8) * xq
+ *   acc_down [P][H][F/64] int32:         per-group sum (u - 8) * hq
+ *   hq [P][F] int8, h_scale [P] fp32:    the quantised SiLU(gate)*up rows
+ * Writing them adds stores only; the arithmetic is the same. */
+typedef struct moe_ffn_probe {
+    int32_t *acc_gate; int32_t *acc_up; int32_t *acc_down;
+    int8_t *hq; float *h_scale;
+} moe_ffn_probe;
+
+/* Optional routing outputs of moe_layer_forward (device pointers, each
+ * nullable): ids [T][K], w [T][K], keff [T], as moe_route writes them. */
+typedef struct moe_routing {
+    int32_t *ids; float *w; int32_t *keff;
+} moe_routing;
+
+/* Bytes of device workspace every call below needs for up to max_tokens
+ * tokens.  Returns 0 for an invalid config or max_tokens < 0. */
+size_t moe_workspace_size(const moe_config *cfg, int max_tokens);
+
+/* Router ["MoE 路由与专家流式加载" §1.1, §1.2].
+ *   x [T][H] fp32, w_router [E][H] fp32, bias [E] fp32 (selection only).
+ *   ids [T][K] int32: kept experts first, in selection order (descending
+ *     sig + bias; equal scores go to the lower index) or, with top-p on, in
+ *     descending gate order; -1 in slots >= keff.
+ *   w [T][K] fp32: applied weights (0 in slots >= keff).  keff [T] int32. */
+int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
+              int T, int32_t *ids, float *w, int32_t *keff,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Batch-union ["MoE 路由与专家流式加载" §1.3] by a stable counting sort
+ * ["Colibri 是什么" §3.3].  Pairs (t, i < keff[t]) are grouped by expert:
+ *   counts [E], offsets [E+1] (exclusive prefix of counts),
+ *   tok [T*K], slot [T*K]: pair p's token and slot t*K + i, ascending token
+ *     within each expert; entries >= offsets[E] are left untouched,
+ *   uniq [E]: experts with a nonzero count, ascending; n_uniq [1].
+ * A kept slot whose id is outside [0, E) is left out of the lists, and a keff
+ * outside [0, K] is clamped; either sets the workspace's device error word,
+ * which moe_check_errors reports. */
+int moe_permute(const moe_config *cfg, const int32_t *ids, const int32_t *keff, int T,
+                int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *slot,
+                int32_t *uniq, int32_t *n_uniq,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Routed expert FFN over a permutation ["MoE 路由与专家流式加载" §1.3;
+ * "colibri 开发演进实录" §2.2].  x [T][H] fp32 is quantised per token inside.
+ * For every pair p of expert e (offsets[e] <= p < offsets[e+1]) and token
+ * t = tok[p]: y_pairs[p] = down(quant(silu(gate(x_t)) * up(x_t))); y_pairs is
+ * [T*K][H] fp32 and rows >= offsets[E] are left untouched.
+ * offsets/tok/uniq/n_uniq as moe_permute writes them.  probe nullable. */
+int moe_expert_ffn(const moe_config *cfg, const float *x, int T,
+                   const moe_expert_weights *routed, const int32_t *offsets,
+                   const int32_t *tok, const int32_t *uniq, const int32_t *n_uniq,
+                   float *y_pairs, const moe_ffn_probe *probe,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Combine ["MoE 路由与专家流式加载" §1.3, §1.4]:
+ *   y[t] = sum_{i < keff[t]} w[t][i] * y_pairs[pair(t, i)] + shared(x_t)
+ * summed in slot order, then the shared expert term (when `shared` is
+ * non-null and cfg->n_shared == 1; x is then needed, else it may be NULL).
+ * pair(t, i) is found in expert ids[t][i]'s token list (offsets, tok); a slot
+ * whose expert id is out of range or whose list lacks t adds nothing. */
+int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
+                const int32_t *keff, const float *w, const int32_t *offsets,
+                const int32_t *tok, int T, const float *x,
+                const moe_expert_weights *shared, float *y,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* The whole layer: route, batch-union, routed and shared expert FFN, combine.
+ * y [T][H] fp32.  `shared` is required when cfg->n_shared == 1 and ignored
+ * otherwise.  routing (nullable) receives the routing.  flags:
+ * MOE_FLAG_SYNC_CHECK ends the call with moe_check_errors. */
+int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float *w_router,
+                      const float *bias, const moe_expert_weights *routed,
+                      const moe_expert_weights *shared, float *y, const moe_routing *routing,
+                      void *workspace, size_t workspace_bytes, int flags, void *stream);
+
+/* Synchronises `stream`, then returns MOE_ERR_DEVICE if a kernel that used
+ * this workspace since the last check found invalid data (see moe_permute),
+ * and clears the record; MOE_OK otherwise.  Not for use inside stream capture. */
+int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Description of the last error returned on this thread ("" if none). */
+const char *moe_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -59,6 +59,75 @@ static float sigmoid32(float v)
     return 1.0f / (1.0f + expf(-v));
 }
 
+/* One token through the router; scratch arrays of E and K entries. */
+static void route_token(const moe_ref_config *c, const float *xt, const float *w_router,
+                        const float *bias, int32_t *ids, float *w, int32_t *keff, float *logits,
+                        float *sig, float *choice, unsigned char *taken, int32_t *sel, float *g)
+{
+    const int H = c->hidden, E = c->n_experts, K = c->top_k;
+    const int topp_on = c->top_p > 0.0f && c->top_p < 1.0f;
+    for (int e = 0; e < E; ++e) {
+        const float *we = w_router + (size_t)e * H;
+        float acc = 0.0f;
+        for (int h = 0; h < H; ++h) acc += xt[h] * we[h];
+        if (logits) logits[e] = acc;
+        sig[e] = sigmoid32(acc);
+        choice[e] = sig[e] + bias[e];
+    }
+
+    /* iterated argmax, excluding the experts already chosen */
+    memset(taken, 0, (size_t)E);
+    for (int k = 0; k < K; ++k) {
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            if (taken[e]) continue;
+            if (best < 0 || choice[e] > choice[best]) best = e;
+        }
+        taken[best] = 1;
+        sel[k] = best;
+        g[k] = sig[best];
+    }
+
+    int m = K;
+    if (topp_on) {
+        /* stable insertion sort by gate, descending */
+        for (int i = 1; i < K; ++i) {
+            float gv = g[i];
+            int32_t sv = sel[i];
+            int j = i;
+            while (j > 0 && g[j - 1] < gv) {
+                g[j] = g[j - 1];
+                sel[j] = sel[j - 1];
+                --j;
+            }
+            g[j] = gv;
+            sel[j] = sv;
+        }
+        float tot = 0.0f;
+        for (int i = 0; i < K; ++i) tot += g[i];
+        const float thr = c->top_p * tot;
+        float cum = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            cum += g[i];
+            if (cum >= thr) { m = i + 1; break; }
+        }
+    }
+
+    float s = 0.0f;
+    for (int i = 0; i < m; ++i) s += g[i];
+    for (int i = 0; i < K; ++i) {
+        if (i < m) {
+            float v = c->norm_topk_prob ? g[i] / s : g[i];
+            w[i] = v * c->routed_scaling_factor;
+            ids[i] = sel[i];
+        } else {
+            w[i] = 0.0f;
+            ids[i] = -1;
+        }
+    }
+    *keff = m;
+}
+
 int moe_ref_route(const moe_ref_config *c, const float *x, const float *w_router,
                   const float *bias, int T, int32_t *ids, float *w, int32_t *keff,
                   float *logits)
@@ -67,83 +136,26 @@ int moe_ref_route(const moe_ref_config *c, const float *x, const float *w_router
     if (rc) return rc;
     if (T < 0 || (T > 0 && (!x || !w_router || !bias || !ids || !w || !keff))) return -1;
     const int H = c->hidden, E = c->n_experts, K = c->top_k;
-    const int topp_on = c->top_p > 0.0f && c->top_p < 1.0f;
-
-    float *sig = (float *)malloc(sizeof(float) * E);
-    float *choice = (float *)malloc(sizeof(float) * E);
-    unsigned char *taken = (unsigned char *)malloc(E);
-    int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * K);
-    float *g = (float *)malloc(sizeof(float) * K);
-    if (!sig || !choice || !taken || !sel || !g) {
+    int err = 0;
+#pragma omp parallel reduction(| : err)
+    {
+        float *sig = (float *)malloc(sizeof(float) * E);
+        float *choice = (float *)malloc(sizeof(float) * E);
+        unsigned char *taken = (unsigned char *)malloc(E);
+        int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * K);
+        float *g = (float *)malloc(sizeof(float) * K);
+        if (!sig || !choice || !taken || !sel || !g) {
+            err = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int t = 0; t < T; ++t)
+                route_token(c, x + (size_t)t * H, w_router, bias, ids + (size_t)t * K,
+                            w + (size_t)t * K, keff + t, logits ? logits + (size_t)t * E : NULL,
+                            sig, choice, taken, sel, g);
+        }
         free(sig); free(choice); free(taken); free(sel); free(g);
-        return -3;
     }
-
-    for (int t = 0; t < T; ++t) {
-        const float *xt = x + (size_t)t * H;
-        for (int e = 0; e < E; ++e) {
-            const float *we = w_router + (size_t)e * H;
-            float acc = 0.0f;
-            for (int h = 0; h < H; ++h) acc += xt[h] * we[h];
-            if (logits) logits[(size_t)t * E + e] = acc;
-            sig[e] = sigmoid32(acc);
-            choice[e] = sig[e] + bias[e];
-        }
-
-        /* iterated argmax, excluding the experts already chosen */
-        memset(taken, 0, (size_t)E);
-        for (int k = 0; k < K; ++k) {
-            int best = -1;
-            for (int e = 0; e < E; ++e) {
-                if (taken[e]) continue;
-                if (best < 0 || choice[e] > choice[best]) best = e;
-            }
-            taken[best] = 1;
-            sel[k] = best;
-            g[k] = sig[best];
-        }
-
-        int m = K;
-        if (topp_on) {
-            /* stable insertion sort by gate, descending */
-            for (int i = 1; i < K; ++i) {
-                float gv = g[i];
-                int32_t sv = sel[i];
-                int j = i;
-                while (j > 0 && g[j - 1] < gv) {
-                    g[j] = g[j - 1];
-                    sel[j] = sel[j - 1];
-                    --j;
-                }
-                g[j] = gv;
-                sel[j] = sv;
-            }
-            float tot = 0.0f;
-            for (int i = 0; i < K; ++i) tot += g[i];
-            const float thr = c->top_p * tot;
-            float cum = 0.0f;
-            for (int i = 0; i < K; ++i) {
-                cum += g[i];
-                if (cum >= thr) { m = i + 1; break; }
-            }
-        }
-
-        float s = 0.0f;
-        for (int i = 0; i < m; ++i) s += g[i];
-        for (int i = 0; i < K; ++i) {
-            if (i < m) {
-                float v = c->norm_topk_prob ? g[i] / s : g[i];
-                w[(size_t)t * K + i] = v * c->routed_scaling_factor;
-                ids[(size_t)t * K + i] = sel[i];
-            } else {
-                w[(size_t)t * K + i] = 0.0f;
-                ids[(size_t)t * K + i] = -1;
-            }
-        }
-        keff[t] = m;
-    }
-    free(sig); free(choice); free(taken); free(sel); free(g);
-    return 0;
+    return err ? -3 : 0;
 }
 
 /* ------------------------------------------------------------------------

@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) sparse MoE FFN layer: router, batch-union, int4 x int8 expert FFN, combine.
+
+The compute lives in ``libmoe.so`` (CUDA kernels behind the C ABI of
+``include/moe.h``); this package is its thin ctypes binding.  Build the library
+with ``python -m sparse_expert_ffn_route_gb300.build``.
+"""
+from .binding import (EXPORTS, LIBRARY_PATH, MOE_ERR_ALIGN, MOE_ERR_ARG, MOE_ERR_CUDA,  # noqa: F401
+                      MOE_ERR_DEVICE, MOE_ERR_SHAPE, MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED,
+                      MOE_ERR_WORKSPACE, MOE_FLAG_SYNC_CHECK, MOE_OK, ExpertWeights, FfnProbe,
+                      MoeConfig, MoeError, Routing, alloc_workspace, last_error, load_library,
+                      moe_check_errors, moe_combine, moe_expert_ffn, moe_layer_forward,
+                      moe_permute, moe_route, moe_workspace_size)

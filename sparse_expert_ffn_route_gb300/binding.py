@@ -1,0 +1,198 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h): argument marshalling only.
+
+Every function takes CUDA torch tensors, passes their device pointers and the
+current CUDA stream to the C entry point of the same name, and raises
+``MoeError`` with the library's message on a nonzero return code.  All the
+layer's arithmetic runs in the library's kernels; there is no other code path.
+If libmoe.so is missing, loading raises ``ImportError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_ARG = -1
+MOE_ERR_SHAPE = -2
+MOE_ERR_ALIGN = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_UNSUPPORTED = -6
+MOE_ERR_WORKSPACE = -7
+MOE_ERR_DEVICE = -8
+MOE_FLAG_SYNC_CHECK = 1
+
+# every symbol include/moe.h declares
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+           "moe_layer_forward", "moe_check_errors", "moe_last_error_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__("%s failed (%d): %s" % (where, code, msg))
+        self.code = code
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("norm_topk_prob", ctypes.c_int32),
+                ("routed_scaling_factor", ctypes.c_float), ("top_p", ctypes.c_float)]
+
+    @classmethod
+    def make(cls, hidden, n_experts, top_k, d_ff, n_shared=0, d_ff_shared=0, norm_topk_prob=1,
+             routed_scaling_factor=1.0, top_p=0.0, group_size=64) -> "MoeConfig":
+        return cls(hidden, n_experts, top_k, d_ff, n_shared, d_ff_shared, group_size,
+                   norm_topk_prob, routed_scaling_factor, top_p)
+
+
+class ExpertWeights(ctypes.Structure):
+    _fields_ = [("w_gate", ctypes.c_void_p), ("s_gate", ctypes.c_void_p),
+                ("w_up", ctypes.c_void_p), ("s_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
+
+    @classmethod
+    def of(cls, d: Dict[str, torch.Tensor]) -> "ExpertWeights":
+        return cls(*[_ptr(d[k]) for k in ("w_gate", "s_gate", "w_up", "s_up", "w_down", "s_down")])
+
+
+class FfnProbe(ctypes.Structure):
+    _fields_ = [("acc_gate", ctypes.c_void_p), ("acc_up", ctypes.c_void_p),
+                ("acc_down", ctypes.c_void_p), ("hq", ctypes.c_void_p),
+                ("h_scale", ctypes.c_void_p)]
+
+
+class Routing(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("w", ctypes.c_void_p), ("keff", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library():
+    """Load libmoe.so (ImportError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY_PATH):
+        raise ImportError("libmoe.so not found at %s; build it with "
+                          "`python -m sparse_expert_ffn_route_gb300.build`" % LIBRARY_PATH)
+    L = ctypes.CDLL(LIBRARY_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.moe_workspace_size.argtypes = [vp, i32]
+    L.moe_workspace_size.restype = sz
+    L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.moe_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, i32, vp]
+    L.moe_check_errors.argtypes = [vp, sz, vp]
+    L.moe_last_error_string.argtypes = []
+    L.moe_last_error_string.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        getattr(L, name).restype = getattr(L, name).restype if name in (
+            "moe_workspace_size", "moe_last_error_string") else ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where, load_library().moe_last_error_string().decode())
+
+
+def last_error() -> str:
+    return load_library().moe_last_error_string().decode()
+
+
+def moe_workspace_size(cfg: MoeConfig, max_tokens: int) -> int:
+    return int(load_library().moe_workspace_size(ctypes.byref(cfg), max_tokens))
+
+
+def alloc_workspace(cfg: MoeConfig, max_tokens: int, device="cuda") -> torch.Tensor:
+    """Zeroed device workspace for up to ``max_tokens`` tokens (uint8 tensor)."""
+    n = moe_workspace_size(cfg, max_tokens)
+    if n == 0:
+        raise MoeError(MOE_ERR_SHAPE, "moe_workspace_size", "invalid config or token count")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_route(cfg, x, w_router, bias, ids, w, keff, workspace, stream=None):
+    T = x.shape[0]
+    _check(load_library().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), T,
+                                     _ptr(ids), _ptr(w), _ptr(keff), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "moe_route")
+
+
+def moe_permute(cfg, ids, keff, counts, offsets, tok, slot, uniq, n_uniq, workspace, stream=None):
+    T = keff.shape[0]
+    _check(load_library().moe_permute(ctypes.byref(cfg), _ptr(ids), _ptr(keff), T, _ptr(counts),
+                                       _ptr(offsets), _ptr(tok), _ptr(slot), _ptr(uniq),
+                                       _ptr(n_uniq), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "moe_permute")
+
+
+def moe_expert_ffn(cfg, x, routed: Dict[str, torch.Tensor], offsets, tok, uniq, n_uniq, y_pairs,
+                   workspace, probe: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    T = x.shape[0]
+    rw = ExpertWeights.of(routed)
+    pr = None
+    if probe is not None:
+        pr = FfnProbe(*[_ptr(probe.get(k)) for k in ("acc_gate", "acc_up", "acc_down", "hq",
+                                                       "h_scale")])
+    _check(load_library().moe_expert_ffn(ctypes.byref(cfg), _ptr(x), T, ctypes.byref(rw),
+                                          _ptr(offsets), _ptr(tok), _ptr(uniq), _ptr(n_uniq),
+                                          _ptr(y_pairs), ctypes.byref(pr) if pr else None,
+                                          _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_expert_ffn")
+
+
+def moe_combine(cfg, y_pairs, ids, keff, w, offsets, tok, y, workspace, x=None,
+                shared: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    T = keff.shape[0]
+    sw = ExpertWeights.of(shared) if shared is not None else None
+    _check(load_library().moe_combine(ctypes.byref(cfg), _ptr(y_pairs), _ptr(ids), _ptr(keff),
+                                       _ptr(w), _ptr(offsets), _ptr(tok), T, _ptr(x),
+                                       ctypes.byref(sw) if sw else None, _ptr(y),
+                                       _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_combine")
+
+
+def moe_layer_forward(cfg, x, w_router, bias, routed, shared, y, workspace, routing=None,
+                      flags: int = 0, stream=None):
+    T = x.shape[0]
+    rw = ExpertWeights.of(routed)
+    sw = ExpertWeights.of(shared) if shared is not None else None
+    ro = None
+    if routing is not None:
+        ro = Routing(_ptr(routing.get("ids")), _ptr(routing.get("w")), _ptr(routing.get("keff")))
+    _check(load_library().moe_layer_forward(ctypes.byref(cfg), _ptr(x), T, _ptr(w_router),
+                                             _ptr(bias), ctypes.byref(rw),
+                                             ctypes.byref(sw) if sw else None, _ptr(y),
+                                             ctypes.byref(ro) if ro else None, _ptr(workspace),
+                                             workspace.numel(), flags, _stream(stream)),
+           "moe_layer_forward")
+
+
+def moe_check_errors(workspace, stream=None):
+    _check(load_library().moe_check_errors(_ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_check_errors")

@@ -1,0 +1,455 @@
+// moe_api.cu -- the extern "C" entry points of libmoe.so: argument validation, workspace
+// layout and the launch sequence of each call.  See include/moe.h for the contract.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "ffn_tiles.cuh"
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok()
+{
+    g_err[0] = 0;
+    return MOE_OK;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int kMaxTokens = 1000000;
+
+int check_config(const moe_config *c)
+{
+    if (!c) return fail(MOE_ERR_ARG, "cfg is NULL");
+    if (c->group_size != kGroup) return fail(MOE_ERR_SHAPE, "group_size must be 64 (got %d)", c->group_size);
+    if (c->hidden < kGroup || c->hidden > kMaxDim || c->hidden % kGroup)
+        return fail(MOE_ERR_SHAPE, "hidden must be a multiple of 64 in [64, %d] (got %d)", kMaxDim, c->hidden);
+    if (c->n_experts < 1 || c->n_experts > kMaxExperts)
+        return fail(MOE_ERR_SHAPE, "n_experts must be in [1, %d] (got %d)", kMaxExperts, c->n_experts);
+    if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts)
+        return fail(MOE_ERR_SHAPE, "top_k must be in [1, min(n_experts, %d)] (got %d)", kMaxTopK, c->top_k);
+    if (c->d_ff < kGroup || c->d_ff > kMaxDim || c->d_ff % kGroup)
+        return fail(MOE_ERR_SHAPE, "d_ff must be a multiple of 64 in [64, %d] (got %d)", kMaxDim, c->d_ff);
+    if (c->n_shared != 0 && c->n_shared != 1)
+        return fail(MOE_ERR_SHAPE, "n_shared must be 0 or 1 (got %d)", c->n_shared);
+    if (c->n_shared && (c->d_ff_shared < kGroup || c->d_ff_shared > kMaxDim || c->d_ff_shared % kGroup))
+        return fail(MOE_ERR_SHAPE, "d_ff_shared must be a multiple of 64 in [64, %d] (got %d)", kMaxDim,
+                    c->d_ff_shared);
+    if (c->norm_topk_prob != 0 && c->norm_topk_prob != 1)
+        return fail(MOE_ERR_ARG, "norm_topk_prob must be 0 or 1 (got %d)", c->norm_topk_prob);
+    if (!(c->routed_scaling_factor == c->routed_scaling_factor) ||
+        c->routed_scaling_factor > 3.0e38f || c->routed_scaling_factor < -3.0e38f)
+        return fail(MOE_ERR_ARG, "routed_scaling_factor must be finite");
+    if (!(c->top_p == c->top_p)) return fail(MOE_ERR_ARG, "top_p must not be NaN");
+    return MOE_OK;
+}
+
+int check_tokens(int T)
+{
+    if (T < 0 || T > kMaxTokens) return fail(MOE_ERR_SHAPE, "T must be in [0, %d] (got %d)", kMaxTokens, T);
+    return MOE_OK;
+}
+
+// The FFN kernels number their tiles with int32: bound the count for the worst routing
+// (every pair in its own one-token chunk).
+int check_tile_count(const moe_config &c, int T)
+{
+    const double pairs = (double)T * c.top_k + (c.n_shared ? (double)T : 0.0) + kMaxSlots;
+    const int fm = c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff;
+    const double gu = pairs * ((fm + 15) / 16), dn = pairs * ((c.hidden + 63) / 64);
+    if (gu > 1.0e9 || dn > 1.0e9)
+        return fail(MOE_ERR_SHAPE, "T=%d is too large for this layer (tile count would exceed 1e9)", T);
+    return MOE_OK;
+}
+
+#define REQUIRE_PTR(p, a)                                                                      \
+    do {                                                                                       \
+        if (!(p)) return fail(MOE_ERR_ARG, "%s is NULL", #p);                                  \
+        if (!aligned((p), (a))) return fail(MOE_ERR_ALIGN, "%s is not %d-byte aligned", #p, (int)(a)); \
+    } while (0)
+
+int check_weights(const moe_expert_weights *w, const char *name)
+{
+    if (!w) return fail(MOE_ERR_ARG, "%s weights are NULL", name);
+    const void *p[6] = {w->w_gate, w->s_gate, w->w_up, w->s_up, w->w_down, w->s_down};
+    static const char *nm[6] = {"w_gate", "s_gate", "w_up", "s_up", "w_down", "s_down"};
+    for (int i = 0; i < 6; ++i) {
+        if (!p[i]) return fail(MOE_ERR_ARG, "%s.%s is NULL", name, nm[i]);
+        if (!aligned(p[i], 16)) return fail(MOE_ERR_ALIGN, "%s.%s is not 16-byte aligned", name, nm[i]);
+    }
+    return MOE_OK;
+}
+
+// compute capability 10.3 check, cached per device
+std::atomic<int> g_dev_ok[64];
+std::atomic<int> g_dev_sms[64];
+
+int check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(MOE_ERR_UNSUPPORTED, "no CUDA device is available");
+    }
+    int st = g_dev_ok[dev].load();
+    if (st == 0) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        st = (major == 10 && minor == 3) ? 1 : -1;
+        g_dev_sms[dev].store(sms > 0 ? sms : 1);
+        g_dev_ok[dev].store(st);
+    }
+    if (st < 0) return fail(MOE_ERR_UNSUPPORTED, "libmoe.so is built for sm_103a; device %d is not compute capability 10.3", dev);
+    return MOE_OK;
+}
+
+int check_ws(const moe_config &c, int T, void *ws, size_t bytes, WsLayout *L)
+{
+    *L = ws_layout(c, T);
+    if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "workspace is not 256-byte aligned");
+    if (bytes < L->total)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes; %zu needed for T=%d", bytes, L->total, T);
+    return MOE_OK;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+template <typename P>
+P *at(void *ws, size_t off)
+{
+    return reinterpret_cast<P *>(static_cast<char *>(ws) + off);
+}
+
+size_t logits_rows(const moe_config &c, int T)
+{
+    // max over T' <= T of S(T') * T' (monotone in T, so regions never shrink as T grows)
+    size_t best = 0;
+    const int tiles = (T + 63) / 64;
+    for (int ct = 1; ct <= tiles; ++ct) {
+        const int tp = ct * 64 < T ? ct * 64 : T;
+        const int s = router_splits(c, tp);
+        const size_t v = (size_t)s * tp;
+        if (v > best) best = v;
+        if (s == 1) {
+            if ((size_t)T > best) best = T;
+            break;
+        }
+    }
+    return best;
+}
+
+int fmax_of(const moe_config &c) { return c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff; }
+
+FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
+{
+    FfnArgs a;
+    memset(&a, 0, sizeof a);
+    a.H = c.hidden;
+    a.F = c.d_ff;
+    a.Fs = c.n_shared ? c.d_ff_shared : c.d_ff;
+    a.E = c.n_experts;
+    a.T = T;
+    a.plan = at<FfnPlan>(ws, L.plan);
+    a.xq.q = at<int8_t>(ws, L.xq);
+    a.xq.scale = at<float>(ws, L.xscale);
+    a.xq.gsum = at<int32_t>(ws, L.xgsum);
+    a.h = at<float>(ws, L.h);
+    a.hstride = fmax_of(c);
+    const double tpe = (double)T * c.top_k / c.n_experts;
+    a.tc_gu = choose_tc(groups_per_lane(c.hidden), tpe);
+    int ngd = groups_per_lane(c.d_ff);
+    if (c.n_shared && groups_per_lane(c.d_ff_shared) > ngd) ngd = groups_per_lane(c.d_ff_shared);
+    a.tc_dn = choose_tc(ngd, tpe);
+    return a;
+}
+
+}  // namespace
+
+int num_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    const int v = g_dev_sms[dev].load();
+    return v > 0 ? v : 1;
+}
+
+WsLayout ws_layout(const moe_config &c, int T)
+{
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += round_up(bytes > 0 ? bytes : 1, 256);
+        return o;
+    };
+    const size_t TK = (size_t)T * c.top_k, E = c.n_experts, H = c.hidden;
+    const size_t ns = c.n_shared ? 1 : 0;
+    L.err = take(4);
+    L.plan = take(sizeof(FfnPlan));
+    L.ids = take(TK * 4);
+    L.w = take(TK * 4);
+    L.keff = take((size_t)T * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.tok = take(TK * 4);
+    L.slot = take(TK * 4);
+    L.uniq = take(E * 4);
+    L.n_uniq = take(4);
+    L.logits = take(E * 4 * logits_rows(c, T));
+    L.xq = take((size_t)T * H);
+    L.xscale = take((size_t)T * 4);
+    L.xgsum = take((size_t)T * (H / kGroup) * 4);
+    const size_t rows = (size_t)T * ns + TK;
+    L.h = take(rows * (size_t)fmax_of(c) * 4);
+    L.y = take(rows * H * 4);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config *cfg, int max_tokens)
+{
+    if (check_config(cfg) != MOE_OK) return 0;
+    if (max_tokens < 0 || max_tokens > kMaxTokens) return 0;
+    return ws_layout(*cfg, max_tokens).total;
+}
+
+const char *moe_last_error_string(void) { return g_err; }
+
+int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
+              int T, int32_t *ids, float *w, int32_t *keff, void *workspace,
+              size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(w_router, 16);
+    REQUIRE_PTR(bias, 4);
+    REQUIRE_PTR(ids, 4);
+    REQUIRE_PTR(w, 4);
+    REQUIRE_PTR(keff, 4);
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = launch_router(*cfg, x, w_router, bias, T, at<float>(workspace, L.logits), ids,
+                                  w, keff, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    return ok();
+}
+
+int moe_permute(const moe_config *cfg, const int32_t *ids, const int32_t *keff, int T,
+                int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *slot, int32_t *uniq,
+                int32_t *n_uniq, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T > 0) {
+        REQUIRE_PTR(ids, 4);
+        REQUIRE_PTR(keff, 4);
+        REQUIRE_PTR(tok, 4);
+        REQUIRE_PTR(slot, 4);
+    }
+    REQUIRE_PTR(counts, 4);
+    REQUIRE_PTR(offsets, 4);
+    REQUIRE_PTR(uniq, 4);
+    REQUIRE_PTR(n_uniq, 4);
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaError_t e = launch_permute(*cfg, ids, keff, T, counts, offsets, tok, slot, uniq, n_uniq,
+                                   at<int32_t>(workspace, L.err), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    return ok();
+}
+
+int moe_expert_ffn(const moe_config *cfg, const float *x, int T, const moe_expert_weights *routed,
+                   const int32_t *offsets, const int32_t *tok, const int32_t *uniq,
+                   const int32_t *n_uniq, float *y_pairs, const moe_ffn_probe *probe,
+                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    if ((rc = check_tile_count(*cfg, T))) return rc;
+    REQUIRE_PTR(x, 16);
+    if ((rc = check_weights(routed, "routed"))) return rc;
+    REQUIRE_PTR(offsets, 4);
+    REQUIRE_PTR(tok, 4);
+    REQUIRE_PTR(uniq, 4);
+    REQUIRE_PTR(n_uniq, 4);
+    REQUIRE_PTR(y_pairs, 16);
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    FfnArgs a = base_args(*cfg, T, workspace, L);
+    a.n_shared = 0;
+    a.include_routed = 1;
+    a.routed = *routed;
+    a.offsets = offsets;
+    a.tok = tok;
+    a.y = y_pairs;
+    a.routed_rowbase = 0;
+    if (probe) a.probe = *probe;
+    cudaError_t e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
+    if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
+    if (e == cudaSuccess) e = launch_ffn(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
+    return ok();
+}
+
+int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
+                const int32_t *keff, const float *w, const int32_t *offsets, const int32_t *tok,
+                int T, const float *x, const moe_expert_weights *shared, float *y,
+                void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    if ((rc = check_tile_count(*cfg, T))) return rc;
+    REQUIRE_PTR(y_pairs, 16);
+    REQUIRE_PTR(ids, 4);
+    REQUIRE_PTR(keff, 4);
+    REQUIRE_PTR(w, 4);
+    REQUIRE_PTR(offsets, 4);
+    REQUIRE_PTR(tok, 4);
+    REQUIRE_PTR(y, 16);
+    const bool use_shared = shared != nullptr && cfg->n_shared == 1;
+    if (use_shared) {
+        REQUIRE_PTR(x, 16);
+        if ((rc = check_weights(shared, "shared"))) return rc;
+    }
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    const float *ys = nullptr;
+    if (use_shared) {
+        FfnArgs a = base_args(*cfg, T, workspace, L);
+        a.n_shared = 1;
+        a.include_routed = 0;
+        a.shared = *shared;
+        a.y = at<float>(workspace, L.y);
+        a.routed_rowbase = T;
+        e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
+        if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
+        if (e == cudaSuccess) e = launch_ffn(a, st);
+        ys = a.y;
+    }
+    if (e == cudaSuccess)
+        e = launch_combine(*cfg, y_pairs, cfg->hidden, ys, ids, keff, w, offsets, tok, T, y, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return ok();
+}
+
+int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_ALIGN, "workspace is not 256-byte aligned");
+    if (workspace_bytes < 256) return fail(MOE_ERR_WORKSPACE, "workspace is smaller than 256 bytes");
+    int rc;
+    if ((rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t flag = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&flag, workspace, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && flag) e = cudaMemsetAsync(workspace, 0, 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "error check");
+    if (flag & kErrBadExpertId) return fail(MOE_ERR_DEVICE, "an expert id outside [0, n_experts) was skipped");
+    if (flag & kErrBadKeff) return fail(MOE_ERR_DEVICE, "a keff outside [0, top_k] was clamped");
+    if (flag) return fail(MOE_ERR_DEVICE, "device error word 0x%x", flag);
+    return ok();
+}
+
+int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float *w_router,
+                      const float *bias, const moe_expert_weights *routed,
+                      const moe_expert_weights *shared, float *y, const moe_routing *routing,
+                      void *workspace, size_t workspace_bytes, int flags, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (flags & ~MOE_FLAG_SYNC_CHECK) return fail(MOE_ERR_ARG, "unknown flags 0x%x", flags);
+    if (T == 0) return ok();
+    if ((rc = check_tile_count(*cfg, T))) return rc;
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(w_router, 16);
+    REQUIRE_PTR(bias, 4);
+    REQUIRE_PTR(y, 16);
+    if ((rc = check_weights(routed, "routed"))) return rc;
+    if (cfg->n_shared && (rc = check_weights(shared, "shared"))) return rc;
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    int32_t *ids = at<int32_t>(workspace, L.ids);
+    float *w = at<float>(workspace, L.w);
+    int32_t *keff = at<int32_t>(workspace, L.keff);
+    if (routing) {
+        if (routing->ids) { REQUIRE_PTR(routing->ids, 4); ids = routing->ids; }
+        if (routing->w) { REQUIRE_PTR(routing->w, 4); w = routing->w; }
+        if (routing->keff) { REQUIRE_PTR(routing->keff, 4); keff = routing->keff; }
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const int ns = cfg->n_shared;
+    int32_t *offsets = at<int32_t>(workspace, L.offsets);
+    int32_t *tok = at<int32_t>(workspace, L.tok);
+    int32_t *uniq = at<int32_t>(workspace, L.uniq);
+    int32_t *n_uniq = at<int32_t>(workspace, L.n_uniq);
+
+    FfnArgs a = base_args(*cfg, T, workspace, L);
+    a.n_shared = ns;
+    a.include_routed = 1;
+    a.routed = *routed;
+    if (ns) a.shared = *shared;
+    a.offsets = offsets;
+    a.tok = tok;
+    a.y = at<float>(workspace, L.y);
+    a.routed_rowbase = T * ns;
+
+    cudaError_t e = launch_router(*cfg, x, w_router, bias, T, at<float>(workspace, L.logits), ids,
+                                  w, keff, st);
+    if (e == cudaSuccess)
+        e = launch_permute(*cfg, ids, keff, T, at<int32_t>(workspace, L.counts), offsets, tok,
+                           at<int32_t>(workspace, L.slot), uniq, n_uniq,
+                           at<int32_t>(workspace, L.err), st);
+    if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
+    if (e == cudaSuccess) e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
+    if (e == cudaSuccess) e = launch_ffn(a, st);
+    if (e == cudaSuccess)
+        e = launch_combine(*cfg, a.y + (size_t)T * ns * cfg->hidden, cfg->hidden,
+                           ns ? a.y : nullptr, ids, keff, w, offsets, tok, T, y, st);
+    if (e != cudaSuccess) return cuda_fail(e, "layer launch");
+    if (flags & MOE_FLAG_SYNC_CHECK) return moe_check_errors(workspace, workspace_bytes, stream);
+    return ok();
+}
+
+}  // extern "C"

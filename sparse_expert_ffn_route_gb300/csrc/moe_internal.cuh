@@ -1,0 +1,111 @@
+// moe_internal.cuh -- internal declarations shared by the translation units of libmoe.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kGroup = 64;        // int4 group size (one fp32 scale per 64 weights)
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxSlots = kMaxExperts + 1;  // routed experts plus the shared one
+constexpr int kMaxDim = 8192;
+
+// device-side error word bits (workspace `err`)
+constexpr int kErrBadExpertId = 1;
+constexpr int kErrBadKeff = 2;
+
+// ---------------------------------------------------------------------------
+// Work plan of the grouped expert FFN.  A "slot" is one expert applied to its
+// token list: slot 0 is the shared expert when there is one, the routed
+// experts follow in ascending id.  A slot's work is cut into tiles of
+// (row block, token chunk); tiles of all slots are numbered consecutively.
+// ---------------------------------------------------------------------------
+struct FfnPlan {
+    int32_t n_slots;
+    int32_t gu_tiles;                 // total gate/up tiles
+    int32_t dn_tiles;                 // total down tiles
+    int32_t pad;
+    int32_t expert[kMaxSlots];        // expert id, -1 for the shared expert
+    int32_t ntok[kMaxSlots];          // tokens routed to the slot
+    int32_t tokbase[kMaxSlots];       // first entry of the slot's list in tok[] (routed)
+    int32_t rowbase[kMaxSlots];       // first output row of the slot
+    int32_t gu_prefix[kMaxSlots + 1]; // exclusive prefix of gate/up tiles per slot
+    int32_t dn_prefix[kMaxSlots + 1];
+};
+
+// Quantised activations: per row n int8 codes stored with each run of 8
+// elements as [e0 e2 e4 e6 | e1 e3 e5 e7] (the even/odd split that the packed
+// nibbles' low/high halves line up with), the row scale, and the sum of the
+// codes of every 64-group (for the zero-point-8 correction).
+struct QuantRows {
+    int8_t *q;       // [rows][n]
+    float *scale;    // [rows]
+    int32_t *gsum;   // [rows][n/64]
+};
+
+struct FfnArgs {
+    // problem
+    int H, F, Fs, E, T, n_shared;
+    int include_routed;               // 0: shared expert only
+    // routed and shared weights (canonical layout)
+    moe_expert_weights routed, shared;
+    // routing lists
+    const int32_t *offsets, *tok;
+    const FfnPlan *plan;
+    // activations
+    QuantRows xq;                     // [T][H]
+    float *h;                         // [rows][hstride] fp32 SiLU(gate)*up
+    int hstride;
+    float *y;                         // [rows][H] fp32 output rows
+    int tc_gu, tc_dn;                 // token chunk per tile
+    moe_ffn_probe probe;              // routed pairs only; row index = pair
+    int routed_rowbase;               // output row of routed pair 0
+};
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct WsLayout {
+    size_t ids, w, keff;              // routing (layer_forward)
+    size_t counts, offsets, tok, slot, uniq, n_uniq;
+    size_t logits;                    // router partial logits [S][T][E]
+    size_t xq, xscale, xgsum;         // quantised x
+    size_t h;                         // [rows][Fmax] fp32
+    size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
+    size_t plan;                      // FfnPlan
+    size_t err;                       // int32 device error word
+    size_t total;
+};
+
+WsLayout ws_layout(const moe_config &c, int max_tokens);
+int router_splits(const moe_config &c, int T);
+
+// ---------------------------------------------------------------------------
+// launchers (return cudaError_t of the launch)
+// ---------------------------------------------------------------------------
+cudaError_t launch_router(const moe_config &c, const float *x, const float *wr, const float *bias,
+                          int T, float *logits_part, int32_t *ids, float *w, int32_t *keff,
+                          cudaStream_t st);
+cudaError_t launch_permute(const moe_config &c, const int32_t *ids, const int32_t *keff, int T,
+                           int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *slot,
+                           int32_t *uniq, int32_t *n_uniq, int32_t *err, cudaStream_t st);
+cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_uniq,
+                        FfnPlan *plan, cudaStream_t st);
+cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride, QuantRows dst,
+                              cudaStream_t st);
+cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t st);
+cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t routed_row_stride,
+                           const float *y_shared, const int32_t *ids, const int32_t *keff,
+                           const float *w, const int32_t *offsets, const int32_t *tok, int T,
+                           float *y, cudaStream_t st);
+
+int num_sms();
+int choose_tc(int ng, double tokens_per_expert);
+int groups_per_lane(int n);
+
+}  // namespace moe

@@ -1,0 +1,98 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol that
+include/moe.h declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_expert_ffn_route_gb300 as moe
+from sparse_expert_ffn_route_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(moe.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _cfg(**kw):
+    base = dict(hidden=256, n_experts=8, top_k=2, d_ff=128, n_shared=1, d_ff_shared=128)
+    base.update(kw)
+    return moe.MoeConfig.make(**base)
+
+
+def test_workspace_size(lib):
+    cfg = _cfg()
+    sizes = [moe.moe_workspace_size(cfg, t) for t in (0, 1, 16, 64, 65, 1000, 5000)]
+    assert all(s > 0 for s in sizes) and sizes == sorted(sizes)
+    for bad in (_cfg(hidden=250), _cfg(top_k=9), _cfg(n_experts=513, top_k=2), _cfg(d_ff=100),
+                _cfg(group_size=32), _cfg(n_shared=2), _cfg(hidden=16384)):
+        assert moe.moe_workspace_size(bad, 16) == 0
+    assert moe.moe_workspace_size(cfg, -1) == 0
+
+
+FAKE = 1 << 20   # aligned, never dereferenced: validation fails before any use
+
+
+def _route(lib, cfg, x=FAKE, wr=FAKE, b=FAKE, T=4, ids=FAKE, w=FAKE, keff=FAKE, ws=FAKE,
+           nbytes=1 << 30):
+    return lib.moe_route(ctypes.byref(cfg), x, wr, b, T, ids, w, keff, ws, nbytes, None)
+
+
+def test_validation_codes(lib):
+    cfg = _cfg()
+    assert _route(lib, _cfg(hidden=100)) == moe.MOE_ERR_SHAPE
+    assert _route(lib, cfg, T=-1) == moe.MOE_ERR_SHAPE
+    assert _route(lib, cfg, x=None) == moe.MOE_ERR_ARG
+    assert "x is NULL" in moe.last_error()
+    assert _route(lib, cfg, x=FAKE + 4) == moe.MOE_ERR_ALIGN
+    assert _route(lib, cfg, ws=None) == moe.MOE_ERR_WORKSPACE
+    assert _route(lib, cfg, ws=FAKE + 16) == moe.MOE_ERR_ALIGN
+    assert _route(lib, cfg, nbytes=100) == moe.MOE_ERR_WORKSPACE
+    assert _route(lib, cfg, T=0) == moe.MOE_OK          # nothing to do, nothing enqueued
+    assert lib.moe_route(None, FAKE, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_ARG
+    rw = moe.ExpertWeights(FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    rc = lib.moe_layer_forward(ctypes.byref(cfg), FAKE, 4, FAKE, FAKE, ctypes.byref(rw),
+                               ctypes.byref(rw), FAKE, None, FAKE, 1 << 30, 0, None)
+    assert rc == moe.MOE_ERR_ARG and "s_down" in moe.last_error()
+    rw = moe.ExpertWeights(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    rc = lib.moe_layer_forward(ctypes.byref(cfg), FAKE, 4, FAKE, FAKE, ctypes.byref(rw), None,
+                               FAKE, None, FAKE, 1 << 30, 0, None)
+    assert rc == moe.MOE_ERR_ARG        # n_shared = 1 needs shared weights
+    rc = lib.moe_layer_forward(ctypes.byref(cfg), FAKE, 4, FAKE, FAKE, ctypes.byref(rw),
+                               ctypes.byref(rw), FAKE, None, FAKE, 1 << 30, 8, None)
+    assert rc == moe.MOE_ERR_ARG        # unknown flag
+    rc = lib.moe_permute(ctypes.byref(cfg), FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2,
+                         FAKE, 1 << 30, None)
+    assert rc == moe.MOE_ERR_ALIGN
+
+
+def test_no_device_is_reported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _route(lib, _cfg()) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from sparse_expert_ffn_route_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIBRARY_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        binding.load_library()

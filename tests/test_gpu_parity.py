@@ -1,0 +1,340 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Bars: selected expert ids, keff, per-expert token lists, unique lists and int32
+per-group accumulators exact; fp32 outputs within max-abs 1e-3 x RMS of the
+oracle's output.  The router's fp32 logits are summed in a different order on
+the two sides, so tokens whose routing decision sits within 1e-5 of a tie are
+counted and excluded from the exact checks (the tiny workload must have none).
+Downstream calls are fed the oracle's routing, never the other way round.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import device_experts, moe_cfg, oracle_tokens, rel_err, routing_margins
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3        # max-abs error relative to the oracle output's RMS
+TIE = 1e-5        # routing margin below which a token is a near tie
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_expert_ffn_route_gb300 as m
+    m.load_library()
+    return m
+
+
+def _inputs(wl, T, batch=0):
+    x = synth.gen_x(wl, T, batch)
+    wr, bias = synth.gen_router(wl)
+    return x, wr, bias
+
+
+def _route_both(moe, wl, T, batch=0):
+    x, wr, bias = _inputs(wl, T, batch)
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    K = wl.top_k
+    ids = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    keff = torch.empty(T, dtype=torch.int32, device="cuda")
+    moe.moe_route(cfg, x.cuda(), wr.cuda(), bias.cuda(), ids, w, keff, ws)
+    torch.cuda.synchronize()
+    ref = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)
+    margin = routing_margins(ref["logits"], bias.numpy(), K, wl.top_p)
+    return x, wr, bias, (ids.cpu().numpy(), w.cpu().numpy(), keff.cpu().numpy()), ref, margin
+
+
+def _check_routing(wl, gpu, ref, margin):
+    ids, w, keff = gpu
+    clear = margin > TIE
+    assert np.array_equal(ids[clear], ref["ids"][clear])
+    assert np.array_equal(keff[clear], ref["keff"][clear])
+    np.testing.assert_allclose(w[clear], ref["w"][clear], rtol=2e-5, atol=1e-7)
+    # near-tie tokens: the GPU's choice must still be a valid routing
+    for t in np.nonzero(~clear)[0]:
+        k = keff[t]
+        assert 1 <= k <= wl.top_k and len(set(ids[t, :k].tolist())) == k
+        assert np.all(ids[t, k:] == -1) and np.all(w[t, k:] == 0)
+    return int((~clear).sum())
+
+
+ROUTE_CASES = [("tiny", 16), ("tiny", 1), ("a3b_decode", 64), ("glm_decode", 1),
+               ("glm_decode", 32), ("wide", 8), ("wide", 512), ("prefill", 4096)]
+
+
+@pytest.mark.parametrize("name,T", ROUTE_CASES)
+def test_route(moe, name, T):
+    wl = synth.WORKLOADS[name]
+    _, _, _, gpu, ref, margin = _route_both(moe, wl, T)
+    near = _check_routing(wl, gpu, ref, margin)
+    if name == "tiny":
+        assert near == 0
+    assert near <= max(1, T // 50)
+
+
+def test_route_top_p_variants(moe):
+    from dataclasses import replace
+    base = synth.WORKLOADS["a3b_decode"]
+    for top_p, norm, scale, K in ((0.5, 1, 1.0, 8), (0.9, 0, 2.5, 6), (0.0, 1, 1.0, 16),
+                                  (0.3, 1, 1.0, 1)):
+        wl = replace(base, top_p=top_p, norm_topk_prob=norm, routed_scaling_factor=scale,
+                     top_k=K)
+        _, _, _, gpu, ref, margin = _route_both(moe, wl, 200)
+        assert _check_routing(wl, gpu, ref, margin) <= 4
+
+
+def _permute_gpu(moe, wl, ids, keff):
+    T, K, E = keff.shape[0], wl.top_k, wl.n_experts
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    d = dict(counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+             offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+             tok=torch.full((max(T * K, 1),), -7, dtype=torch.int32, device="cuda"),
+             slot=torch.full((max(T * K, 1),), -7, dtype=torch.int32, device="cuda"),
+             uniq=torch.full((E,), -7, dtype=torch.int32, device="cuda"),
+             n_uniq=torch.empty(1, dtype=torch.int32, device="cuda"))
+    moe.moe_permute(cfg, torch.from_numpy(ids).cuda(), torch.from_numpy(keff).cuda(),
+                    d["counts"], d["offsets"], d["tok"], d["slot"], d["uniq"], d["n_uniq"], ws)
+    moe.moe_check_errors(ws)
+    return {k: v.cpu().numpy() for k, v in d.items()}, ws
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 0), ("a3b_decode", 64),
+                                    ("glm_decode", 32), ("prefill", 4096), ("wide", 8192)])
+def test_permute(moe, name, T):
+    wl = synth.WORKLOADS[name]
+    x, wr, bias = _inputs(wl, max(T, 1))
+    ref_r = oracle.route(oracle.config_of(wl), x[:T], wr, bias)
+    g, _ = _permute_gpu(moe, wl, ref_r["ids"], ref_r["keff"])
+    ref = oracle.permute(oracle.config_of(wl), ref_r["ids"], ref_r["keff"])
+    P = int(ref["offsets"][-1])
+    assert np.array_equal(g["counts"], ref["counts"])
+    assert np.array_equal(g["offsets"], ref["offsets"])
+    assert np.array_equal(g["tok"][:P], ref["tok"]) and np.array_equal(g["slot"][:P], ref["slot"])
+    assert int(g["n_uniq"][0]) == ref["n_uniq"]
+    assert np.array_equal(g["uniq"][:ref["n_uniq"]], ref["uniq"])
+    if P < g["tok"].size:
+        assert np.all(g["tok"][P:] == -7)   # entries past offsets[E] untouched
+
+
+def test_permute_skewed_and_invalid(moe):
+    wl = synth.Workload("skew", 64, 16, 4, 64, 0, 0, (3000,))
+    rng = np.random.default_rng(0)
+    T, K = 3000, 4
+    ids = np.stack([rng.permutation(16)[:K] for _ in range(T)]).astype(np.int32)
+    ids[:1500, 0] = 3                     # one expert takes half the tokens first
+    for t in range(1500):
+        if 3 in ids[t, 1:]:
+            ids[t, 1:] = [e for e in rng.permutation(16) if e != 3][:K - 1]
+    keff = rng.integers(1, K + 1, T).astype(np.int32)
+    for t in range(T):
+        ids[t, keff[t]:] = -1
+    g, _ = _permute_gpu(moe, wl, ids, keff)
+    ref = oracle.permute(oracle.config_of(wl), ids, keff)
+    P = int(ref["offsets"][-1])
+    assert np.array_equal(g["offsets"], ref["offsets"])
+    assert np.array_equal(g["tok"][:P], ref["tok"]) and np.array_equal(g["slot"][:P], ref["slot"])
+    # an id out of range is skipped and reported, without a fault
+    bad = ids.copy()
+    bad[5, 0] = 99
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    dev = {k: torch.zeros(n, dtype=torch.int32, device="cuda")
+           for k, n in (("c", 16), ("o", 17), ("t", T * K), ("s", T * K), ("u", 16), ("n", 1))}
+    moe.moe_permute(cfg, torch.from_numpy(bad).cuda(), torch.from_numpy(keff).cuda(), dev["c"],
+                    dev["o"], dev["t"], dev["s"], dev["u"], dev["n"], ws)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_check_errors(ws)
+    assert ei.value.code == moe.MOE_ERR_DEVICE
+    moe.moe_check_errors(ws)   # the record is cleared
+    assert int(dev["o"][-1]) == P - 1
+
+
+def _ffn_both(moe, wl, T, batch=0, probes=True):
+    """GPU moe_expert_ffn on the oracle's routing vs the oracle, with probes."""
+    x, wr, bias = _inputs(wl, T, batch)
+    cfg_r = oracle.config_of(wl)
+    r = oracle.route(cfg_r, x, wr, bias)
+    perm = oracle.permute(cfg_r, r["ids"], r["keff"])
+    P, E, H, F = int(perm["offsets"][-1]), wl.n_experts, wl.hidden, wl.d_ff
+    R_dev = device_experts(wl)
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    y = torch.full((max(P, 1), H), float("nan"), device="cuda")
+    probe = None
+    if probes:
+        probe = dict(acc_gate=torch.zeros(P, F, H // 64, dtype=torch.int32, device="cuda"),
+                     acc_up=torch.zeros(P, F, H // 64, dtype=torch.int32, device="cuda"),
+                     acc_down=torch.zeros(P, H, F // 64, dtype=torch.int32, device="cuda"),
+                     hq=torch.zeros(P, F, dtype=torch.int8, device="cuda"),
+                     h_scale=torch.zeros(P, dtype=torch.float32, device="cuda"))
+    moe.moe_expert_ffn(cfg, x.cuda(), R_dev, torch.from_numpy(perm["offsets"]).cuda(),
+                       torch.from_numpy(perm["tok"]).cuda(),
+                       torch.from_numpy(np.pad(perm["uniq"], (0, E - perm["n_uniq"]))).cuda(),
+                       torch.tensor([perm["n_uniq"]], dtype=torch.int32, device="cuda"), y, ws,
+                       probe=probe)
+    torch.cuda.synchronize()
+    R_host = {k: v.numpy() for k, v in synth.gen_experts(wl).items()}
+    ref = oracle.expert_ffn(cfg_r, x, R_host, perm["offsets"], perm["tok"], probes=probes)
+    g = {k: v.cpu().numpy() for k, v in (probe or {}).items()}
+    g["y"] = y[:P].cpu().numpy()
+    return g, ref, perm
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 3), ("a3b_decode", 64)])
+def test_expert_ffn_exact_accumulators(moe, name, T):
+    wl = synth.WORKLOADS[name]
+    g, ref, perm = _ffn_both(moe, wl, T)
+    assert np.array_equal(g["acc_gate"], ref["acc_gate"])
+    assert np.array_equal(g["acc_up"], ref["acc_up"])
+    # h is fp32 on both sides but summed in a different order: a code may move by one step
+    # at a rounding boundary.  Rows with identical codes must give identical down accumulators.
+    same = np.all(g["hq"] == ref["hq"], axis=1)
+    diff = np.abs(g["hq"].astype(np.int32) - ref["hq"].astype(np.int32))
+    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
+    assert same.mean() > 0.9
+    assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
+    np.testing.assert_allclose(g["h_scale"], ref["hs"], rtol=1e-5)
+    assert rel_err(g["y"], ref["y_pairs"]) <= TOL
+
+
+def test_expert_ffn_glm_full_width(moe):
+    """Full GLM-decode widths (H=6144, F=2048) at T=4: exact gate/up accumulators."""
+    wl = synth.WORKLOADS["glm_decode"]
+    g, ref, _ = _ffn_both(moe, wl, 4)
+    assert np.array_equal(g["acc_gate"], ref["acc_gate"])
+    assert np.array_equal(g["acc_up"], ref["acc_up"])
+    same = np.all(g["hq"] == ref["hq"], axis=1)
+    assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
+    assert rel_err(g["y"], ref["y_pairs"]) <= TOL
+
+
+def _layer_gpu(moe, wl, x, wr, bias, routing=True):
+    T, K = x.shape[0], wl.top_k
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    y = torch.full((T, wl.hidden), float("nan"), device="cuda")
+    rt = dict(ids=torch.empty(T, K, dtype=torch.int32, device="cuda"),
+              w=torch.empty(T, K, dtype=torch.float32, device="cuda"),
+              keff=torch.empty(T, dtype=torch.int32, device="cuda"))
+    moe.moe_layer_forward(cfg, x.cuda(), wr.cuda(), bias.cuda(), device_experts(wl),
+                          device_experts(wl, shared=True) if wl.n_shared else None, y, ws,
+                          routing=rt, flags=moe.MOE_FLAG_SYNC_CHECK)
+    return y.cpu().numpy(), {k: v.cpu().numpy() for k, v in rt.items()}
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("a3b_decode", 64)])
+def test_layer_forward(moe, name, T):
+    wl = synth.WORKLOADS[name]
+    x, wr, bias = _inputs(wl, T)
+    y, rt = _layer_gpu(moe, wl, x, wr, bias)
+    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
+                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
+    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
+    clear = routing_margins(logits, bias.numpy(), wl.top_k, wl.top_p) > TIE
+    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
+    assert np.isfinite(y).all()
+    assert rel_err(y[clear], ref["y"][clear]) <= TOL
+
+
+@pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 32, [0, 13, 31]),
+                                           ("wide", 64, [0, 40]), ("prefill", 4096, [0, 2047, 4095])])
+def test_layer_forward_full_size_sampled(moe, name, T, sample):
+    """Full-size layer through moe_layer_forward (the call the benchmark times); routing of
+    every token against the oracle, outputs of sampled tokens against the oracle run on just
+    the experts those tokens use."""
+    wl = synth.WORKLOADS[name]
+    x, wr, bias = _inputs(wl, T)
+    y, rt = _layer_gpu(moe, wl, x, wr, bias)
+    assert np.isfinite(y).all()
+    ref = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)
+    margin = routing_margins(ref["logits"], bias.numpy(), wl.top_k, wl.top_p)
+    _check_routing(wl, (rt["ids"], rt["w"], rt["keff"]), ref, margin)
+    rows = [t for t in sample if margin[t] > TIE]
+    assert rows
+    yref = oracle_tokens(wl, x.numpy()[rows], ref["ids"][rows], ref["w"][rows], ref["keff"][rows])
+    assert rel_err(y[rows], yref) <= TOL
+
+
+def test_combine_with_shared(moe):
+    wl = synth.WORKLOADS["tiny"]
+    T = 16
+    x, wr, bias = _inputs(wl, T)
+    cfg_r = oracle.config_of(wl)
+    r = oracle.route(cfg_r, x, wr, bias)
+    perm = oracle.permute(cfg_r, r["ids"], r["keff"])
+    ffn = oracle.expert_ffn(cfg_r, x, synth.gen_experts(wl), perm["offsets"], perm["tok"])
+    S = synth.gen_experts(wl, shared=True)
+    ys = oracle.shared_ffn(cfg_r, x, S)
+    ref = oracle.combine(cfg_r, ffn["y_pairs"], perm["slot"], perm["offsets"], r["w"], r["keff"], ys)
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    y = torch.empty(T, wl.hidden, device="cuda")
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    moe.moe_combine(cfg, cu(ffn["y_pairs"].astype(np.float32)), cu(r["ids"]), cu(r["keff"]),
+                    cu(r["w"]), cu(perm["offsets"]), cu(perm["tok"]), y, ws, x=x.cuda(),
+                    shared=device_experts(wl, shared=True))
+    assert rel_err(y.cpu().numpy(), ref) <= TOL
+    # without the shared expert
+    ref0 = oracle.combine(cfg_r, ffn["y_pairs"], perm["slot"], perm["offsets"], r["w"], r["keff"])
+    moe.moe_combine(cfg, cu(ffn["y_pairs"].astype(np.float32)), cu(r["ids"]), cu(r["keff"]),
+                    cu(r["w"]), cu(perm["offsets"]), cu(perm["tok"]), y, ws)
+    assert rel_err(y.cpu().numpy(), ref0) <= TOL
+
+
+EDGE = [
+    # name, H, E, K, F, ns, Fs, T, top_p, norm, scale
+    ("dense_E1", 256, 1, 1, 192, 0, 0, 33, 0.0, 1, 1.0),
+    ("H64_tiny_groups", 64, 4, 2, 64, 1, 128, 9, 0.0, 1, 1.0),
+    ("ragged_odd_groups", 704, 12, 3, 320, 1, 192, 37, 0.6, 0, 2.5),
+    ("K_equals_E", 128, 4, 4, 128, 0, 0, 10, 0.0, 1, 1.0),
+    ("one_token", 512, 64, 8, 256, 1, 256, 1, 0.7, 1, 2.5),
+    ("wide_groups", 7168, 16, 4, 192, 1, 64, 5, 0.0, 1, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: c[0])
+def test_edge_cases(moe, case):
+    name, H, E, K, F, ns, Fs, T, top_p, norm, scale = case
+    wl = synth.Workload(name, H, E, K, F, ns, Fs, (T,), norm, scale, top_p, 0.3)
+    x, wr, bias = _inputs(wl, T)
+    y, rt = _layer_gpu(moe, wl, x, wr, bias)
+    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias, synth.gen_experts(wl),
+                               synth.gen_experts(wl, shared=True) if ns else None)
+    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
+    clear = routing_margins(logits, bias.numpy(), K, top_p) > TIE
+    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
+    assert rel_err(y[clear], ref["y"][clear]) <= TOL
+    g, refp, _ = _ffn_both(moe, wl, T)
+    assert np.array_equal(g["acc_gate"], refp["acc_gate"])
+    assert np.array_equal(g["acc_up"], refp["acc_up"])
+
+
+def test_zero_tokens_and_deterministic(moe):
+    wl = synth.WORKLOADS["tiny"]
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, 16)
+    x = torch.empty(0, wl.hidden, device="cuda")
+    y = torch.empty(0, wl.hidden, device="cuda")
+    wr, bias = synth.gen_router(wl)
+    moe.moe_layer_forward(cfg, x, wr.cuda(), bias.cuda(), device_experts(wl),
+                          device_experts(wl, shared=True), y, ws, flags=moe.MOE_FLAG_SYNC_CHECK)
+    x, wr, bias = _inputs(wl, 16)
+    y1, _ = _layer_gpu(moe, wl, x, wr, bias)
+    y2, _ = _layer_gpu(moe, wl, x, wr, bias)
+    assert np.array_equal(y1, y2)
+
+
+def test_generator_identical_on_gpu(moe):
+    wl = synth.WORKLOADS["a3b_decode"]
+    d = device_experts(wl)
+    h = synth.gen_experts(wl, experts=[0, 77, 255])
+    for k in h:
+        assert torch.equal(d[k][[0, 77, 255]].cpu(), h[k])
