@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse MoE FFN layer on GB300: MoE-layer tokens/s and the expert FFN's
+HBM roofline fraction.
+
+Default workload: the decode-shaped GLM-style layer (hidden 6144, 256 routed experts, top-8,
+d_ff 2048, one shared expert d_ff 2048, routed_scaling_factor 2.5) at a batch of 32 tokens.
+A step is one moe_layer_forward call (router, batch-union, routed + shared expert FFN,
+combine) on a batch of synthetic tokens; the batches rotate over 5 seeded inputs so that
+the set of experts read changes from step to step.  Every step reads ~3.5 GB of expert
+weights, far above the 126 MB L2, so nothing is served from L2 across steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--tokens T] [--no-sweep] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU and its own
+batches (weak scaling, no collective on the data path); rank 0 prints the JSON line with
+the whole-job tokens/s over the slowest rank's time.  ``--impl reference`` times the CPU
+oracle (the slow reference program) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300 (expert-weight HBM GB/s as % of roofline in 'roofline')"
+UNIT = "tokens/s"
+N_BATCHES = 5
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# --------------------------------------------------------------------------- ranks
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while active."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- peaks
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture of this kernel (profiles/), or None
+    when the kernel's source changed since the capture."""
+    import hashlib
+    path = os.path.join(PROFILE_DIR, "%s_%s.md" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("<!-- ") and "=" in line:
+            k, v = line[5:].split("-->")[0].strip().split("=", 1)
+            vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "sparse_expert_ffn_route_gb300", "csrc", vals.get("source", ""))
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if digest != vals.get("source_sha256_16"):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------- our arm
+
+def workload_of(args) -> synth.Workload:
+    wl = synth.WORKLOADS[args.workload]
+    return wl
+
+
+def expert_bytes_gate_up(wl, shared=False):
+    F = wl.d_ff_shared if shared else wl.d_ff
+    return 2 * (F * wl.hidden // 2 + F * wl.hidden // 64 * 4)
+
+
+def expert_bytes_down(wl, shared=False):
+    F = wl.d_ff_shared if shared else wl.d_ff
+    return F * wl.hidden // 2 + F * wl.hidden // 64 * 4
+
+
+def algorithmic_bytes(wl, T, U, pairs):
+    """Bytes per layer call each stage must move at least (weights of the unique experts
+    read once, activations in, results out)."""
+    ns = wl.n_shared
+    H, F = wl.hidden, wl.d_ff
+    rows = pairs + T * ns
+    gu = U * expert_bytes_gate_up(wl) + ns * expert_bytes_gate_up(wl, True) \
+        + T * H + T * (H // 64) * 4 + rows * F * 4
+    dn = U * expert_bytes_down(wl) + ns * expert_bytes_down(wl, True) \
+        + rows * F * 4 + rows * H * 4
+    layer = U * wl.expert_bytes() + ns * wl.expert_bytes(True) + wl.n_experts * H * 4 \
+        + T * H * 4 * 2
+    return {"gate_up": gu, "down": dn, "layer": layer}
+
+
+def run_ours(args, world, rank, local):
+    import sparse_expert_ffn_route_gb300 as moe
+    from sparse_expert_ffn_route_gb300 import build as moe_build
+
+    moe_build.build()
+    moe.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload_of(args)
+    T = args.tokens or max(wl.tokens)
+    cfg = moe.MoeConfig.make(wl.hidden, wl.n_experts, wl.top_k, wl.d_ff, wl.n_shared,
+                             wl.d_ff_shared, wl.norm_topk_prob, wl.routed_scaling_factor,
+                             wl.top_p)
+    routed = synth.gen_experts(wl, device=dev)
+    shared = synth.gen_experts(wl, shared=True, device=dev) if wl.n_shared else None
+    wr, bias = synth.gen_router(wl)
+    wr, bias = wr.to(dev), bias.to(dev)
+
+    def batches(Tb):
+        xs = [synth.gen_x(wl, Tb, batch=rank * N_BATCHES + b) for b in range(N_BATCHES)]
+        return xs, [x.to(dev) for x in xs]
+
+    def routing_stats(xd, Tb, ws):
+        """(unique experts, pairs) of each batch, from the library's own router + permute."""
+        out = []
+        K, E = wl.top_k, wl.n_experts
+        ids = torch.empty(Tb, K, dtype=torch.int32, device=dev)
+        w = torch.empty(Tb, K, dtype=torch.float32, device=dev)
+        keff = torch.empty(Tb, dtype=torch.int32, device=dev)
+        bufs = [torch.empty(n, dtype=torch.int32, device=dev)
+                for n in (E, E + 1, Tb * K, Tb * K, E, 1)]
+        for x in xd:
+            moe.moe_route(cfg, x, wr, bias, ids, w, keff, ws)
+            moe.moe_permute(cfg, ids, keff, *bufs, ws)
+            out.append((int(bufs[5].item()), int(bufs[1][-1].item())))
+        return out
+
+    def time_layer(xd, Tb, ws, y, steps, flags=0):
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(steps):
+            moe.moe_layer_forward(cfg, xd[k % N_BATCHES], wr, bias, routed, shared, y, ws,
+                                  flags=flags)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1)
+
+    ws = moe.alloc_workspace(cfg, T, device=dev)
+    xh, xd = batches(T)
+    y = torch.empty(T, wl.hidden, device=dev)
+    stats = routing_stats(xd, T, ws)
+
+    for k in range(args.warmup):
+        moe.moe_layer_forward(cfg, xd[k % N_BATCHES], wr, bias, routed, shared, y, ws,
+                              flags=moe.MOE_FLAG_SYNC_CHECK if k == 0 else 0)
+    torch.cuda.synchronize()
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    with ClockSampler(gpu_index) as clk:
+        ms = time_layer(xd, T, ws, y, args.steps)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(ms, world, dev)
+    value = T * args.steps * world / (ms_max / 1e3)
+
+    # per-stage device time over a second pass of the same K steps (events between stages)
+    moe.moe_stage_times(reset=True)
+    ms_ev = time_layer(xd, T, ws, y, args.steps, flags=moe.MOE_FLAG_STAGE_EVENTS)
+    st = moe.moe_stage_times(reset=True)
+    tot_bytes = {"gate_up": 0.0, "down": 0.0, "layer": 0.0}
+    for k in range(args.steps):
+        U, P = stats[k % N_BATCHES]
+        for key, v in algorithmic_bytes(wl, T, U, P).items():
+            tot_bytes[key] += v
+    dom = max(("gate_up", "down"), key=lambda s: st[s][0])
+    peak, peak_kind = hbm_peak()
+    achieved = tot_bytes[dom] / (st[dom][0] / 1e3) / 1e9
+    traffic = recorded_traffic("ffn_" + dom, "%s_T%d" % (wl.name, T))
+    roofline = {"bound": "hbm", "kernel": "ffn_" + dom, "achieved": round(achieved, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": round(tot_bytes[dom] / args.steps),
+                "launch_ms": round(st[dom][0] / args.steps, 4),
+                "layer_frac": round(tot_bytes["layer"] / (ms / 1e3) / 1e9 / peak, 4)}
+    stages = {s: round(v[0] / args.steps, 4) for s, v in st.items()}
+    launches = sum(v[1] for v in st.values())
+
+    # end to end through the public call with host buffers: pinned x in, y out, every step
+    e2e = None
+    if world >= 1:
+        pin_x = [x.pin_memory() for x in xh]
+        pin_y = torch.empty(T, wl.hidden).pin_memory()
+        xbuf = torch.empty(T, wl.hidden, device=dev)
+        k2 = args.steps
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(k2):
+            xbuf.copy_(pin_x[k % N_BATCHES], non_blocking=True)
+            moe.moe_layer_forward(cfg, xbuf, wr, bias, routed, shared, y, ws)
+            pin_y.copy_(y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        nbytes = T * wl.hidden * 4
+        e2e = {"value": round(T * k2 * world / (ms_e2e / 1e3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+    sweep = None
+    if not args.no_sweep and rank == 0 and world == 1 and len(wl.tokens) > 1:
+        sweep = {}
+        for Tb in wl.tokens:
+            wsb = moe.alloc_workspace(cfg, Tb, device=dev)
+            _, xdb = batches(Tb)
+            yb = torch.empty(Tb, wl.hidden, device=dev)
+            sb = routing_stats(xdb, Tb, wsb)
+            steps_b = max(50, min(args.steps, 400))
+            time_layer(xdb, Tb, wsb, yb, 10)
+            msb = time_layer(xdb, Tb, wsb, yb, steps_b)
+            lb = sum(algorithmic_bytes(wl, Tb, *sb[k % N_BATCHES])["layer"] for k in range(steps_b))
+            sweep["T%d" % Tb] = {"tokens_per_s": round(Tb * steps_b / (msb / 1e3), 1),
+                                 "us_per_layer": round(msb / steps_b * 1e3, 2),
+                                 "layer_hbm_frac": round(lb / (msb / 1e3) / 1e9 / peak, 4),
+                                 "unique_experts_mean": round(float(np.mean([s[0] for s in sb])), 1)}
+            del wsb, xdb, yb
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i4xi8->i32,f32",
+        "data": "synthetic (seeded SplitMix64 inputs of the workload's shapes and distributions)",
+        "config": {"workload": "%s_T%d" % (wl.name, T), "hidden": wl.hidden,
+                   "n_experts": wl.n_experts, "top_k": wl.top_k, "d_ff": wl.d_ff,
+                   "n_shared": wl.n_shared, "d_ff_shared": wl.d_ff_shared, "tokens": T,
+                   "routed_scaling_factor": wl.routed_scaling_factor, "top_p": wl.top_p,
+                   "unique_experts_mean": round(float(np.mean([s[0] for s in stats])), 1),
+                   "batches_rotated": N_BATCHES,
+                   "l2": "inputs larger than L2: each step reads %.2f GB of expert weights"
+                         % (np.mean([algorithmic_bytes(wl, T, *s)["layer"] for s in stats]) / 1e9),
+                   "parallelism": "dp%d (replicas, no collective)" % world},
+        "roofline": roofline, "stage_ms_per_step": stages,
+        "stage_timing_overhead_ms_per_step": round((ms_ev - ms) / args.steps, 5),
+        "gpu_launches": launches, "clocks": clocks, "e2e": e2e,
+    }
+    if sweep:
+        out["sweep"] = sweep
+    return out
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_sample_run(wl, T, pairs_budget, steps=1, time_budget_s=None):
+    """Time the CPU oracle on a bounded sample of the workload: the first tokens of batch 0
+    routed by the oracle, each taken whole (its kept experts plus the shared expert) until
+    ``pairs_budget`` expert applications per step.  Returns (tokens per second, cores, text)."""
+    import oracle
+    oracle.build()
+    cfg = oracle.config_of(wl)
+    x = synth.gen_x(wl, T, batch=0).numpy()
+    wr, bias = synth.gen_router(wl)
+    r = oracle.route(cfg, x, wr, bias)
+    per_tok = r["keff"] + wl.n_shared
+    ntok = int(max(1, np.searchsorted(np.cumsum(per_tok), pairs_budget, side="right")))
+    ntok = min(ntok, T)
+    rows = list(range(ntok))
+    used = sorted({int(e) for t in rows for e in r["ids"][t, :r["keff"][t]]})
+    remap = {e: i for i, e in enumerate(used)}
+    from dataclasses import replace
+    wl_c = replace(wl, n_experts=len(used), top_k=min(wl.top_k, len(used)))
+    cfg_c = oracle.config_of(wl_c)
+    R = {k: v.numpy() for k, v in synth.gen_experts(wl, experts=used).items()}
+    S = ({k: v[0].numpy() for k, v in synth.gen_experts(wl, shared=True).items()}
+         if wl.n_shared else None)
+    ids_c = np.full((ntok, wl_c.top_k), -1, np.int32)
+    for t in rows:
+        for i in range(r["keff"][t]):
+            ids_c[t, i] = remap[int(r["ids"][t, i])]
+    keff = r["keff"][:ntok].copy()
+    w = r["w"][:ntok, :wl_c.top_k].copy()
+    xs = np.ascontiguousarray(x[:ntok])
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.route(cfg, xs, wr, bias)                        # routing of the sample
+        perm = oracle.permute(cfg_c, ids_c, keff)
+        ffn = oracle.expert_ffn(cfg_c, xs, R, perm["offsets"], perm["tok"])
+        ys = oracle.shared_ffn(cfg_c, xs, S) if S is not None else None
+        oracle.combine(cfg_c, ffn["y_pairs"], perm["slot"], perm["offsets"], w, keff, ys)
+        times.append(time.perf_counter() - t0)
+        if time_budget_s is not None and sum(times) > time_budget_s:
+            break
+    tot = sum(times)
+    text = ("oracle on the first %d token(s) of batch 0 (%d expert applications incl. shared, "
+            "full routing of those tokens), %d timed run(s)" % (ntok, int(per_tok[:ntok].sum()),
+                                                                len(times)))
+    return ntok * len(times) / tot, oracle.threads(), text, tot, len(times)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    wl = workload_of(args)
+    T = args.tokens or max(wl.tokens)
+    # size each step so that warmup + steps end within about two minutes
+    rate, cores, text, tot, n = oracle_sample_run(wl, T, pairs_budget=wl.top_k + wl.n_shared,
+                                                  steps=1)
+    per_step = tot / n
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    pairs = (wl.top_k + wl.n_shared) * max(1, int(budget / per_step))
+    oracle_sample_run(wl, T, pairs_budget=pairs, steps=max(0, args.warmup))
+    rate, cores, text, tot, n = oracle_sample_run(wl, T, pairs_budget=pairs, steps=args.steps)
+    return {"metric": METRIC, "value": round(rate, 4), "unit": UNIT, "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": round(tot / n * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "i4xi8->i32,f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "%s_T%d" % (wl.name, T), "sample": text},
+            "cpu_baseline": {"value": round(rate, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": text},
+            "e2e": {"value": round(rate, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="glm_decode", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0, help="batch size (default: the largest)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            out = run_reference(args, world, rank)
+        else:
+            out = run_ours(args, world, rank, local)
+            if out is not None and rank == 0 and world == 1 and not args.no_cpu_baseline:
+                wl = workload_of(args)
+                T = args.tokens or max(wl.tokens)
+                rate, cores, text, tot, n = oracle_sample_run(
+                    wl, T, pairs_budget=4 * (wl.top_k + wl.n_shared), steps=3, time_budget_s=20)
+                out["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores,
+                                       "kind": "oracle", "sample": text}
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

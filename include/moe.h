@@ -66,7 +66,18 @@ extern "C" {
 #define MOE_ERR_DEVICE      -8  /* a kernel found invalid data (e.g. an expert id out of range) */
 
 /* flags of moe_layer_forward */
-#define MOE_FLAG_SYNC_CHECK  1  /* synchronise the stream and report device-side errors */
+#define MOE_FLAG_SYNC_CHECK    1  /* synchronise the stream and report device-side errors */
+#define MOE_FLAG_STAGE_EVENTS  2  /* record a CUDA event pair around each stage (moe_stage_times) */
+
+/* stages of moe_layer_forward, for moe_stage_times */
+#define MOE_STAGE_ROUTER   0  /* router logits + selection (2 kernels) */
+#define MOE_STAGE_PERMUTE  1  /* batch-union counting sort (1 kernel) */
+#define MOE_STAGE_PLAN     2  /* FFN tile plan (1 kernel) */
+#define MOE_STAGE_QUANT    3  /* int8 quantisation of x (1 kernel) */
+#define MOE_STAGE_GATE_UP  4  /* expert gate/up + SiLU*up (1 kernel) */
+#define MOE_STAGE_DOWN     5  /* expert down projection (1 kernel) */
+#define MOE_STAGE_COMBINE  6  /* gated sum + shared expert (1 kernel) */
+#define MOE_N_STAGES       7
 
 typedef struct moe_config {
     int32_t hidden;                /* H */
@@ -159,7 +170,8 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
 /* The whole layer: route, batch-union, routed and shared expert FFN, combine.
  * y [T][H] fp32.  `shared` is required when cfg->n_shared == 1 and ignored
  * otherwise.  routing (nullable) receives the routing.  flags:
- * MOE_FLAG_SYNC_CHECK ends the call with moe_check_errors. */
+ * MOE_FLAG_SYNC_CHECK ends the call with moe_check_errors; MOE_FLAG_STAGE_EVENTS
+ * brackets each stage with CUDA events on `stream` (see moe_stage_times). */
 int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float *w_router,
                       const float *bias, const moe_expert_weights *routed,
                       const moe_expert_weights *shared, float *y, const moe_routing *routing,
@@ -169,6 +181,13 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
  * this workspace since the last check found invalid data (see moe_permute),
  * and clears the record; MOE_OK otherwise.  Not for use inside stream capture. */
 int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Per-stage device time of the moe_layer_forward calls made on this thread
+ * with MOE_FLAG_STAGE_EVENTS since the last reset: waits for their events,
+ * then writes the summed milliseconds ms[MOE_N_STAGES] and the number of
+ * kernel launches launches[MOE_N_STAGES] (either pointer nullable, host
+ * memory).  reset != 0 clears the sums afterwards. */
+int moe_stage_times(double *ms, long long *launches, int reset);
 
 /* Description of the last error returned on this thread ("" if none). */
 const char *moe_last_error_string(void);

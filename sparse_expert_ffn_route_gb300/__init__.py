@@ -6,7 +6,7 @@ with ``python -m sparse_expert_ffn_route_gb300.build``.
 """
 from .binding import (EXPORTS, LIBRARY_PATH, MOE_ERR_ALIGN, MOE_ERR_ARG, MOE_ERR_CUDA,  # noqa: F401
                       MOE_ERR_DEVICE, MOE_ERR_SHAPE, MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED,
-                      MOE_ERR_WORKSPACE, MOE_FLAG_SYNC_CHECK, MOE_OK, ExpertWeights, FfnProbe,
+                      MOE_ERR_WORKSPACE, MOE_FLAG_STAGE_EVENTS, MOE_FLAG_SYNC_CHECK, MOE_OK, STAGES, ExpertWeights, FfnProbe,
                       MoeConfig, MoeError, Routing, alloc_workspace, last_error, load_library,
                       moe_check_errors, moe_combine, moe_expert_ffn, moe_layer_forward,
-                      moe_permute, moe_route, moe_workspace_size)
+                      moe_permute, moe_route, moe_stage_times, moe_workspace_size)

@@ -27,10 +27,12 @@ MOE_ERR_UNSUPPORTED = -6
 MOE_ERR_WORKSPACE = -7
 MOE_ERR_DEVICE = -8
 MOE_FLAG_SYNC_CHECK = 1
+MOE_FLAG_STAGE_EVENTS = 2
+STAGES = ("router", "permute", "plan", "quant", "gate_up", "down", "combine")
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
-           "moe_layer_forward", "moe_check_errors", "moe_last_error_string")
+           "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string")
 
 
 class MoeError(RuntimeError):
@@ -94,11 +96,9 @@ def load_library():
     L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, i32, vp]
     L.moe_check_errors.argtypes = [vp, sz, vp]
+    L.moe_stage_times.argtypes = [vp, vp, i32]
     L.moe_last_error_string.argtypes = []
     L.moe_last_error_string.restype = ctypes.c_char_p
-    for name in EXPORTS:
-        getattr(L, name).restype = getattr(L, name).restype if name in (
-            "moe_workspace_size", "moe_last_error_string") else ctypes.c_int
     _lib = L
     return L
 
@@ -196,3 +196,12 @@ def moe_layer_forward(cfg, x, w_router, bias, routed, shared, y, workspace, rout
 def moe_check_errors(workspace, stream=None):
     _check(load_library().moe_check_errors(_ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_check_errors")
+
+
+def moe_stage_times(reset: bool = True):
+    """Per-stage device milliseconds and kernel launches of the layer calls made with
+    MOE_FLAG_STAGE_EVENTS on this thread since the last reset: {stage: (ms, launches)}."""
+    ms = (ctypes.c_double * len(STAGES))()
+    n = (ctypes.c_longlong * len(STAGES))()
+    _check(load_library().moe_stage_times(ms, n, 1 if reset else 0), "moe_stage_times")
+    return {name: (ms[i], int(n[i])) for i, name in enumerate(STAGES)}

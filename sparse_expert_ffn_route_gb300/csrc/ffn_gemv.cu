@@ -455,23 +455,35 @@ size_t down_smem_bytes(int tc, int fmax)
     return (size_t)tc * fmax + (size_t)tc * (fmax / kGroup) * 4 + (size_t)tc * 4;
 }
 
-cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t st)
+namespace {
+
+int down_ng(const FfnArgs &a)
 {
-    const int ng_gu = groups_per_lane(a.H);
-    int ng_dn = groups_per_lane(a.F);
-    if (a.n_shared) ng_dn = ng_dn > groups_per_lane(a.Fs) ? ng_dn : groups_per_lane(a.Fs);
-    FfnKernel gu = gu_kernel(ng_gu, a.tc_gu);
-    FfnKernel dn = dn_kernel(ng_dn, a.tc_dn);
-    if (!gu || !dn) return cudaErrorInvalidConfiguration;
+    int ng = groups_per_lane(a.F);
+    if (a.n_shared && groups_per_lane(a.Fs) > ng) ng = groups_per_lane(a.Fs);
+    return ng;
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st)
+{
+    FfnKernel gu = gu_kernel(groups_per_lane(a.H), a.tc_gu);
+    if (!gu) return cudaErrorInvalidConfiguration;
+    gu<<<grid_for(gu, 0), kFfnWarps * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st)
+{
+    FfnKernel dn = dn_kernel(down_ng(a), a.tc_dn);
+    if (!dn) return cudaErrorInvalidConfiguration;
     const size_t smem = down_smem_bytes(a.tc_dn, a.hstride);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(dn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
     }
-    gu<<<grid_for(gu, 0), kFfnWarps * 32, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     dn<<<grid_for(dn, smem), kFfnWarps * 32, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "ffn_tiles.cuh"
 #include "moe_internal.cuh"
@@ -189,6 +190,50 @@ FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
     return a;
 }
 
+// ---- per-stage CUDA-event timing (MOE_FLAG_STAGE_EVENTS) ----
+struct StageRec {
+    int stage;
+    cudaEvent_t start, stop;
+};
+
+constexpr int kStageLaunches[MOE_N_STAGES] = {2, 1, 1, 1, 1, 1, 1};
+thread_local std::vector<StageRec> t_pending;
+thread_local std::vector<cudaEvent_t> t_spare;
+thread_local double t_ms[MOE_N_STAGES];
+thread_local long long t_launches[MOE_N_STAGES];
+
+cudaEvent_t take_event()
+{
+    if (!t_spare.empty()) {
+        cudaEvent_t e = t_spare.back();
+        t_spare.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+struct StageScope {
+    // records a start event now and a stop event when finished (only when enabled)
+    StageScope(bool on, int stage, cudaStream_t st) : on_(on), st_(st)
+    {
+        rec_.stage = stage;
+        rec_.start = rec_.stop = nullptr;
+        if (on_ && (rec_.start = take_event()) != nullptr) cudaEventRecord(rec_.start, st_);
+    }
+    void finish()
+    {
+        if (!on_ || !rec_.start) return;
+        rec_.stop = take_event();
+        if (rec_.stop && cudaEventRecord(rec_.stop, st_) == cudaSuccess) t_pending.push_back(rec_);
+        on_ = false;
+    }
+    bool on_;
+    cudaStream_t st_;
+    StageRec rec_;
+};
+
 }  // namespace
 
 int num_sms()
@@ -323,7 +368,8 @@ int moe_expert_ffn(const moe_config *cfg, const float *x, int T, const moe_exper
     if (probe) a.probe = *probe;
     cudaError_t e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
     if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
-    if (e == cudaSuccess) e = launch_ffn(a, st);
+    if (e == cudaSuccess) e = launch_ffn_gate_up(a, st);
+    if (e == cudaSuccess) e = launch_ffn_down(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
     return ok();
 }
@@ -363,7 +409,8 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
         a.routed_rowbase = T;
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
-        if (e == cudaSuccess) e = launch_ffn(a, st);
+        if (e == cudaSuccess) e = launch_ffn_gate_up(a, st);
+        if (e == cudaSuccess) e = launch_ffn_down(a, st);
         ys = a.y;
     }
     if (e == cudaSuccess)
@@ -399,7 +446,7 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
 {
     int rc;
     if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
-    if (flags & ~MOE_FLAG_SYNC_CHECK) return fail(MOE_ERR_ARG, "unknown flags 0x%x", flags);
+    if (flags & ~(MOE_FLAG_SYNC_CHECK | MOE_FLAG_STAGE_EVENTS)) return fail(MOE_ERR_ARG, "unknown flags 0x%x", flags);
     if (T == 0) return ok();
     if ((rc = check_tile_count(*cfg, T))) return rc;
     REQUIRE_PTR(x, 16);
@@ -435,20 +482,75 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     a.y = at<float>(workspace, L.y);
     a.routed_rowbase = T * ns;
 
-    cudaError_t e = launch_router(*cfg, x, w_router, bias, T, at<float>(workspace, L.logits), ids,
-                                  w, keff, st);
-    if (e == cudaSuccess)
+    const bool ev = (flags & MOE_FLAG_STAGE_EVENTS) != 0;
+    cudaError_t e;
+    {
+        StageScope sc(ev, MOE_STAGE_ROUTER, st);
+        e = launch_router(*cfg, x, w_router, bias, T, at<float>(workspace, L.logits), ids, w,
+                          keff, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_PERMUTE, st);
         e = launch_permute(*cfg, ids, keff, T, at<int32_t>(workspace, L.counts), offsets, tok,
                            at<int32_t>(workspace, L.slot), uniq, n_uniq,
                            at<int32_t>(workspace, L.err), st);
-    if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
-    if (e == cudaSuccess) e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
-    if (e == cudaSuccess) e = launch_ffn(a, st);
-    if (e == cudaSuccess)
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_PLAN, st);
+        e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_QUANT, st);
+        e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_GATE_UP, st);
+        e = launch_ffn_gate_up(a, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_DOWN, st);
+        e = launch_ffn_down(a, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        StageScope sc(ev, MOE_STAGE_COMBINE, st);
         e = launch_combine(*cfg, a.y + (size_t)T * ns * cfg->hidden, cfg->hidden,
                            ns ? a.y : nullptr, ids, keff, w, offsets, tok, T, y, st);
+        sc.finish();
+    }
     if (e != cudaSuccess) return cuda_fail(e, "layer launch");
     if (flags & MOE_FLAG_SYNC_CHECK) return moe_check_errors(workspace, workspace_bytes, stream);
+    return ok();
+}
+
+int moe_stage_times(double *ms, long long *launches, int reset)
+{
+    for (const StageRec &r : t_pending) {
+        float v = 0.0f;
+        if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+            cudaEventElapsedTime(&v, r.start, r.stop) == cudaSuccess) {
+            t_ms[r.stage] += v;
+            t_launches[r.stage] += kStageLaunches[r.stage];
+        } else {
+            cudaGetLastError();
+        }
+        t_spare.push_back(r.start);
+        t_spare.push_back(r.stop);
+    }
+    t_pending.clear();
+    for (int i = 0; i < MOE_N_STAGES; ++i) {
+        if (ms) ms[i] = t_ms[i];
+        if (launches) launches[i] = t_launches[i];
+        if (reset) {
+            t_ms[i] = 0.0;
+            t_launches[i] = 0;
+        }
+    }
     return ok();
 }
 

@@ -98,7 +98,8 @@ cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_
                         FfnPlan *plan, cudaStream_t st);
 cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride, QuantRows dst,
                               cudaStream_t st);
-cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t st);
+cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);
+cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t routed_row_stride,
                            const float *y_shared, const int32_t *ids, const int32_t *keff,
                            const float *w, const int32_t *offsets, const int32_t *tok, int T,
