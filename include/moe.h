@@ -129,6 +129,28 @@ int moe_route(const moe_config *cfg, const float *x, const float *w_router, cons
               int T, int32_t *ids, float *w, int32_t *keff,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* moe_route without a workspace.  The pages have no counterpart of this entry
+ * point; it exists for callers that cannot allocate device memory themselves,
+ * e.g. a plugin inside a host engine that owns every device allocation and
+ * forbids its extensions to call cudaMalloc, or a decode loop that cannot
+ * afford the device synchronisation a cudaMalloc/cudaFree may cause.
+ *   Same arguments, results and errors as moe_route, minus the workspace.  The
+ *   router's scratch (partial logits, router_splits(T) * T * E floats) lives in
+ *   a fixed 8 MiB array in device memory that libmoe.so defines; every GPU
+ *   that loads the library holds it until the process exits.  A call whose
+ *   scratch would exceed 2,097,152 floats returns MOE_ERR_SHAPE (for E = 256
+ *   every batch up to T = 4096 fits; larger ones use moe_route with a workspace).
+ *   The call allocates nothing.  Its first call on each device looks up the
+ *   array's device address (cudaGetSymbolAddress) with that device current:
+ *   make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents; the
+ *   router overwrites every scratch entry before reading it, so nothing needs
+ *   clearing.  Calls that overlap on the GPU (other streams or host threads)
+ *   race on the array: serialise them, e.g. on one stream. */
+int moe_route_noalloc(const moe_config *cfg, const float *x, const float *w_router,
+                      const float *bias, int T, int32_t *ids, float *w, int32_t *keff,
+                      void *stream);
+
 /* Batch-union ["MoE 路由与专家流式加载" §1.3] by a stable counting sort
  * ["Colibri 是什么" §3.3].  Pairs (t, i < keff[t]) are grouped by expert:
  *   counts [E], offsets [E+1] (exclusive prefix of counts),

@@ -9,4 +9,5 @@ from .binding import (EXPORTS, LIBRARY_PATH, MOE_ERR_ALIGN, MOE_ERR_ARG, MOE_ERR
                       MOE_ERR_WORKSPACE, MOE_FLAG_STAGE_EVENTS, MOE_FLAG_SYNC_CHECK, MOE_OK, STAGES, ExpertWeights, FfnProbe,
                       MoeConfig, MoeError, Routing, alloc_workspace, last_error, load_library,
                       moe_check_errors, moe_combine, moe_expert_ffn, moe_layer_forward,
-                      moe_permute, moe_route, moe_stage_times, moe_workspace_size)
+                      moe_permute, moe_route, moe_route_noalloc, moe_stage_times,
+                      moe_workspace_size)

@@ -32,7 +32,8 @@ STAGES = ("router", "permute", "plan", "quant", "gate_up", "down", "combine")
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
-           "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string")
+           "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
+           "moe_route_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -97,6 +98,7 @@ def load_library():
     L.moe_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, i32, vp]
     L.moe_check_errors.argtypes = [vp, sz, vp]
     L.moe_stage_times.argtypes = [vp, vp, i32]
+    L.moe_route_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp]
     L.moe_last_error_string.argtypes = []
     L.moe_last_error_string.restype = ctypes.c_char_p
     _lib = L
@@ -141,6 +143,15 @@ def moe_route(cfg, x, w_router, bias, ids, w, keff, workspace, stream=None):
     _check(load_library().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), T,
                                      _ptr(ids), _ptr(w), _ptr(keff), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(cfg, x, w_router, bias, ids, w, keff, stream=None):
+    """moe_route without a workspace (the router scratch is a fixed array inside libmoe.so,
+    so the call allocates nothing); same outputs as moe_route, batches up to its limit."""
+    T = x.shape[0]
+    _check(load_library().moe_route_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(w_router),
+                                             _ptr(bias), T, _ptr(ids), _ptr(w), _ptr(keff),
+                                             _stream(stream)), "moe_route_noalloc")
 
 
 def moe_permute(cfg, ids, keff, counts, offsets, tok, slot, uniq, n_uniq, workspace, stream=None):

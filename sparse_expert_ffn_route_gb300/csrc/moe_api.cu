@@ -236,6 +236,33 @@ struct StageScope {
 
 }  // namespace
 
+int set_error(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int require_device() { return check_device(); }
+
+int validate_route_args(const moe_config *cfg, const float *x, const float *w_router,
+                        const float *bias, int T, const int32_t *ids, const float *w,
+                        const int32_t *keff)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(w_router, 16);
+    REQUIRE_PTR(bias, 4);
+    REQUIRE_PTR(ids, 4);
+    REQUIRE_PTR(w, 4);
+    REQUIRE_PTR(keff, 4);
+    return MOE_OK;
+}
+
 int num_sms()
 {
     int dev = 0;

@@ -105,6 +105,13 @@ cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t r
                            const float *w, const int32_t *offsets, const int32_t *tok, int T,
                            float *y, cudaStream_t st);
 
+// host helpers shared with the entry points outside moe_api.cu
+int set_error(int code, const char *fmt, ...);   // records the thread's last error message
+int require_device();                            // MOE_OK on a compute capability 10.3 device
+int validate_route_args(const moe_config *cfg, const float *x, const float *w_router,
+                        const float *bias, int T, const int32_t *ids, const float *w,
+                        const int32_t *keff);
+
 int num_sms();
 int choose_tc(int ng, double tokens_per_expert);
 int groups_per_lane(int n);
