@@ -170,7 +170,11 @@ def recorded_traffic(kernel: str, workload: str):
 # --------------------------------------------------------------------------- our arm
 
 def workload_of(args) -> synth.Workload:
+    from dataclasses import replace
     wl = synth.WORKLOADS[args.workload]
+    if args.n_experts:
+        # smaller expert count of the same shapes (profiling captures of a few GB)
+        wl = replace(wl, name="%s_E%d" % (wl.name, args.n_experts), n_experts=args.n_experts)
     return wl
 
 
@@ -191,9 +195,9 @@ def algorithmic_bytes(wl, T, U, pairs):
     H, F = wl.hidden, wl.d_ff
     rows = pairs + T * ns
     gu = U * expert_bytes_gate_up(wl) + ns * expert_bytes_gate_up(wl, True) \
-        + T * H + T * (H // 64) * 4 + rows * F * 4
+        + T * H + T * (H // 32) * 4 + rows * F * 4
     dn = U * expert_bytes_down(wl) + ns * expert_bytes_down(wl, True) \
-        + rows * F * 4 + rows * H * 4
+        + rows * F + rows * (F // 32) * 4 + rows * H * 4
     layer = U * wl.expert_bytes() + ns * wl.expert_bytes(True) + wl.n_experts * H * 4 \
         + T * H * 4 * 2
     return {"gate_up": gu, "down": dn, "layer": layer}
@@ -325,11 +329,15 @@ def run_ours(args, world, rank, local):
             steps_b = max(50, min(args.steps, 400))
             time_layer(xdb, Tb, wsb, yb, 10)
             msb = time_layer(xdb, Tb, wsb, yb, steps_b)
+            moe.moe_stage_times(reset=True)
+            time_layer(xdb, Tb, wsb, yb, steps_b, flags=moe.MOE_FLAG_STAGE_EVENTS)
+            stb = moe.moe_stage_times(reset=True)
             lb = sum(algorithmic_bytes(wl, Tb, *sb[k % N_BATCHES])["layer"] for k in range(steps_b))
             sweep["T%d" % Tb] = {"tokens_per_s": round(Tb * steps_b / (msb / 1e3), 1),
                                  "us_per_layer": round(msb / steps_b * 1e3, 2),
                                  "layer_hbm_frac": round(lb / (msb / 1e3) / 1e9 / peak, 4),
-                                 "unique_experts_mean": round(float(np.mean([s[0] for s in sb])), 1)}
+                                 "unique_experts_mean": round(float(np.mean([s[0] for s in sb])), 1),
+                                 "stage_us": {k: round(v[0] / steps_b * 1e3, 1) for k, v in stb.items()}}
             del wsb, xdb, yb
 
     out = {
@@ -439,6 +447,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="glm_decode", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="batch size (default: the largest)")
+    ap.add_argument("--n-experts", type=int, default=0,
+                    help="override the routed expert count (for small profiling captures)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -75,9 +75,10 @@ extern "C" {
 #define MOE_STAGE_PLAN     2  /* FFN tile plan (1 kernel) */
 #define MOE_STAGE_QUANT    3  /* int8 quantisation of x (1 kernel) */
 #define MOE_STAGE_GATE_UP  4  /* expert gate/up + SiLU*up (1 kernel) */
-#define MOE_STAGE_DOWN     5  /* expert down projection (1 kernel) */
-#define MOE_STAGE_COMBINE  6  /* gated sum + shared expert (1 kernel) */
-#define MOE_N_STAGES       7
+#define MOE_STAGE_QUANT_H  5  /* int8 quantisation of SiLU(gate)*up (1 kernel) */
+#define MOE_STAGE_DOWN     6  /* expert down projection (1 kernel) */
+#define MOE_STAGE_COMBINE  7  /* gated sum + shared expert (1 kernel) */
+#define MOE_N_STAGES       8
 
 typedef struct moe_config {
     int32_t hidden;                /* H */

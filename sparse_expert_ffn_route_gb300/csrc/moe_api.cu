@@ -76,7 +76,7 @@ int check_tile_count(const moe_config &c, int T)
 {
     const double pairs = (double)T * c.top_k + (c.n_shared ? (double)T : 0.0) + kMaxSlots;
     const int fm = c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff;
-    const double gu = pairs * ((fm + 15) / 16), dn = pairs * ((c.hidden + 63) / 64);
+    const double gu = pairs * ((fm + 7) / 8), dn = pairs * ((c.hidden + 7) / 8);
     if (gu > 1.0e9 || dn > 1.0e9)
         return fail(MOE_ERR_SHAPE, "T=%d is too large for this layer (tile count would exceed 1e9)", T);
     return MOE_OK;
@@ -167,6 +167,8 @@ size_t logits_rows(const moe_config &c, int T)
 
 int fmax_of(const moe_config &c) { return c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff; }
 
+// Fields common to every FFN call; the caller sets n_shared / include_routed / weights /
+// lists / outputs and then calls ffn_configure().
 FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
 {
     FfnArgs a;
@@ -175,19 +177,47 @@ FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
     a.F = c.d_ff;
     a.Fs = c.n_shared ? c.d_ff_shared : c.d_ff;
     a.E = c.n_experts;
+    a.K = c.top_k;
     a.T = T;
+    a.err = at<int32_t>(ws, L.err);
     a.plan = at<FfnPlan>(ws, L.plan);
     a.xq.q = at<int8_t>(ws, L.xq);
     a.xq.scale = at<float>(ws, L.xscale);
-    a.xq.gsum = at<int32_t>(ws, L.xgsum);
+    a.xq.csum = at<int32_t>(ws, L.xcsum);
+    a.xq.q_ld = c.hidden;
+    a.xq.c_ld = c.hidden / 32;
     a.h = at<float>(ws, L.h);
     a.hstride = fmax_of(c);
-    const double tpe = (double)T * c.top_k / c.n_experts;
-    a.tc_gu = choose_tc(groups_per_lane(c.hidden), tpe);
-    int ngd = groups_per_lane(c.d_ff);
-    if (c.n_shared && groups_per_lane(c.d_ff_shared) > ngd) ngd = groups_per_lane(c.d_ff_shared);
-    a.tc_dn = choose_tc(ngd, tpe);
+    a.hq.q = at<int8_t>(ws, L.hq);
+    a.hq.scale = at<float>(ws, L.hscale);
+    a.hq.csum = at<int32_t>(ws, L.hcsum);
+    a.hq.q_ld = a.hstride;
+    a.hq.c_ld = a.hstride / 32;
     return a;
+}
+
+// gate/up -> quantise h -> down, each stage optionally bracketed by events
+template <typename Scope>
+cudaError_t run_ffn(const FfnArgs &a, int T, int ns, bool routed_rows, bool ev, cudaStream_t st)
+{
+    cudaError_t e;
+    {
+        Scope sc(ev, MOE_STAGE_GATE_UP, st);
+        e = launch_ffn_gate_up(a, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        Scope sc(ev, MOE_STAGE_QUANT_H, st);
+        const int max_rows = T * ns + (routed_rows ? T * a.K : 0);
+        e = launch_quant_h(a, T * ns, a.Fs, a.F, max_rows, st);
+        sc.finish();
+    }
+    if (e == cudaSuccess) {
+        Scope sc(ev, MOE_STAGE_DOWN, st);
+        e = launch_ffn_down(a, st);
+        sc.finish();
+    }
+    return e;
 }
 
 // ---- per-stage CUDA-event timing (MOE_FLAG_STAGE_EVENTS) ----
@@ -196,7 +226,7 @@ struct StageRec {
     cudaEvent_t start, stop;
 };
 
-constexpr int kStageLaunches[MOE_N_STAGES] = {2, 1, 1, 1, 1, 1, 1};
+constexpr int kStageLaunches[MOE_N_STAGES] = {2, 1, 1, 1, 1, 1, 1, 1};
 thread_local std::vector<StageRec> t_pending;
 thread_local std::vector<cudaEvent_t> t_spare;
 thread_local double t_ms[MOE_N_STAGES];
@@ -296,9 +326,13 @@ WsLayout ws_layout(const moe_config &c, int T)
     L.logits = take(E * 4 * logits_rows(c, T));
     L.xq = take((size_t)T * H);
     L.xscale = take((size_t)T * 4);
-    L.xgsum = take((size_t)T * (H / kGroup) * 4);
+    L.xcsum = take((size_t)T * (H / 32) * 4);
     const size_t rows = (size_t)T * ns + TK;
-    L.h = take(rows * (size_t)fmax_of(c) * 4);
+    const size_t fm = (size_t)fmax_of(c);
+    L.h = take(rows * fm * 4);
+    L.hq = take(rows * fm);
+    L.hscale = take(rows * 4);
+    L.hcsum = take(rows * (fm / 32) * 4);
     L.y = take(rows * H * 4);
     L.total = off;
     return L;
@@ -393,10 +427,10 @@ int moe_expert_ffn(const moe_config *cfg, const float *x, int T, const moe_exper
     a.y = y_pairs;
     a.routed_rowbase = 0;
     if (probe) a.probe = *probe;
+    ffn_configure(a);
     cudaError_t e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
     if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
-    if (e == cudaSuccess) e = launch_ffn_gate_up(a, st);
-    if (e == cudaSuccess) e = launch_ffn_down(a, st);
+    if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 0, true, false, st);
     if (e != cudaSuccess) return cuda_fail(e, "expert FFN launch");
     return ok();
 }
@@ -434,10 +468,10 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
         a.shared = *shared;
         a.y = at<float>(workspace, L.y);
         a.routed_rowbase = T;
+        ffn_configure(a);
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
-        if (e == cudaSuccess) e = launch_ffn_gate_up(a, st);
-        if (e == cudaSuccess) e = launch_ffn_down(a, st);
+        if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 1, false, false, st);
         ys = a.y;
     }
     if (e == cudaSuccess)
@@ -508,6 +542,7 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     a.tok = tok;
     a.y = at<float>(workspace, L.y);
     a.routed_rowbase = T * ns;
+    ffn_configure(a);
 
     const bool ev = (flags & MOE_FLAG_STAGE_EVENTS) != 0;
     cudaError_t e;
@@ -534,16 +569,7 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         sc.finish();
     }
-    if (e == cudaSuccess) {
-        StageScope sc(ev, MOE_STAGE_GATE_UP, st);
-        e = launch_ffn_gate_up(a, st);
-        sc.finish();
-    }
-    if (e == cudaSuccess) {
-        StageScope sc(ev, MOE_STAGE_DOWN, st);
-        e = launch_ffn_down(a, st);
-        sc.finish();
-    }
+    if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, ns, true, ev, st);
     if (e == cudaSuccess) {
         StageScope sc(ev, MOE_STAGE_COMBINE, st);
         e = launch_combine(*cfg, a.y + (size_t)T * ns * cfg->hidden, cfg->hidden,

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "moe.h"
+#include "ffn_tiles.cuh"
 
 namespace moe {
 
@@ -27,30 +28,32 @@ constexpr int kErrBadKeff = 2;
 // ---------------------------------------------------------------------------
 struct FfnPlan {
     int32_t n_slots;
-    int32_t gu_tiles;                 // total gate/up tiles
-    int32_t dn_tiles;                 // total down tiles
+    int32_t gu_tiles;                 // total gate/up tasks
+    int32_t dn_tiles;                 // total down tasks
     int32_t pad;
     int32_t expert[kMaxSlots];        // expert id, -1 for the shared expert
     int32_t ntok[kMaxSlots];          // tokens routed to the slot
     int32_t tokbase[kMaxSlots];       // first entry of the slot's list in tok[] (routed)
     int32_t rowbase[kMaxSlots];       // first output row of the slot
-    int32_t gu_prefix[kMaxSlots + 1]; // exclusive prefix of gate/up tiles per slot
+    int32_t gu_prefix[kMaxSlots + 1]; // exclusive prefix of gate/up tasks per slot
     int32_t dn_prefix[kMaxSlots + 1];
 };
 
 // Quantised activations: per row n int8 codes stored with each run of 8
 // elements as [e0 e2 e4 e6 | e1 e3 e5 e7] (the even/odd split that the packed
 // nibbles' low/high halves line up with), the row scale, and the sum of the
-// codes of every 64-group (for the zero-point-8 correction).
+// codes of every 32-element chunk (for the zero-point-8 correction).
 struct QuantRows {
-    int8_t *q;       // [rows][n]
+    int8_t *q;       // [rows][q_ld]
     float *scale;    // [rows]
-    int32_t *gsum;   // [rows][n/64]
+    int32_t *csum;   // [rows][c_ld], c_ld >= n/32
+    int q_ld, c_ld;
 };
 
 struct FfnArgs {
     // problem
-    int H, F, Fs, E, T, n_shared;
+    int H, F, Fs, E, K, T, n_shared;
+    int32_t *err;                     // device error word (pipeline timeouts)
     int include_routed;               // 0: shared expert only
     // routed and shared weights (canonical layout)
     moe_expert_weights routed, shared;
@@ -61,8 +64,10 @@ struct FfnArgs {
     QuantRows xq;                     // [T][H]
     float *h;                         // [rows][hstride] fp32 SiLU(gate)*up
     int hstride;
+    QuantRows hq;                     // [rows][hstride] quantised h
     float *y;                         // [rows][H] fp32 output rows
-    int tc_gu, tc_dn;                 // token chunk per tile
+    int tc_gu, tc_dn;                 // token chunk per task
+    Geo geo_gu[2], geo_dn[2];         // task geometry: [0] routed experts, [1] shared expert
     moe_ffn_probe probe;              // routed pairs only; row index = pair
     int routed_rowbase;               // output row of routed pair 0
 };
@@ -74,8 +79,9 @@ struct WsLayout {
     size_t ids, w, keff;              // routing (layer_forward)
     size_t counts, offsets, tok, slot, uniq, n_uniq;
     size_t logits;                    // router partial logits [S][T][E]
-    size_t xq, xscale, xgsum;         // quantised x
+    size_t xq, xscale, xcsum;         // quantised x
     size_t h;                         // [rows][Fmax] fp32
+    size_t hq, hscale, hcsum;         // quantised h
     size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
     size_t plan;                      // FfnPlan
     size_t err;                       // int32 device error word
@@ -98,6 +104,12 @@ cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_
                         FfnPlan *plan, cudaStream_t st);
 cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride, QuantRows dst,
                               cudaStream_t st);
+// quantise the h rows of an FFN call: `first_rows` rows of n_first values, then the routed
+// pair rows (count read on the device from offsets[n_experts]) of n_rest values
+cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_rest,
+                           int max_rows, cudaStream_t st);
+// host-side choice of the FFN kernels' tile shape and pipeline depth
+void ffn_configure(FfnArgs &a);
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t routed_row_stride,
@@ -113,7 +125,5 @@ int validate_route_args(const moe_config *cfg, const float *x, const float *w_ro
                         const int32_t *keff);
 
 int num_sms();
-int choose_tc(int ng, double tokens_per_expert);
-int groups_per_lane(int n);
 
 }  // namespace moe

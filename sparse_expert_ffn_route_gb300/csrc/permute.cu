@@ -21,9 +21,10 @@ namespace moe {
 namespace {
 
 struct PlanParams {
-    int T, H, F, Fs, n_shared, include_routed;
+    int T, n_shared, include_routed;
     int rowbase_routed;   // output row of routed pair 0
     int tc_gu, tc_dn;
+    Geo geo_gu[2], geo_dn[2];   // [0] routed, [1] shared
 };
 
 // Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
@@ -70,22 +71,22 @@ __device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const i
         const int s = s0 + threadIdx.x;
         int gu = 0, dn = 0;
         if (s < nslots) {
-            int e, ntok, tokbase, rowbase, F;
+            int e, ntok, tokbase, rowbase, sh;
             if (s < ns) {
-                e = -1; ntok = pp.T; tokbase = 0; rowbase = 0; F = pp.Fs;
+                e = -1; ntok = pp.T; tokbase = 0; rowbase = 0; sh = 1;
             } else {
                 e = uniq[s - ns];
                 tokbase = offsets[e];
                 ntok = offsets[e + 1] - tokbase;
                 rowbase = pp.rowbase_routed + tokbase;
-                F = pp.F;
+                sh = 0;
             }
             plan->expert[s] = e;
             plan->ntok[s] = ntok;
             plan->tokbase[s] = tokbase;
             plan->rowbase[s] = rowbase;
-            gu = gu_tiles_of(F, pp.H, ntok, pp.tc_gu);
-            dn = dn_tiles_of(F, pp.H, ntok, pp.tc_dn);
+            gu = tasks_of(pp.geo_gu[sh], ntok, pp.tc_gu);
+            dn = tasks_of(pp.geo_dn[sh], ntok, pp.tc_dn);
         }
         int tot_gu, tot_dn;
         const int ex_gu = block_exclusive_scan(gu, &tot_gu, s_warp);
@@ -231,8 +232,17 @@ cudaError_t launch_permute(const moe_config &c, const int32_t *ids, const int32_
 cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_uniq,
                         FfnPlan *plan, cudaStream_t st)
 {
-    PlanParams pp{a.T, a.H, a.F, a.Fs, a.n_shared, a.include_routed, a.routed_rowbase, a.tc_gu,
-                  a.tc_dn};
+    PlanParams pp;
+    pp.T = a.T;
+    pp.n_shared = a.n_shared;
+    pp.include_routed = a.include_routed;
+    pp.rowbase_routed = a.routed_rowbase;
+    pp.tc_gu = a.tc_gu;
+    pp.tc_dn = a.tc_dn;
+    for (int i = 0; i < 2; ++i) {
+        pp.geo_gu[i] = a.geo_gu[i];
+        pp.geo_dn[i] = a.geo_dn[i];
+    }
     plan_kernel<<<1, 1024, 0, st>>>(pp, a.offsets, uniq, n_uniq, plan);
     return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
-// quant.cu -- per-row symmetric int8 quantisation of the layer input, done once per layer
-// and shared by every expert that reads the token ["colibri 开发演进实录" §2.2: activation
-// quantisation hoisted to the layer].  One CTA per row.
+// quant.cu -- per-row symmetric int8 quantisation: of the layer input x, done once per
+// layer and shared by every expert that reads the token ["colibri 开发演进实录" §2.2:
+// activation quantisation hoisted to the layer], and of h = SiLU(gate)*up before the down
+// projection.  One CTA per row.
 #include "device_util.cuh"
 #include "moe_internal.cuh"
 
@@ -10,14 +11,15 @@ namespace {
 
 constexpr int kQThreads = 256;
 
-__global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__restrict__ src,
-                                                               int n, int stride, QuantRows dst)
+// Quantises one row of n values (n a multiple of 32) with the whole block: codes in runs of
+// 8 stored [e0 e2 e4 e6 | e1 e3 e5 e7], the code sum of every 32-element chunk, the scale.
+// canon (nullable) receives the codes in element order.
+__device__ void quant_row_block(const float *__restrict__ v, int n, int8_t *__restrict__ q,
+                                int32_t *__restrict__ csum, float *__restrict__ scale,
+                                int8_t *__restrict__ canon, float *__restrict__ canon_scale)
 {
     __shared__ float s_max[kQThreads / 32];
-    const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const float *v = src + (size_t)row * stride;
-
     float amax = 0.0f;
     for (int i = tid * 4; i < n; i += kQThreads * 4) {
         const float4 x = *reinterpret_cast<const float4 *>(v + i);
@@ -32,7 +34,7 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
     for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
     const float inv = quant_inv(amax);
 
-    const int runs = n / 8, G = n / kGroup;
+    const int runs = n / 8;
     for (int base = 0; base < runs; base += kQThreads) {
         const int run = base + tid;
         if (base + (tid & ~31) >= runs) break;   // whole warp past the end
@@ -42,14 +44,49 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
             const float4 b = *reinterpret_cast<const float4 *>(v + run * 8 + 4);
             const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             const uint2 pk = quant_pack8(x, inv, sum);
-            *reinterpret_cast<uint2 *>(dst.q + (size_t)row * n + run * 8) = pk;
+            *reinterpret_cast<uint2 *>(q + run * 8) = pk;
+            if (canon) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) canon[run * 8 + i] = (int8_t)quant_code(x[i], inv);
+            }
         }
+        // the 4 runs of a 32-element chunk are 4 consecutive lanes
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        if ((lane & 7) == 0 && run < runs) dst.gsum[(size_t)row * G + run / 8] = sum;
+        if ((lane & 3) == 0 && run < runs) csum[run / 4] = sum;
     }
-    if (tid == 0) dst.scale[row] = quant_scale(amax);
+    if (tid == 0) {
+        *scale = quant_scale(amax);
+        if (canon_scale) *canon_scale = quant_scale(amax);
+    }
+}
+
+__global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__restrict__ src,
+                                                               int n, int stride, QuantRows dst)
+{
+    const int row = blockIdx.x;
+    quant_row_block(src + (size_t)row * stride, n, dst.q + (size_t)row * dst.q_ld,
+                    dst.csum + (size_t)row * dst.c_ld, dst.scale + row, nullptr, nullptr);
+}
+
+// h rows: [0, first) of n_first values (the shared expert), then the routed pair rows,
+// as many as *rest_count (device value; null = none), of n_rest values.
+__global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restrict__ h, int ld,
+                                                            int first, int n_first, int n_rest,
+                                                            const int32_t *rest_count,
+                                                            int routed_rowbase, QuantRows dst,
+                                                            int8_t *probe_hq, float *probe_hs)
+{
+    const int row = blockIdx.x;
+    const int rest = rest_count ? *rest_count : 0;
+    if (row >= first + rest) return;
+    const bool routed = row >= first;
+    const int n = routed ? n_rest : n_first;
+    const size_t pr = (size_t)(row - routed_rowbase);
+    quant_row_block(h + (size_t)row * ld, n, dst.q + (size_t)row * dst.q_ld,
+                    dst.csum + (size_t)row * dst.c_ld, dst.scale + row,
+                    (routed && probe_hq) ? probe_hq + pr * n : nullptr,
+                    (routed && probe_hs) ? probe_hs + pr : nullptr);
 }
 
 }  // namespace
@@ -59,6 +96,17 @@ cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride,
 {
     if (rows <= 0) return cudaSuccess;
     quant_rows_kernel<<<rows, kQThreads, 0, st>>>(src, n, src_stride, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_rest,
+                           int max_rows, cudaStream_t st)
+{
+    if (max_rows <= 0) return cudaSuccess;
+    const int32_t *rest = a.include_routed ? a.offsets + a.E : nullptr;
+    quant_h_kernel<<<max_rows, kQThreads, 0, st>>>(a.h, a.hstride, first_rows, n_first, n_rest,
+                                                    rest, a.routed_rowbase, a.hq, a.probe.hq,
+                                                    a.probe.h_scale);
     return cudaGetLastError();
 }
 

@@ -297,6 +297,8 @@ EDGE = [
     ("K_equals_E", 128, 4, 4, 128, 0, 0, 10, 0.0, 1, 1.0),
     ("one_token", 512, 64, 8, 256, 1, 256, 1, 0.7, 1, 2.5),
     ("wide_groups", 7168, 16, 4, 192, 1, 64, 5, 0.0, 1, 1.0),
+    # routed rows of 6 chunks beside shared rows of 64: one down launch serves both widths
+    ("mixed_widths", 256, 8, 2, 192, 1, 2048, 12, 0.0, 1, 1.0),
 ]
 
 
