@@ -69,16 +69,19 @@ extern "C" {
 #define MOE_FLAG_SYNC_CHECK    1  /* synchronise the stream and report device-side errors */
 #define MOE_FLAG_STAGE_EVENTS  2  /* record a CUDA event pair around each stage (moe_stage_times) */
 
-/* stages of moe_layer_forward, for moe_stage_times */
-#define MOE_STAGE_ROUTER   0  /* router logits + selection (2 kernels) */
-#define MOE_STAGE_PERMUTE  1  /* batch-union counting sort (1 kernel) */
-#define MOE_STAGE_PLAN     2  /* FFN tile plan (1 kernel) */
-#define MOE_STAGE_QUANT    3  /* int8 quantisation of x (1 kernel) */
-#define MOE_STAGE_GATE_UP  4  /* expert gate/up + SiLU*up (1 kernel) */
-#define MOE_STAGE_QUANT_H  5  /* int8 quantisation of SiLU(gate)*up (1 kernel) */
-#define MOE_STAGE_DOWN     6  /* expert down projection (1 kernel) */
-#define MOE_STAGE_COMBINE  7  /* gated sum + shared expert (1 kernel) */
-#define MOE_N_STAGES       8
+/* stages of moe_layer_forward, for moe_stage_times.  Batches of at most 64 tokens take the
+ * decode route: ROUTER also quantises x and SELECT also runs the batch-union and the FFN
+ * plan, so PERMUTE, PLAN and QUANT launch nothing; larger batches use one kernel per stage. */
+#define MOE_STAGE_ROUTER   0  /* router logits (1 kernel) */
+#define MOE_STAGE_SELECT   1  /* top-k, top-p, norm, scale (1 kernel) */
+#define MOE_STAGE_PERMUTE  2  /* batch-union counting sort */
+#define MOE_STAGE_PLAN     3  /* FFN tile plan */
+#define MOE_STAGE_QUANT    4  /* int8 quantisation of x */
+#define MOE_STAGE_GATE_UP  5  /* expert gate/up + SiLU*up (1 kernel) */
+#define MOE_STAGE_QUANT_H  6  /* int8 quantisation of SiLU(gate)*up (1 kernel) */
+#define MOE_STAGE_DOWN     7  /* expert down projection (1 kernel) */
+#define MOE_STAGE_COMBINE  8  /* gated sum + shared expert (1 kernel) */
+#define MOE_N_STAGES       9
 
 typedef struct moe_config {
     int32_t hidden;                /* H */

@@ -28,7 +28,7 @@ MOE_ERR_WORKSPACE = -7
 MOE_ERR_DEVICE = -8
 MOE_FLAG_SYNC_CHECK = 1
 MOE_FLAG_STAGE_EVENTS = 2
-STAGES = ("router", "permute", "plan", "quant", "gate_up", "quant_h", "down", "combine")
+STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", "down", "combine")
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",

@@ -1,10 +1,13 @@
 // combine.cu -- gated sum of each token's kept experts plus the shared expert
 // ["MoE 路由与专家流式加载" §1.3, §1.4]:
 //     y[t] = sum_{i < keff[t]} w[t][i] * y_e(t, i) + y_shared[t]
-// summed in slot order, then the shared term, one fp32 FMA chain per output element.
+// summed in slot order, then the shared term, one fp32 FMA chain per output element.  When
+// the down rows were sliced, y_e and y_shared are first formed from their slice planes,
+// added in slice order.
 // The pair holding (t, i) is found by binary search in expert ids[t][i]'s token list,
 // which the batch-union sorted by token.
 #include "device_util.cuh"
+#include "launch.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -17,17 +20,22 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     const float *__restrict__ y_routed, int64_t rstride, const float *__restrict__ y_shared,
     const int32_t *__restrict__ ids, const int32_t *__restrict__ keff,
     const float *__restrict__ w, const int32_t *__restrict__ offsets,
-    const int32_t *__restrict__ tok, int K, int E, int H, float *__restrict__ y)
+    const int32_t *__restrict__ tok, const int32_t *__restrict__ pair_of, int K, int E, int H,
+    int S_r, int S_s, int64_t plane, float *__restrict__ y)
 {
     __shared__ int s_pair[kMaxTopK];
     __shared__ float s_w[kMaxTopK];
+    pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.y;
     const int k = max(0, min(K, keff[t]));
     if (threadIdx.x < k) {
         const int i = threadIdx.x;
         const int e = ids[(size_t)t * K + i];
         int pair = -1;
-        if (e >= 0 && e < E) {
+        if (pair_of) {
+            pair = pair_of[(size_t)t * K + i];
+        } else if (e >= 0 && e < E) {
             int lo = offsets[e], hi = offsets[e + 1];   // first entry >= t
             const int end = hi;
             while (lo < hi) {
@@ -46,7 +54,12 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = 0; i < k; ++i) {
         if (s_pair[i] < 0) continue;
-        const float4 v = *reinterpret_cast<const float4 *>(y_routed + (size_t)s_pair[i] * rstride + c);
+        const float *src = y_routed + (size_t)s_pair[i] * rstride + c;
+        float4 v = *reinterpret_cast<const float4 *>(src);
+        for (int s = 1; s < S_r; ++s) {
+            const float4 q = *reinterpret_cast<const float4 *>(src + s * plane);
+            v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+        }
         const float wi = s_w[i];
         acc.x = fmaf(wi, v.x, acc.x);
         acc.y = fmaf(wi, v.y, acc.y);
@@ -54,7 +67,12 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
         acc.w = fmaf(wi, v.w, acc.w);
     }
     if (y_shared) {
-        const float4 v = *reinterpret_cast<const float4 *>(y_shared + (size_t)t * H + c);
+        const float *src = y_shared + (size_t)t * H + c;
+        float4 v = *reinterpret_cast<const float4 *>(src);
+        for (int s = 1; s < S_s; ++s) {
+            const float4 q = *reinterpret_cast<const float4 *>(src + s * plane);
+            v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+        }
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     *reinterpret_cast<float4 *>(y + (size_t)t * H + c) = acc;
@@ -64,14 +82,15 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
 
 cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t routed_row_stride,
                            const float *y_shared, const int32_t *ids, const int32_t *keff,
-                           const float *w, const int32_t *offsets, const int32_t *tok, int T,
+                           const float *w, const int32_t *offsets, const int32_t *tok,
+                           const int32_t *pair_of, int S_r, int S_s, int64_t plane, int T,
                            float *y, cudaStream_t st)
 {
     if (T <= 0) return cudaSuccess;
     dim3 grid((c.hidden / 4 + kCThreads - 1) / kCThreads, T);
-    combine_kernel<<<grid, kCThreads, 0, st>>>(y_routed, routed_row_stride, y_shared, ids, keff, w,
-                                               offsets, tok, c.top_k, c.n_experts, c.hidden, y);
-    return cudaGetLastError();
+    return launch_kernel(combine_kernel, grid, dim3(kCThreads), 0, st, 1, y_routed,
+                         (int64_t)routed_row_stride, y_shared, ids, keff, w, offsets, tok, pair_of, c.top_k,
+                         c.n_experts, c.hidden, S_r, S_s, plane, y);
 }
 
 }  // namespace moe

@@ -150,3 +150,52 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with programmatic
+// stream serialisation, so it may be scheduled while the kernel before it in the stream is
+// still running.  Each kernel therefore calls pdl_wait() before its first access to global
+// memory (the wait returns once the previous grid has completed and its writes are
+// visible) and pdl_launch_dependents() to let the next kernel be scheduled early.
+// ---------------------------------------------------------------------------------------
+namespace moe {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------------------------------
+// cp.async (global -> shared, per thread, completion tracked per thread by commit groups).
+// With `valid` false nothing is read and the destination is zero-filled; `src` must still
+// be a mapped global address.
+// ---------------------------------------------------------------------------------------
+namespace moe {
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace moe

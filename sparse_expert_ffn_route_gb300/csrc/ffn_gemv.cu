@@ -1,7 +1,9 @@
 // ffn_gemv.cu -- host side of the grouped expert FFN: chooses the kernel variant (chunks
 // per lane, tokens per chunk, rows in flight) and the task geometry, and launches.
 #include "ffn_kernels.cuh"
+#include "launch.cuh"
 
+#include <cmath>
 #include <map>
 #include <mutex>
 
@@ -23,58 +25,59 @@ Variant variant(bool gu, int nc, int tc)
     return {};
 }
 
-// true when ptxas kept the kernel in registers (no local-memory spills)
-bool spill_free(FfnKernel k)
-{
-    static std::mutex mu;
-    static std::map<FfnKernel, bool> known;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = known.find(k);
-    if (it != known.end()) return it->second;
-    cudaFuncAttributes at{};
-    const bool ok = cudaFuncGetAttributes(&at, k) == cudaSuccess && at.localSizeBytes == 0;
-    known[k] = ok;
-    return ok;
-}
-
 struct Chosen {
     FfnKernel k;
     int ru;
+    size_t smem;
 };
 
 Chosen choose(bool gu, int nc, int tc, bool probe)
 {
     const Variant v = variant(gu, nc, tc);
-    if (!v.k1) return {nullptr, 0};
-    if (probe) return {v.kprobe, v.ru1};
-    if (spill_free(v.k2)) return {v.k2, v.ru2};
-    return {v.k1, v.ru1};
+    return {probe ? v.kprobe : v.k, v.ru, v.smem};
 }
 
 int max_nc(const Geo (&g)[2], bool both) { return both && g[1].nc > g[0].nc ? g[1].nc : g[0].nc; }
 
+// raises a kernel's dynamic shared memory limit to what its ring needs (once per kernel and
+// device)
+cudaError_t allow_smem(FfnKernel k, size_t bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, FfnKernel>, bool> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({dev, k})) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)bytes);
+    if (e == cudaSuccess) done[{dev, k}] = true;
+    return e;
+}
+
 cudaError_t launch(Chosen c, const FfnArgs &a, cudaStream_t st)
 {
     if (!c.k) return cudaErrorInvalidConfiguration;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c.k, kFfnThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    c.k<<<per_sm * num_sms(), kFfnThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e = allow_smem(c.k, c.smem);
+    if (e != cudaSuccess) return e;
+    // one CTA of 8 warps per SM (the rings take most of shared memory)
+    return launch_kernel(c.k, dim3(num_sms()), dim3(kFfnThreads), c.smem, st, 1, a);
 }
 
 bool probes_gu(const FfnArgs &a) { return a.probe.acc_gate != nullptr || a.probe.acc_up != nullptr; }
 bool probes_dn(const FfnArgs &a) { return a.probe.acc_down != nullptr; }
 
-// tokens per chunk (one pass over the expert's weights per chunk): 1 while experts see
-// about one token each, more once the batch gives each expert several, as far as the
-// activations of a chunk fit 64 registers per lane (16 warps per SM)
-int pick_tc(int nc, int T, int K, int E)
+// tokens per chunk (one pass over the expert's weights per chunk): enough for the tokens an
+// expert is expected to receive, as far as their activations fit the registers
+// (ffn_impl::tc_max) -- the routed experts' expected share T*K/U, U the expected number of
+// distinct experts under uniform routing, and with a shared expert its T tokens.
+int pick_tc(int nc, int T, int K, int E, bool shared)
 {
-    const double tpe = (double)T * K / E;
+    const double U = E * (1.0 - pow(1.0 - (double)K / E, (double)T));
+    double want = U > 0.0 ? (double)T * K / U : 1.0;
+    if (shared && T > want) want = T;
     int tc = 1;
-    while (tc < 8 && tc < tpe && nc * 8 * (tc * 2) <= 64) tc *= 2;
+    while (tc < ffn_impl::tc_max(nc) && tc < want) tc *= 2;
     return tc;
 }
 
@@ -83,19 +86,25 @@ int pick_tc(int nc, int T, int K, int E)
 void ffn_configure(FfnArgs &a)
 {
     const bool sh = a.n_shared != 0;
+    const bool small = a.T <= kRouteClusterMaxT;
+    const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;
+    const bool sgu = small && a.slice_gu && a.H > 32 * kSliceChunks;
+    const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks;
+    a.slice_gu = sgu ? 1 : 0;
+    a.slice_dn = sdn ? 1 : 0;
     // gate/up: both matrices reduce over H
-    const int ncg = make_geo(a.H, a.F, 1, false).nc;
-    a.tc_gu = pick_tc(ncg, a.T, a.K, a.E);
+    const int ncg = make_geo(a.H, a.F, 1, false, sgu).nc;
+    a.tc_gu = pick_tc(ncg, a.T, a.K, a.E, sh);
     const int ru_gu = choose(true, ncg, a.tc_gu, probes_gu(a)).ru;
-    a.geo_gu[0] = make_geo(a.H, a.F, ru_gu > 0 ? ru_gu : 1, ncg > 1);
-    a.geo_gu[1] = make_geo(a.H, a.Fs, ru_gu > 0 ? ru_gu : 1, ncg > 1);
+    a.geo_gu[0] = make_geo(a.H, a.F, ru_gu > 0 ? ru_gu : 1, ncg > 1, sgu);
+    a.geo_gu[1] = make_geo(a.H, a.Fs, ru_gu > 0 ? ru_gu : 1, ncg > 1, sgu);
     // down: the routed matrix reduces over F, the shared one over Fs
-    const int nd0 = make_geo(a.F, a.H, 1, false).nc, nd1 = make_geo(a.Fs, a.H, 1, false).nc;
+    const int nd0 = make_geo(a.F, a.H, 1, false, sdn).nc, nd1 = make_geo(a.Fs, a.H, 1, false, sdn).nc;
     const int ncd = sh && nd1 > nd0 ? nd1 : nd0;
-    a.tc_dn = pick_tc(ncd, a.T, a.K, a.E);
+    a.tc_dn = pick_tc(ncd, a.T, a.K, a.E, sh);
     const int ru_dn = choose(false, ncd, a.tc_dn, probes_dn(a)).ru;
-    a.geo_dn[0] = make_geo(a.F, a.H, ru_dn > 0 ? ru_dn : 1, ncd > 1);
-    a.geo_dn[1] = make_geo(a.Fs, a.H, ru_dn > 0 ? ru_dn : 1, ncd > 1);
+    a.geo_dn[0] = make_geo(a.F, a.H, ru_dn > 0 ? ru_dn : 1, ncd > 1, sdn);
+    a.geo_dn[1] = make_geo(a.Fs, a.H, ru_dn > 0 ? ru_dn : 1, ncd > 1, sdn);
 }
 
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st)

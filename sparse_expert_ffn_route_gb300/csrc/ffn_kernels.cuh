@@ -3,20 +3,35 @@
 // "colibri 开发演进实录" §2.2 K1: unsigned nibbles, dot(u - 8, q) = dot(u, q) - 8 * sum(q);
 // K1b: integer dot per 64-group, then the group scale].
 //
-// Work: tasks (slot, token chunk, block of rows) numbered by the planner, chunk-major within
-// a slot.  The grid is persistent; every warp owns a contiguous range of tasks and walks it,
-// so it keeps the int8 activations of its lanes' chunks in registers for as long as the
-// (expert, token chunk) stays the same.  The packed nibbles stream from HBM with 16-byte
-// read-only loads: a lane issues ru * nc loads per matrix before computing, which with 16
-// warps per SM keeps enough bytes in flight to run at the HBM roof.
+// Work: tasks (slot, token chunk, input slice, block of rows) numbered by the planner, in
+// that order of significance within a slot.  The grid is persistent (one CTA of 8 warps per
+// SM); every warp owns a contiguous range of tasks of equal summed cost (task_weight: a
+// task of a many-token chunk costs more than a one-token one) and walks it, keeping the int8
+// activations of its lanes' chunks in registers for as long as the (expert, token chunk,
+// slice) stays the same.
 //
-// In a row, lanes gl (of lpr) own the 16-byte chunks gl, gl+lpr, ... (32 codes each).  Per
-// chunk and token:
+// Weight streaming: each lane copies the 16-byte nibble chunks it will multiply (and their
+// group scales) with cp.async into its own slots of a per-warp ring of D stages in shared
+// memory, D-1 tasks ahead of the one it computes.  A lane only ever reads back what it
+// copied itself, so the ring needs no barrier: cp.async.wait_group orders it.  The bytes in
+// flight (7/8 of the ring: ~100 KB per SM) are held by shared memory, not registers, which
+// leaves the registers to the activations of up to 8 tokens.
+//
+// In a row, lanes gl (of lpr) own the 16-byte chunks gl, gl+lpr, ... (32 codes each) of the
+// task's slice.  Per chunk and token:
 //     A = -8 * sum(codes) + sum_{4 words} dp4a(w & 0x0F0F0F0F, even codes)
-//                                       + dp4a((w >> 4) & 0x0F0F0F0F, odd codes)   (int32)
+//                         + (sum_{4 words} dp4a(w & 0xF0F0F0F0, odd codes)) / 16    (int32)
 //     acc += scale[row][chunk/2] * A                                                (fp32)
-// then acc is summed over the row's lanes with shuffles.  gate/up tasks carry both matrices
-// and end with h = SiLU(sx*gate) * (sx*up); down tasks end with y = sh * acc.
+// (the high nibbles stay in place, so their products come out 16x and the division by 16
+// is exact).
+// then acc is summed over the row's lanes: with a whole warp per row, all V accumulators of
+// the task (rows x matrices x tokens) at once by a reduce-scatter (V-1 shuffles in all, lane
+// l ends with one total); with fewer lanes per row, each by a shuffle tree.  gate/up tasks
+// carry both matrices and end with h = SiLU(sx*gate) * (sx*up); down tasks end with
+// y = sh * acc.  When the rows are sliced (decode-sized batches), a task ends with its
+// slice's partial sums instead: sx*gate and sx*up into per-slice planes that the h
+// quantisation adds up in slice order, and sh*acc into the slice's plane of y that the
+// combine adds up in slice order.
 #pragma once
 
 #include "device_util.cuh"
@@ -28,31 +43,39 @@ namespace moe {
 namespace ffn_impl {
 
 struct Task {
-    int slot, sh, e, j0, nt, rowbase, r0, tokbase;
+    int slot, sh, e, j0, nt, rowbase, r0, tokbase, s;   // s: slice of the rows' inputs
 };
 
-// walks a contiguous range of tasks without a search per task; everything it does not
-// change is read from the kernel arguments (constant bank) when needed
+// Walks a contiguous range of tasks: one binary search over the slots' task prefixes at the
+// start, then a mixed-radix count (row block, slice, token chunk, slot) with no division.
 template <bool GU>
 struct Walker {
-    int slot, local, slot_tasks, nblk;
+    Task t;                    // the current task
+    int blk, nblk, rb, S, ntok, tc;
 
-    __device__ __forceinline__ const Geo &geo(const FfnArgs &a, int sh) const
+    __device__ __forceinline__ void enter(const FfnArgs &a, int s)
     {
-        return GU ? a.geo_gu[sh] : a.geo_dn[sh];
-    }
-
-    __device__ void enter(const FfnArgs &a, int s)
-    {
-        slot = s;
-        const int sh = a.plan->expert[s] < 0 ? 1 : 0;
-        const Geo &g = geo(a, sh);
+        const FfnPlan *plan = a.plan;
+        t.slot = s;
+        t.e = plan->expert[s];
+        t.sh = t.e < 0 ? 1 : 0;
+        const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+        rb = g.rb;
         nblk = (g.nrows + g.rb - 1) / g.rb;
-        slot_tasks = tasks_of(g, a.plan->ntok[s], GU ? a.tc_gu : a.tc_dn);
+        S = g.S;
+        ntok = plan->ntok[s];
+        t.tokbase = plan->tokbase[s];
+        t.rowbase = plan->rowbase[s];
+        t.j0 = 0;
+        t.s = 0;
+        t.r0 = 0;
+        blk = 0;
+        t.nt = min(tc, ntok);
     }
 
     __device__ void start(const FfnArgs &a, int task)
     {
+        tc = GU ? a.tc_gu : a.tc_dn;
         const int32_t *prefix = GU ? a.plan->gu_prefix : a.plan->dn_prefix;
         int lo = 0, hi = a.plan->n_slots;   // prefix[lo] <= task < prefix[hi]
         while (hi - lo > 1) {
@@ -61,34 +84,36 @@ struct Walker {
             else hi = mid;
         }
         enter(a, lo);
-        local = task - prefix[lo];
-    }
-
-    __device__ void next(const FfnArgs &a)
-    {
-        if (++local >= slot_tasks) {
-            int s = slot + 1;
-            enter(a, s);
-            while (slot_tasks == 0 && s + 1 < a.plan->n_slots) enter(a, ++s);
-            local = 0;
-        }
-    }
-
-    __device__ Task task(const FfnArgs &a) const
-    {
-        const FfnPlan *plan = a.plan;
-        const int tc = GU ? a.tc_gu : a.tc_dn;
-        Task t;
-        t.slot = slot;
-        t.e = plan->expert[slot];
-        t.sh = t.e < 0 ? 1 : 0;
-        const int ch = local / nblk, blk = local - ch * nblk;
+        // local index = (chunk * S + slice) * nblk + block
+        const int local = task - prefix[lo];
+        const int cs = local / nblk;
+        blk = local - cs * nblk;
+        const int ch = cs / S;
+        t.s = cs - ch * S;
         t.j0 = ch * tc;
-        t.nt = min(tc, plan->ntok[slot] - t.j0);
-        t.rowbase = plan->rowbase[slot] + t.j0;
-        t.r0 = blk * geo(a, t.sh).rb;
-        t.tokbase = plan->tokbase[slot];
-        return t;
+        t.rowbase += t.j0;
+        t.r0 = blk * rb;
+        t.nt = min(tc, ntok - t.j0);
+    }
+
+    // only called while another task of the range follows
+    __device__ __forceinline__ void next(const FfnArgs &a)
+    {
+        t.r0 += rb;
+        if (++blk < nblk) return;
+        blk = 0;
+        t.r0 = 0;
+        if (++t.s < S) return;
+        t.s = 0;
+        t.j0 += tc;
+        t.rowbase += tc;
+        if (t.j0 < ntok) {
+            t.nt = min(tc, ntok - t.j0);
+            return;
+        }
+        int s = t.slot + 1;
+        enter(a, s);
+        while (ntok == 0 && s + 1 < a.plan->n_slots) enter(a, ++s);
     }
 };
 
@@ -100,25 +125,57 @@ __device__ __forceinline__ int lpr_of(const Geo &g)
     return NC >= 2 ? 32 : g.lpr;
 }
 
-template <int NC, int TC, int RU, int N, bool GU, bool PROBE>
-__device__ __forceinline__ void run_task(const FfnArgs &a, const Task &t, const Geo &g,
-                                         const uint32_t (&act)[TC][NC][8], const int (&csum)[TC][NC],
-                                         const float (&ascale)[TC])
+// Sums each of n values (n a power of two, <= 32) over the 32 lanes: at offsets 16, 8, ...
+// a lane keeps one half of its values, sends the other half to its partner and adds what
+// it receives; once one value is left the remaining offsets add it up.  Lane l ends with the
+// total of value l >> (5 - log2 n).
+template <int n, int d>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int lane)
+    {
+        if constexpr (d > 0) {
+            if constexpr (n > 1) {
+                const bool up = (lane & d) != 0;
+#pragma unroll
+                for (int i = 0; i < n / 2; ++i) {
+                    const float send = up ? v[i] : v[i + n / 2];
+                    const float keep = up ? v[i + n / 2] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+                }
+                ReduceScatter<n / 2, d / 2>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], d);
+                ReduceScatter<1, d / 2>::run(v, lane);
+            }
+        }
+    }
+};
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
+// one lane's ring slots: [stage][u][m][c] x 32 lanes
+template <int NC, int RU, int NM>
+__device__ __forceinline__ int slot_of(int st, int u, int m, int c, int lane)
+{
+    return (((st * RU + u) * NM + m) * NC + c) * 32 + lane;
+}
+
+// Issue the copies of one task into ring stage `st` (zero-fill outside the rows / slice).
+template <int NC, int RU, bool GU>
+__device__ __forceinline__ void issue_task(const FfnArgs &a, const Task &t, int st, uint4 *wbuf,
+                                           float *sbuf)
 {
     constexpr int NM = GU ? 2 : 1;
     const int lane = threadIdx.x & 31;
+    const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
     const int lpr = lpr_of<NC>(g), rpw = 32 / lpr;
     const int sub = lane / lpr, gl = lane - sub * lpr;
-    const int nch = g.kdim / 32;
-    const bool shared = t.sh != 0;
-    const moe_expert_weights &W = shared ? a.shared : a.routed;
-    const size_t erow = shared ? 0 : (size_t)t.e * g.nrows;
+    const int cb = t.s * g.sch;
+    const int sn = min(g.sch, g.kdim / 32 - cb);
+    const moe_expert_weights &W = t.sh ? a.shared : a.routed;
+    const size_t erow = t.sh ? 0 : (size_t)t.e * g.nrows;
     const uint8_t *wm[2] = {GU ? W.w_gate : W.w_down, W.w_up};
     const float *smat[2] = {GU ? W.s_gate : W.s_down, W.s_up};
-
-    // issue every load of the task first
-    uint4 w[RU][NM][NC];
-    float sc[RU][NM][NC];
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
         const int r = t.r0 + u * rpw + sub;
@@ -126,63 +183,79 @@ __device__ __forceinline__ void run_task(const FfnArgs &a, const Task &t, const 
         const size_t row = erow + (size_t)(rv ? r : 0);
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
-            const uint8_t *wrow = wm[m] + row * g.rowbytes + (size_t)gl * 16;
-            const float *srow = smat[m] + row * g.G;
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                const int ci = gl + c * lpr;
-                if (rv && ci < nch) {
-                    w[u][m][c] = ld_stream_v4(wrow + c * lpr * 16);
-                    sc[u][m][c] = ld_stream_f32(srow + (ci >> 1));
-                } else {
-                    w[u][m][c] = make_uint4(0u, 0u, 0u, 0u);
-                    sc[u][m][c] = 0.0f;
-                }
+                const int li = gl + c * lpr;
+                const bool ok = rv && li < sn;
+                const int ci = cb + (ok ? li : 0);
+                const int k = slot_of<NC, RU, NM>(st, u, m, c, lane);
+                cp_async16(wbuf + k, wm[m] + row * g.rowbytes + (size_t)ci * 16, ok);
+                cp_async4(sbuf + k, smat[m] + row * g.G + (ci >> 1), ok);
             }
         }
     }
+}
 
+template <int NC, int TC, int RU, int N, bool GU, bool PROBE>
+__device__ __forceinline__ void run_task(const FfnArgs &a, const Task &t, const Geo &g, int st,
+                                         const uint4 *wbuf, const float *sbuf,
+                                         const uint32_t (&act)[TC][NC][8], const int (&csum8)[TC][NC],
+                                         const float (&ascale)[TC])
+{
+    constexpr int NM = GU ? 2 : 1;
+    constexpr int V = RU * N * NM;        // accumulators of the task
+    const int lane = threadIdx.x & 31;
+    const int lpr = lpr_of<NC>(g), rpw = 32 / lpr;
+    const int sub = lane / lpr, gl = lane - sub * lpr;
+    const int cb = t.s * g.sch;
+    const int sn = min(g.sch, g.kdim / 32 - cb);
+
+    // acc[o] with o = (u * N + j) * NM + m
+    float acc[V];
+#pragma unroll
+    for (int o = 0; o < V; ++o) acc[o] = 0.0f;
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
         const int r = t.r0 + u * rpw + sub;
         const bool rv = r < g.nrows;
-        float acc[NM][N];
-#pragma unroll
-        for (int m = 0; m < NM; ++m)
-#pragma unroll
-            for (int j = 0; j < N; ++j) acc[m][j] = 0.0f;
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                const int ci = gl + c * lpr;
-                const uint32_t wv[4] = {w[u][m][c].x, w[u][m][c].y, w[u][m][c].z, w[u][m][c].w};
-                int a0[N], a1[N];   // two independent chains per token
+                const int li = gl + c * lpr, ci = cb + li;
+                const int k = slot_of<NC, RU, NM>(st, u, m, c, lane);
+                const uint4 wq = wbuf[k];
+                const float sc = sbuf[k];
+                const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+                // low nibbles against the even codes, high nibbles (kept in place, i.e. 16x)
+                // against the odd codes: two chains per token, the first starting from the
+                // zero-point correction -8 * sum(codes)
+                int clo[N], chi[N];
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
-                    a0[j] = -8 * csum[j][c];
-                    a1[j] = 0;
+                    clo[j] = csum8[j][c];
+                    chi[j] = 0;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t lo = wv[q] & 0x0F0F0F0Fu;
-                    const uint32_t hi = (wv[q] >> 4) & 0x0F0F0F0Fu;
+                    const uint32_t hi16 = wv[q] & 0xF0F0F0F0u;
 #pragma unroll
                     for (int j = 0; j < N; ++j) {
-                        int &x = q < 2 ? a0[j] : a1[j];
-                        x = dp4a_us(lo, act[j][c][2 * q], x);
-                        x = dp4a_us(hi, act[j][c][2 * q + 1], x);
+                        clo[j] = dp4a_us(lo, act[j][c][2 * q], clo[j]);
+                        chi[j] = dp4a_us(hi16, act[j][c][2 * q + 1], chi[j]);
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
-                    const int ai = a0[j] + a1[j];
-                    acc[m][j] = fmaf(sc[u][m][c], (float)ai, acc[m][j]);
+                    const int ai = clo[j] + (chi[j] >> 4);   // exact: chi is 16 x an integer
+                    float &x = acc[(u * N + j) * NM + m];
+                    x = fmaf(sc, (float)ai, x);
                     if (PROBE) {
                         // exact per-64-group accumulators: the two chunks of a group sit in
                         // lanes gl and gl ^ 1 (lpr is even)
                         const int other = __shfl_xor_sync(0xffffffffu, ai, 1);
-                        if (rv && ci < nch && !shared && j < t.nt && (ci & 1) == 0) {
+                        if (rv && li < sn && t.sh == 0 && j < t.nt && (ci & 1) == 0) {
                             const size_t pr = (size_t)(t.rowbase + j - a.routed_rowbase);
                             const size_t o = (pr * g.nrows + r) * g.G + (ci >> 1);
                             int32_t *dst = GU ? (m == 0 ? a.probe.acc_gate : a.probe.acc_up)
@@ -193,59 +266,155 @@ __device__ __forceinline__ void run_task(const FfnArgs &a, const Task &t, const 
                 }
             }
         }
+    }
+
+    // output o of the task: row t.r0 + u*rpw + sub, token j, matrix m
+    auto emit = [&](int o, float v, float partner) {
+        const int m = o % NM, j = (o / NM) % N, u = o / (NM * N);
+        const int r = t.r0 + u * rpw + sub;
+        if (r >= g.nrows || j >= t.nt) return;
+        float sx = 0.0f;
 #pragma unroll
-        for (int m = 0; m < NM; ++m)
-#pragma unroll
-            for (int j = 0; j < N; ++j)
-                for (int off = lpr >> 1; off > 0; off >>= 1)
-                    acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], off);
-        if (gl == 0 && rv) {
-#pragma unroll
-            for (int j = 0; j < N; ++j) {
-                if (j >= t.nt) continue;
-                const size_t orow = (size_t)(t.rowbase + j);
-                if (GU) {
-                    const float gate = ascale[j] * acc[0][j];
-                    const float up = ascale[j] * acc[NM - 1][j];
+        for (int jj = 0; jj < N; ++jj)
+            if (jj == j) sx = ascale[jj];
+        const size_t orow = (size_t)(t.rowbase + j);
+        const size_t prow = (size_t)t.s * a.plane_rows + orow;   // row of the slice's plane
+        if (GU) {
+            if (g.S == 1) {
+                if (m == 0) {
+                    const float gate = sx * v, up = sx * partner;
                     a.h[orow * a.hstride + r] = gate / (1.0f + expf(-gate)) * up;
-                } else {
-                    a.y[orow * a.H + r] = ascale[j] * acc[0][j];
                 }
+            } else {
+                (m == 0 ? a.gpart : a.upart)[prow * a.hstride + r] = sx * v;
+            }
+        } else {
+            a.y[prow * a.H + r] = sx * v;
+        }
+    };
+
+    if (lpr == 32) {
+        // one row per u: reduce-scatter all V accumulators, 32 at a time
+        constexpr int G32 = V < 32 ? V : 32;
+        constexpr int SH = 5 - ilog2(G32);   // lanes sharing one total: 1 << SH
+#pragma unroll
+        for (int base = 0; base < V; base += G32) {
+            ReduceScatter<G32, 16>::run(acc + base, lane);
+            const float v = acc[base];
+            // gate and up of one (row, token) are neighbours (m is the lowest digit of o)
+            const float partner = __shfl_xor_sync(0xffffffffu, v, 1 << SH);
+            if ((lane & ((1 << SH) - 1)) == 0) emit(base + (lane >> SH), v, partner);
+        }
+    } else {
+#pragma unroll
+        for (int o = 0; o < V; ++o)
+            for (int off = lpr >> 1; off > 0; off >>= 1)
+                acc[o] += __shfl_xor_sync(0xffffffffu, acc[o], off);
+        if (gl == 0) {
+#pragma unroll
+            for (int o = 0; o < V; o += NM) emit(o, acc[o], acc[o + NM - 1]);
+            if (!GU || g.S > 1) {
+#pragma unroll
+                for (int o = 1; o < V; o += NM)
+                    if (NM > 1) emit(o, acc[o], 0.0f);
             }
         }
     }
 }
 
-template <int NC, int TC, int RU, bool GU, int MINB, bool PROBE>
-__global__ void __launch_bounds__(kFfnThreads, MINB) ffn_kernel(const __grid_constant__ FfnArgs a)
+// global index of the task whose cost interval holds cost c (0 <= c < total cost)
+template <bool GU>
+__device__ int task_at(const FfnArgs &a, long long c)
 {
-    const int lane = threadIdx.x & 31;
+    const FfnPlan *plan = a.plan;
+    const int64_t *cost = GU ? plan->gu_cost : plan->dn_cost;
+    int lo = 0, hi = plan->n_slots;   // the last slot starting at or before c
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cost[mid] <= c) lo = mid;
+        else hi = mid;
+    }
+    const int sh = plan->expert[lo] < 0 ? 1 : 0;
+    const Geo &g = GU ? a.geo_gu[sh] : a.geo_dn[sh];
+    return (GU ? plan->gu_prefix : plan->dn_prefix)[lo] +
+           task_at_cost(g, plan->ntok[lo], GU ? a.tc_gu : a.tc_dn, c - cost[lo]);
+}
+
+template <int NC, int RU, bool GU>
+constexpr int ring_slots() { return RU * (GU ? 2 : 1) * NC; }
+
+// stages of the ring: about 36 slots per lane (~184 KB for 8 warps), at least 2, at most 4
+template <int NC, int RU, bool GU>
+constexpr int ring_depth()
+{
+    constexpr int d = 36 / ring_slots<NC, RU, GU>();
+    return d < 2 ? 2 : (d > 4 ? 4 : d);
+}
+
+template <int NC, int RU, bool GU>
+constexpr size_t ring_bytes()
+{
+    return (size_t)kFfnWarpsPerCta * ring_depth<NC, RU, GU>() * ring_slots<NC, RU, GU>() * 32 *
+           (sizeof(uint4) + sizeof(float));
+}
+
+template <int NC, int TC, int RU, bool GU, bool PROBE>
+__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_constant__ FfnArgs a)
+{
+    constexpr int D = ring_depth<NC, RU, GU>();
+    constexpr int SL = ring_slots<NC, RU, GU>();
+    extern __shared__ uint4 ffn_ring[];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint4 *wbuf = ffn_ring + (size_t)wid * D * SL * 32;
+    float *sbuf = reinterpret_cast<float *>(ffn_ring + (size_t)kFfnWarpsPerCta * D * SL * 32) +
+                  (size_t)wid * D * SL * 32;
+
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    const int total = GU ? a.plan->gu_tiles : a.plan->dn_tiles;
-    const int t_begin = (int)(gw * total / nw), t_end = (int)((gw + 1) * total / nw);
+    const int n_slots = a.plan->n_slots;
+    const long long C = (GU ? a.plan->gu_cost : a.plan->dn_cost)[n_slots];
+    if (C <= 0) return;
+    const int t_begin = task_at<GU>(a, C * gw / nw);
+    const int t_end = gw + 1 == nw ? (GU ? a.plan->gu_tiles : a.plan->dn_tiles)
+                                   : task_at<GU>(a, C * (gw + 1) / nw);
     if (t_begin >= t_end) return;
     const QuantRows &src = GU ? a.xq : a.hq;
 
-    Walker<GU> walk;
-    walk.start(a, t_begin);
+    Walker<GU> cw;   // the task being computed
+    cw.start(a, t_begin);
+    Walker<GU> iw = cw;   // the next task to copy in
+    int issued = t_begin;
+    auto issue_next = [&](int st) {
+        if (issued < t_end) {
+            issue_task<NC, RU, GU>(a, iw.t, st, wbuf, sbuf);
+            if (++issued < t_end) iw.next(a);
+        }
+        cp_async_commit();   // possibly empty: keeps one group per task
+    };
+#pragma unroll
+    for (int k = 0; k < D - 1; ++k) issue_next(k);
 
     uint32_t act[TC][NC][8];
-    int csum[TC][NC];
+    int csum8[TC][NC];   // -8 x the chunk's code sum
     float ascale[TC];
-    int cur_slot = -1, cur_j0 = -1;
+    int cur_slot = -1, cur_j0 = -1, cur_s = -1;
 
-    for (int task = t_begin; task < t_end; ++task) {
-        if (task > t_begin) walk.next(a);
-        const Task t = walk.task(a);
+    for (int task = t_begin, it = 0; task < t_end; ++task, ++it) {
+        issue_next((it + D - 1) % D);
+        cp_async_wait<D - 1>();   // this task's copies (group `it`) have landed
+        if (task > t_begin) cw.next(a);
+        const Task &t = cw.t;
         const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
 
         // activations of this lane's chunks for the task's tokens (kept across tasks)
-        if (t.slot != cur_slot || t.j0 != cur_j0) {
+        if (t.slot != cur_slot || t.j0 != cur_j0 || t.s != cur_s) {
             cur_slot = t.slot;
             cur_j0 = t.j0;
+            cur_s = t.s;
             const int lpr = lpr_of<NC>(g);
-            const int gl = lane % lpr, nch = g.kdim / 32;
+            const int gl = lane % lpr, cb = t.s * g.sch, sn = min(g.sch, g.kdim / 32 - cb);
 #pragma unroll
             for (int j = 0; j < TC; ++j) {
                 int row = 0;
@@ -257,65 +426,62 @@ __global__ void __launch_bounds__(kFfnThreads, MINB) ffn_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
-                    const int ci = gl + c * lpr;
-                    if (j < t.nt && ci < nch) {
+                    const int li = gl + c * lpr, ci = cb + li;
+                    if (j < t.nt && li < sn) {
                         const uint4 *p = reinterpret_cast<const uint4 *>(
                             src.q + (size_t)row * src.q_ld + (size_t)ci * 32);
                         const uint4 v0 = p[0], v1 = p[1];
                         act[j][c][0] = v0.x; act[j][c][1] = v0.y; act[j][c][2] = v0.z; act[j][c][3] = v0.w;
                         act[j][c][4] = v1.x; act[j][c][5] = v1.y; act[j][c][6] = v1.z; act[j][c][7] = v1.w;
-                        csum[j][c] = src.csum[(size_t)row * src.c_ld + ci];
+                        csum8[j][c] = -8 * src.csum[(size_t)row * src.c_ld + ci];
                     } else {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) act[j][c][q] = 0;
-                        csum[j][c] = 0;
+                        csum8[j][c] = 0;
                     }
                 }
             }
         }
 
         // the chunk's real token count picks the variant, so padding costs little
+        const int st = it % D;
         if (t.nt == 1 || TC == 1)
-            run_task<NC, TC, RU, 1, GU, PROBE>(a, t, g, act, csum, ascale);
+            run_task<NC, TC, RU, 1, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
         else if (t.nt == 2 || TC == 2)
-            run_task<NC, TC, RU, (TC >= 2 ? 2 : 1), GU, PROBE>(a, t, g, act, csum, ascale);
+            run_task<NC, TC, RU, (TC >= 2 ? 2 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+        else if (t.nt <= 4 || TC == 4)
+            run_task<NC, TC, RU, (TC >= 4 ? 4 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
         else
-            run_task<NC, TC, RU, TC, GU, PROBE>(a, t, g, act, csum, ascale);
+            run_task<NC, TC, RU, TC, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
     }
+    cp_async_wait<0>();
 }
 
 typedef void (*FfnKernel)(const FfnArgs);
 
-// Each (kind, chunks, tokens) combination is built three ways: with two CTAs (16 warps) per
-// SM, with one CTA and twice the rows in flight, and as the probe-writing twin of the latter.
-// The host takes the 16-warp build unless the compiler had to spill it to local memory.
+// Each (kind, chunks, tokens) combination: the production kernel and its probe-writing twin
+// (the same arithmetic, plus stores of the exact per-group accumulators), the rows per task
+// and the dynamic shared memory of the ring.
 struct Variant {
-    FfnKernel k2;       // 16 warps per SM
-    int ru2;
-    FfnKernel k1;       // 8 warps per SM
-    int ru1;
-    FfnKernel kprobe;   // the 8-warp build that also writes the test probes
+    FfnKernel k;
+    FfnKernel kprobe;
+    int ru;
+    size_t smem;
 };
 
-// Rows in flight per task: about 12 (two CTAs) or 24 (one CTA) 16-byte loads per lane, so
-// that roughly 100 KB of weight loads are outstanding per SM (the streaming rate of a GB300
-// saturates near 50 KB per SM, measured); fewer once a token chunk's activations take more
-// than 64 registers.
-constexpr int ru_for(int nc, int tc, int nm, int ctas)
+// Rows per task: about 8 ring slots (16-byte loads) per lane and task, a power of two.
+constexpr int ru_for(int nc, int nm)
 {
-    int ru = 12 * (3 - ctas) / (nm * nc);
-    ru = ru < 1 ? 1 : (ru > 8 ? 8 : ru);
-    if (nc * 8 * tc > 64 && ru > 1) ru = ru / 2;
-    return ru;
+    const int want = 8 / (nm * nc);
+    return want >= 8 ? 8 : (want >= 4 ? 4 : (want >= 2 ? 2 : 1));
 }
 
 template <bool GU, int NC, int TC>
 Variant variant_tc()
 {
-    constexpr int NM = GU ? 2 : 1;
-    constexpr int R2 = ru_for(NC, TC, NM, 2), R1 = ru_for(NC, TC, NM, 1);
-    return {ffn_kernel<NC, TC, R2, GU, 2, false>, R2, ffn_kernel<NC, TC, R1, GU, 1, false>, R1,
-            ffn_kernel<NC, TC, R1, GU, 1, true>};
+    constexpr int RU = ru_for(NC, GU ? 2 : 1);
+    return {ffn_kernel<NC, TC, RU, GU, false>, ffn_kernel<NC, TC, RU, GU, true>, RU,
+            ring_bytes<NC, RU, GU>()};
 }
 
 // largest tokens-per-chunk whose activations fit the registers

@@ -2,12 +2,15 @@
 // configuration, the planner and the kernels so that all three cut a slot's work alike.
 //
 // A matrix row reducing over `kdim` inputs is kdim/2 bytes of packed nibbles, i.e. kdim/32
-// 16-byte chunks of 32 codes.  `lpr` lanes of a warp share a row: the whole warp when the row
-// has more than 32 chunks or when the launch's other matrix does ("full"), else the smallest
-// power of two covering the chunks.  A warp covers rpw = 32/lpr rows at once and a lane owns
-// nc chunks of the row (gl, gl+lpr, ...), so nc > 1 only ever goes with lpr = 32.  A task is one block of ru*rpw consecutive rows of
-// one expert for one chunk of at most tc tokens; a warp loads the ru row groups of a task
-// together, so ru*nc 16-byte loads per matrix are in flight per lane.
+// 16-byte chunks of 32 codes.  The row may be cut into S slices of sch chunks (the last one
+// ragged); each slice is reduced on its own and the S partial sums are added later in slice
+// order.  `lpr` lanes of a warp share a row of a slice: the whole warp when the slice has
+// more than 32 chunks or when the launch's other matrix does ("full"), else the smallest
+// power of two covering the slice's chunks.  A warp covers rpw = 32/lpr rows at once and a
+// lane owns nc chunks of the slice (gl, gl+lpr, ...), so nc > 1 only ever goes with
+// lpr = 32.  A task is one block of ru*rpw consecutive rows of one expert, one slice, one
+// chunk of at most tc tokens; a warp loads the ru row groups of a task together, so ru*nc
+// 16-byte loads per matrix are in flight per lane.
 #pragma once
 
 #include "device_util.cuh"
@@ -16,9 +19,11 @@ namespace moe {
 
 constexpr int kFfnWarpsPerCta = 8;
 constexpr int kFfnThreads = kFfnWarpsPerCta * 32;
+constexpr int kSliceChunks = 32;   // chunks per slice when rows are sliced (1024 inputs)
 
 struct Geo {
     int kdim, nrows;      // reduction length and rows of the matrix (per expert)
+    int S, sch;           // slices per row, chunks per slice
     int lpr, rpw, nc;     // lanes per row, rows per warp at once, chunks per lane
     int ru, rb;           // row groups per task, rows per task (ru * rpw)
     int rowbytes, G;      // bytes per row, 64-groups per row
@@ -31,15 +36,17 @@ __host__ __device__ __forceinline__ int pow2_ceil_ge(int v, int cap)
     return l;
 }
 
-__host__ __device__ inline Geo make_geo(int kdim, int nrows, int ru, bool full)
+__host__ __device__ inline Geo make_geo(int kdim, int nrows, int ru, bool full, bool sliced)
 {
     Geo g;
     g.kdim = kdim;
     g.nrows = nrows;
     const int nch = kdim / 32;
-    g.lpr = full ? 32 : pow2_ceil_ge(nch, 32);
+    g.sch = sliced && nch > kSliceChunks ? kSliceChunks : nch;
+    g.S = (nch + g.sch - 1) / g.sch;
+    g.lpr = full ? 32 : pow2_ceil_ge(g.sch, 32);
     g.rpw = 32 / g.lpr;
-    g.nc = (nch + g.lpr - 1) / g.lpr;
+    g.nc = (g.sch + g.lpr - 1) / g.lpr;
     g.ru = ru;
     g.rb = ru * g.rpw;
     g.rowbytes = kdim / 2;
@@ -47,11 +54,45 @@ __host__ __device__ inline Geo make_geo(int kdim, int nrows, int ru, bool full)
     return g;
 }
 
-// Tasks of a slot: (token chunk of at most tc tokens, row block), chunk-major.
+// Tasks of a slot: (token chunk of at most tc tokens, slice, row block), in that order of
+// significance.
 __host__ __device__ __forceinline__ int tasks_of(const Geo &g, int ntok, int tc)
 {
     if (ntok <= 0) return 0;
-    return ((g.nrows + g.rb - 1) / g.rb) * ((ntok + tc - 1) / tc);
+    return ((g.nrows + g.rb - 1) / g.rb) * g.S * ((ntok + tc - 1) / tc);
+}
+
+// Tokens a kernel built for chunks of tc computes for a chunk of nt (its code path) ...
+__host__ __device__ __forceinline__ int chunk_width(int nt, int tc)
+{
+    if (nt <= 1 || tc == 1) return 1;
+    if (nt == 2 || tc == 2) return 2;
+    if (nt <= 4 || tc == 4) return 4;
+    return tc;
+}
+
+// ... and the relative cost of one of its tasks: the per-token work plus about three
+// tokens' worth of per-task work (copies, unpacking, reduction, stores).  Warps take equal
+// shares of the summed cost, not of the task count.
+__host__ __device__ __forceinline__ int task_weight(int nt, int tc) { return chunk_width(nt, tc) + 3; }
+
+__host__ __device__ __forceinline__ long long slot_cost(const Geo &g, int ntok, int tc)
+{
+    if (ntok <= 0) return 0;
+    const long long per_chunk = (long long)((g.nrows + g.rb - 1) / g.rb) * g.S;
+    const int nch = (ntok + tc - 1) / tc, nlast = ntok - (nch - 1) * tc;
+    return per_chunk * ((long long)(nch - 1) * task_weight(tc, tc) + task_weight(nlast, tc));
+}
+
+// the slot's task whose cost interval holds x (0 <= x < slot_cost)
+__host__ __device__ __forceinline__ int task_at_cost(const Geo &g, int ntok, int tc, long long x)
+{
+    const long long per_chunk = (long long)((g.nrows + g.rb - 1) / g.rb) * g.S;
+    const int nch = (ntok + tc - 1) / tc, nlast = ntok - (nch - 1) * tc;
+    const long long wf = task_weight(tc, tc);
+    const long long full = (long long)(nch - 1) * per_chunk * wf;
+    if (x < full) return (int)(x / wf);
+    return (int)((nch - 1) * per_chunk + (x - full) / task_weight(nlast, tc));
 }
 
 }  // namespace moe

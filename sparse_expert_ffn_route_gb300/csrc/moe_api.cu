@@ -187,6 +187,9 @@ FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
     a.xq.q_ld = c.hidden;
     a.xq.c_ld = c.hidden / 32;
     a.h = at<float>(ws, L.h);
+    a.gpart = at<float>(ws, L.hp);
+    a.upart = a.gpart + L.hp_plane_floats;
+    a.slice_gu = 1;
     a.hstride = fmax_of(c);
     a.hq.q = at<int8_t>(ws, L.hq);
     a.hq.scale = at<float>(ws, L.hscale);
@@ -222,11 +225,9 @@ cudaError_t run_ffn(const FfnArgs &a, int T, int ns, bool routed_rows, bool ev, 
 
 // ---- per-stage CUDA-event timing (MOE_FLAG_STAGE_EVENTS) ----
 struct StageRec {
-    int stage;
+    int stage, launches;
     cudaEvent_t start, stop;
 };
-
-constexpr int kStageLaunches[MOE_N_STAGES] = {2, 1, 1, 1, 1, 1, 1, 1};
 thread_local std::vector<StageRec> t_pending;
 thread_local std::vector<cudaEvent_t> t_spare;
 thread_local double t_ms[MOE_N_STAGES];
@@ -246,9 +247,10 @@ cudaEvent_t take_event()
 
 struct StageScope {
     // records a start event now and a stop event when finished (only when enabled)
-    StageScope(bool on, int stage, cudaStream_t st) : on_(on), st_(st)
+    StageScope(bool on, int stage, cudaStream_t st, int launches = 1) : on_(on), st_(st)
     {
         rec_.stage = stage;
+        rec_.launches = launches;
         rec_.start = rec_.stop = nullptr;
         if (on_ && (rec_.start = take_event()) != nullptr) cudaEventRecord(rec_.start, st_);
     }
@@ -323,17 +325,25 @@ WsLayout ws_layout(const moe_config &c, int T)
     L.slot = take(TK * 4);
     L.uniq = take(E * 4);
     L.n_uniq = take(4);
+    L.pair_of = take(TK * 4);
     L.logits = take(E * 4 * logits_rows(c, T));
     L.xq = take((size_t)T * H);
     L.xscale = take((size_t)T * 4);
     L.xcsum = take((size_t)T * (H / 32) * 4);
     const size_t rows = (size_t)T * ns + TK;
     const size_t fm = (size_t)fmax_of(c);
+    // sliced rows (batches of at most kRouteClusterMaxT tokens): per-slice partial planes
+    const int ts = T < kRouteClusterMaxT ? T : kRouteClusterMaxT;
+    const size_t rows_s = (size_t)ts * ns + (size_t)ts * c.top_k;
+    const size_t s_gu = (H + 32 * kSliceChunks - 1) / (32 * kSliceChunks);
+    const size_t s_dn = (fm + 32 * kSliceChunks - 1) / (32 * kSliceChunks);
     L.h = take(rows * fm * 4);
+    L.hp_plane_floats = s_gu > 1 ? s_gu * rows_s * fm : 0;
+    L.hp = take(2 * L.hp_plane_floats * 4);
     L.hq = take(rows * fm);
     L.hscale = take(rows * 4);
     L.hcsum = take(rows * (fm / 32) * 4);
-    L.y = take(rows * H * 4);
+    L.y = take((rows > s_dn * rows_s ? rows : s_dn * rows_s) * H * 4);
     L.total = off;
     return L;
 }
@@ -393,8 +403,9 @@ int moe_permute(const moe_config *cfg, const int32_t *ids, const int32_t *keff, 
     REQUIRE_PTR(n_uniq, 4);
     WsLayout L;
     if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
-    cudaError_t e = launch_permute(*cfg, ids, keff, T, counts, offsets, tok, slot, uniq, n_uniq,
-                                   at<int32_t>(workspace, L.err), (cudaStream_t)stream);
+    const PermuteOut o{counts, offsets, tok, slot, uniq, n_uniq, at<int32_t>(workspace, L.err),
+                       nullptr};
+    cudaError_t e = launch_permute(*cfg, ids, keff, T, o, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
     return ok();
 }
@@ -426,6 +437,8 @@ int moe_expert_ffn(const moe_config *cfg, const float *x, int T, const moe_exper
     a.tok = tok;
     a.y = y_pairs;
     a.routed_rowbase = 0;
+    a.plane_rows = T * cfg->top_k;
+    a.slice_dn = 0;   // y_pairs holds one plane
     if (probe) a.probe = *probe;
     ffn_configure(a);
     cudaError_t e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
@@ -461,6 +474,8 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     const float *ys = nullptr;
+    int s_sh = 1;
+    int64_t plane = 0;
     if (use_shared) {
         FfnArgs a = base_args(*cfg, T, workspace, L);
         a.n_shared = 1;
@@ -468,14 +483,19 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
         a.shared = *shared;
         a.y = at<float>(workspace, L.y);
         a.routed_rowbase = T;
+        a.plane_rows = T;
+        a.slice_dn = 1;
         ffn_configure(a);
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
         if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 1, false, false, st);
         ys = a.y;
+        s_sh = a.slice_dn ? a.geo_dn[1].S : 1;
+        plane = (int64_t)a.plane_rows * cfg->hidden;
     }
     if (e == cudaSuccess)
-        e = launch_combine(*cfg, y_pairs, cfg->hidden, ys, ids, keff, w, offsets, tok, T, y, st);
+        e = launch_combine(*cfg, y_pairs, cfg->hidden, ys, ids, keff, w, offsets, tok, nullptr, 1,
+                           s_sh, plane, T, y, st);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return ok();
 }
@@ -542,38 +562,63 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     a.tok = tok;
     a.y = at<float>(workspace, L.y);
     a.routed_rowbase = T * ns;
+    a.plane_rows = T * ns + T * cfg->top_k;
+    a.slice_dn = 1;
     ffn_configure(a);
 
     const bool ev = (flags & MOE_FLAG_STAGE_EVENTS) != 0;
+    float *logits = at<float>(workspace, L.logits);
+    const PermuteOut perm{at<int32_t>(workspace, L.counts), offsets, tok,
+                          at<int32_t>(workspace, L.slot), uniq, n_uniq,
+                          at<int32_t>(workspace, L.err), at<int32_t>(workspace, L.pair_of)};
     cudaError_t e;
-    {
-        StageScope sc(ev, MOE_STAGE_ROUTER, st);
-        e = launch_router(*cfg, x, w_router, bias, T, at<float>(workspace, L.logits), ids, w,
-                          keff, st);
-        sc.finish();
-    }
-    if (e == cudaSuccess) {
-        StageScope sc(ev, MOE_STAGE_PERMUTE, st);
-        e = launch_permute(*cfg, ids, keff, T, at<int32_t>(workspace, L.counts), offsets, tok,
-                           at<int32_t>(workspace, L.slot), uniq, n_uniq,
-                           at<int32_t>(workspace, L.err), st);
-        sc.finish();
-    }
-    if (e == cudaSuccess) {
-        StageScope sc(ev, MOE_STAGE_PLAN, st);
-        e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
-        sc.finish();
-    }
-    if (e == cudaSuccess) {
-        StageScope sc(ev, MOE_STAGE_QUANT, st);
-        e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
-        sc.finish();
+    int splits = 1;
+    if (T <= kRouteClusterMaxT) {
+        // decode route: router + x quantisation, then selection + batch-union + plan
+        {
+            StageScope sc(ev, MOE_STAGE_ROUTER, st);
+            e = launch_router_logits(*cfg, x, w_router, T, logits, &a.xq, &splits, st);
+            sc.finish();
+        }
+        if (e == cudaSuccess) {
+            StageScope sc(ev, MOE_STAGE_SELECT, st);
+            e = launch_route_tail(*cfg, logits, bias, T, ids, w, keff, &perm, &a, st);
+            sc.finish();
+        }
+    } else {
+        {
+            StageScope sc(ev, MOE_STAGE_ROUTER, st);
+            e = launch_router_logits(*cfg, x, w_router, T, logits, nullptr, &splits, st);
+            sc.finish();
+        }
+        if (e == cudaSuccess) {
+            StageScope sc(ev, MOE_STAGE_SELECT, st);
+            e = launch_router_select(*cfg, logits, splits, bias, T, ids, w, keff, st);
+            sc.finish();
+        }
+        if (e == cudaSuccess) {
+            StageScope sc(ev, MOE_STAGE_PERMUTE, st);
+            e = launch_permute(*cfg, ids, keff, T, perm, st);
+            sc.finish();
+        }
+        if (e == cudaSuccess) {
+            StageScope sc(ev, MOE_STAGE_PLAN, st);
+            e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
+            sc.finish();
+        }
+        if (e == cudaSuccess) {
+            StageScope sc(ev, MOE_STAGE_QUANT, st);
+            e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
+            sc.finish();
+        }
     }
     if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, ns, true, ev, st);
     if (e == cudaSuccess) {
         StageScope sc(ev, MOE_STAGE_COMBINE, st);
         e = launch_combine(*cfg, a.y + (size_t)T * ns * cfg->hidden, cfg->hidden,
-                           ns ? a.y : nullptr, ids, keff, w, offsets, tok, T, y, st);
+                           ns ? a.y : nullptr, ids, keff, w, offsets, tok, perm.pair_of,
+                           a.slice_dn ? a.geo_dn[0].S : 1, a.slice_dn ? a.geo_dn[1].S : 1,
+                           (int64_t)a.plane_rows * cfg->hidden, T, y, st);
         sc.finish();
     }
     if (e != cudaSuccess) return cuda_fail(e, "layer launch");
@@ -588,7 +633,7 @@ int moe_stage_times(double *ms, long long *launches, int reset)
         if (cudaEventSynchronize(r.stop) == cudaSuccess &&
             cudaEventElapsedTime(&v, r.start, r.stop) == cudaSuccess) {
             t_ms[r.stage] += v;
-            t_launches[r.stage] += kStageLaunches[r.stage];
+            t_launches[r.stage] += r.launches;
         } else {
             cudaGetLastError();
         }

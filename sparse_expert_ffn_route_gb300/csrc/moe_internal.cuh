@@ -15,6 +15,9 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxSlots = kMaxExperts + 1;  // routed experts plus the shared one
 constexpr int kMaxDim = 8192;
+// batches up to this many tokens take the decode route: cluster router (with the x
+// quantisation) and one CTA for selection, batch-union and FFN plan
+constexpr int kRouteClusterMaxT = 64;
 
 // device-side error word bits (workspace `err`)
 constexpr int kErrBadExpertId = 1;
@@ -37,6 +40,8 @@ struct FfnPlan {
     int32_t rowbase[kMaxSlots];       // first output row of the slot
     int32_t gu_prefix[kMaxSlots + 1]; // exclusive prefix of gate/up tasks per slot
     int32_t dn_prefix[kMaxSlots + 1];
+    int64_t gu_cost[kMaxSlots + 1];   // exclusive prefix of gate/up task cost per slot
+    int64_t dn_cost[kMaxSlots + 1];
 };
 
 // Quantised activations: per row n int8 codes stored with each run of 8
@@ -65,7 +70,11 @@ struct FfnArgs {
     float *h;                         // [rows][hstride] fp32 SiLU(gate)*up
     int hstride;
     QuantRows hq;                     // [rows][hstride] quantised h
-    float *y;                         // [rows][H] fp32 output rows
+    float *y;                         // [S_down][plane_rows][H] fp32 output rows (plane 0
+                                      // holds the result when down rows are not sliced)
+    float *gpart, *upart;             // [S_gate/up][plane_rows][hstride] partial gate / up
+    int plane_rows;                   // output rows of the call (shared rows + routed pairs)
+    int slice_gu, slice_dn;           // rows cut into 1024-input slices
     int tc_gu, tc_dn;                 // token chunk per task
     Geo geo_gu[2], geo_dn[2];         // task geometry: [0] routed experts, [1] shared expert
     moe_ffn_probe probe;              // routed pairs only; row index = pair
@@ -77,10 +86,11 @@ struct FfnArgs {
 // ---------------------------------------------------------------------------
 struct WsLayout {
     size_t ids, w, keff;              // routing (layer_forward)
-    size_t counts, offsets, tok, slot, uniq, n_uniq;
+    size_t counts, offsets, tok, slot, uniq, n_uniq, pair_of;
     size_t logits;                    // router partial logits [S][T][E]
     size_t xq, xscale, xcsum;         // quantised x
     size_t h;                         // [rows][Fmax] fp32
+    size_t hp, hp_plane_floats;       // partial gate planes then partial up planes
     size_t hq, hscale, hcsum;         // quantised h
     size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
     size_t plan;                      // FfnPlan
@@ -94,12 +104,29 @@ int router_splits(const moe_config &c, int T);
 // ---------------------------------------------------------------------------
 // launchers (return cudaError_t of the launch)
 // ---------------------------------------------------------------------------
+// router logits into `scratch` ([T][E] final logits for T <= kRouteClusterMaxT, else
+// [splits][T][E] partial sums); with xq non-null (decode route only) also quantises x
+cudaError_t launch_router_logits(const moe_config &c, const float *x, const float *wr, int T,
+                                 float *scratch, const QuantRows *xq, int *splits, cudaStream_t st);
+cudaError_t launch_router_select(const moe_config &c, const float *scratch, int splits,
+                                 const float *bias, int T, int32_t *ids, float *w, int32_t *keff,
+                                 cudaStream_t st);
+// logits + selection (moe_route)
 cudaError_t launch_router(const moe_config &c, const float *x, const float *wr, const float *bias,
-                          int T, float *logits_part, int32_t *ids, float *w, int32_t *keff,
+                          int T, float *scratch, int32_t *ids, float *w, int32_t *keff,
                           cudaStream_t st);
+// outputs of the batch-union
+struct PermuteOut {
+    int32_t *counts, *offsets, *tok, *slot, *uniq, *n_uniq, *err;
+    int32_t *pair_of;   // nullable: [T*K] list position of pair (t, i), -1 for i >= keff[t]
+};
+// one CTA: selection from final logits [T][E] (T <= kRouteClusterMaxT), then, when perm is
+// non-null, the batch-union, then, when plan_args is non-null, the FFN plan
+cudaError_t launch_route_tail(const moe_config &c, const float *logits, const float *bias, int T,
+                              int32_t *ids, float *w, int32_t *keff, const PermuteOut *perm,
+                              const FfnArgs *plan_args, cudaStream_t st);
 cudaError_t launch_permute(const moe_config &c, const int32_t *ids, const int32_t *keff, int T,
-                           int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *slot,
-                           int32_t *uniq, int32_t *n_uniq, int32_t *err, cudaStream_t st);
+                           const PermuteOut &o, cudaStream_t st);
 cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_uniq,
                         FfnPlan *plan, cudaStream_t st);
 cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride, QuantRows dst,
@@ -112,9 +139,13 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
 void ffn_configure(FfnArgs &a);
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
+// pair_of (nullable) gives each (t, i) its list position directly; without it the position
+// is found by binary search in the expert's token list.  S_r / S_s slice planes (plane
+// stride `plane` floats) hold the routed / shared rows' partial sums.
 cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t routed_row_stride,
                            const float *y_shared, const int32_t *ids, const int32_t *keff,
-                           const float *w, const int32_t *offsets, const int32_t *tok, int T,
+                           const float *w, const int32_t *offsets, const int32_t *tok,
+                           const int32_t *pair_of, int S_r, int S_s, int64_t plane, int T,
                            float *y, cudaStream_t st);
 
 // host helpers shared with the entry points outside moe_api.cu

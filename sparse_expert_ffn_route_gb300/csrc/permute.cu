@@ -10,11 +10,16 @@
 //      warps of this chunk + its rank among the lanes of its warp with the same expert
 //      (__match_any_sync).  No atomic decides an order, so the lists are deterministic and
 //      ascending in token.
-// plan_kernel (and the tail of permute_kernel when asked): slot table and tile prefix sums
-// of the FFN kernels.
+// plan_kernel: slot table and tile prefix sums of the FFN kernels.
+// route_tail_kernel: decode-sized batches -- selection from the final router logits
+// (router_select.cuh), the batch-union and the plan, all in one CTA of 1024 threads.
+#include <atomic>
+
 #include "device_util.cuh"
-#include "moe_internal.cuh"
 #include "ffn_tiles.cuh"
+#include "launch.cuh"
+#include "moe_internal.cuh"
+#include "router_select.cuh"
 
 namespace moe {
 
@@ -27,31 +32,32 @@ struct PlanParams {
     Geo geo_gu[2], geo_dn[2];   // [0] routed, [1] shared
 };
 
-// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
-__device__ int block_exclusive_scan(int v, int *total, int *s_warp)
+// Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).
+template <typename V>
+__device__ V block_exclusive_scan(V v, V *total, V *s_warp)
 {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-    int incl = v;
+    V incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        const V o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
     if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        int w = lane < nw ? s_warp[lane] : 0;
-        int wi = w;
+        V w = lane < nw ? s_warp[lane] : V(0);
+        V wi = w;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            const V o = __shfl_up_sync(0xffffffffu, wi, off);
             if (lane >= off) wi += o;
         }
         if (lane < nw) s_warp[lane] = wi - w;   // exclusive prefix of warp totals
         if (lane == nw - 1) s_warp[32] = wi;
     }
     __syncthreads();
-    const int res = s_warp[wid] + incl - v;
+    const V res = s_warp[wid] + incl - v;
     *total = s_warp[32];
     __syncthreads();
     return res;
@@ -63,13 +69,16 @@ __device__ int block_exclusive_scan(int v, int *total, int *s_warp)
 __device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const int32_t *uniq,
                            const int32_t *n_uniq, FfnPlan *plan, int *s_warp)
 {
+    __shared__ long long s_warp64[33];
     const int ns = pp.n_shared;
     const int nu = pp.include_routed ? *n_uniq : 0;
     const int nslots = ns + nu;
     int base_gu = 0, base_dn = 0;
+    long long cbase_gu = 0, cbase_dn = 0;
     for (int s0 = 0; s0 < nslots; s0 += blockDim.x) {
         const int s = s0 + threadIdx.x;
         int gu = 0, dn = 0;
+        long long cgu = 0, cdn = 0;
         if (s < nslots) {
             int e, ntok, tokbase, rowbase, sh;
             if (s < ns) {
@@ -87,47 +96,88 @@ __device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const i
             plan->rowbase[s] = rowbase;
             gu = tasks_of(pp.geo_gu[sh], ntok, pp.tc_gu);
             dn = tasks_of(pp.geo_dn[sh], ntok, pp.tc_dn);
+            cgu = slot_cost(pp.geo_gu[sh], ntok, pp.tc_gu);
+            cdn = slot_cost(pp.geo_dn[sh], ntok, pp.tc_dn);
         }
         int tot_gu, tot_dn;
         const int ex_gu = block_exclusive_scan(gu, &tot_gu, s_warp);
         const int ex_dn = block_exclusive_scan(dn, &tot_dn, s_warp);
+        long long ctot_gu, ctot_dn;
+        const long long cex_gu = block_exclusive_scan(cgu, &ctot_gu, s_warp64);
+        const long long cex_dn = block_exclusive_scan(cdn, &ctot_dn, s_warp64);
         if (s < nslots) {
             plan->gu_prefix[s] = base_gu + ex_gu;
             plan->dn_prefix[s] = base_dn + ex_dn;
+            plan->gu_cost[s] = cbase_gu + cex_gu;
+            plan->dn_cost[s] = cbase_dn + cex_dn;
         }
         base_gu += tot_gu;
         base_dn += tot_dn;
+        cbase_gu += ctot_gu;
+        cbase_dn += ctot_dn;
     }
     if (threadIdx.x == 0) {
         plan->n_slots = nslots;
         plan->gu_prefix[nslots] = base_gu;
         plan->dn_prefix[nslots] = base_dn;
+        plan->gu_cost[nslots] = cbase_gu;
+        plan->dn_cost[nslots] = cbase_dn;
         plan->gu_tiles = base_gu;
         plan->dn_tiles = base_dn;
     }
 }
 
-__global__ void __launch_bounds__(1024) permute_kernel(
-    const int32_t *__restrict__ ids, const int32_t *__restrict__ keff, int T, int K, int E,
-    int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tok,
-    int32_t *__restrict__ slot, int32_t *__restrict__ uniq, int32_t *__restrict__ n_uniq,
-    int32_t *__restrict__ err)
-{
-    __shared__ int s_cnt[kMaxExperts];
-    __shared__ int s_off[kMaxExperts];
-    __shared__ int s_base[kMaxExperts];
-    __shared__ int s_tot[kMaxExperts];
-    __shared__ unsigned short s_wt[32][kMaxExperts];
-    __shared__ int s_warp[33];
+// Shared-memory working set of the batch-union (E <= kMaxExperts).
+struct PermuteSmem {
+    int *cnt, *off, *base, *tot;   // [kMaxExperts]; off has one more entry: the pair total
+    unsigned short *wt;            // [32][kMaxExperts]
+    int *uniq, *nu;                // unique experts [kMaxExperts], their count [1]
+    int *warp;                     // [33] scan scratch
+};
 
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+constexpr size_t kPermuteSmemBytes =
+    sizeof(int) * (4 * kMaxExperts + 1) + sizeof(unsigned short) * 32 * kMaxExperts +
+    sizeof(int) * (kMaxExperts + 1) + sizeof(int) * 33;
+
+__device__ PermuteSmem carve_permute_smem(char *pool)
+{
+    PermuteSmem m;
+    m.wt = reinterpret_cast<unsigned short *>(pool);
+    int *p = reinterpret_cast<int *>(pool + sizeof(unsigned short) * 32 * kMaxExperts);
+    m.cnt = p; p += kMaxExperts;
+    m.off = p; p += kMaxExperts + 1;
+    m.base = p; p += kMaxExperts;
+    m.tot = p; p += kMaxExperts;
+    m.uniq = p; p += kMaxExperts;
+    m.nu = p; p += 1;
+    m.warp = p;
+    return m;
+}
+
+// The batch-union by the whole block (blockDim.x == 1024).  ids / keff may point to global
+// or shared memory.  Besides the global outputs, sm.off[0..E] (offsets), sm.uniq and *sm.nu
+// hold the lists' heads for the caller.
+__device__ void permute_block(const int32_t *ids, const int32_t *keff, int T, int K, int E,
+                              const PermuteOut &o, const PermuteSmem &sm)
+{
+    int32_t *__restrict__ counts = o.counts;
+    int32_t *__restrict__ offsets = o.offsets;
+    int32_t *__restrict__ tok = o.tok;
+    int32_t *__restrict__ slot = o.slot;
+    int32_t *__restrict__ uniq = o.uniq;
+    int32_t *__restrict__ n_uniq = o.n_uniq;
+    int32_t *__restrict__ err = o.err;
+    int *s_cnt = sm.cnt, *s_off = sm.off, *s_base = sm.base, *s_tot = sm.tot;
+    unsigned short(*s_wt)[kMaxExperts] = reinterpret_cast<unsigned short(*)[kMaxExperts]>(sm.wt);
+
+    const int tid = threadIdx.x, wid = tid >> 5;
     const long long P = (long long)T * K;
 
     for (int e = tid; e < E; e += blockDim.x) {
         s_cnt[e] = 0;
         s_base[e] = 0;
     }
-    for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) (&s_wt[0][0])[i] = 0;
+    for (int i = tid; i < 32 * kMaxExperts; i += blockDim.x) sm.wt[i] = 0;
     __syncthreads();
 
     int bad = 0;
@@ -151,18 +201,23 @@ __global__ void __launch_bounds__(1024) permute_kernel(
     {
         const int v = tid < E ? s_cnt[tid] : 0;
         int total, nu;
-        const int ex = block_exclusive_scan(v, &total, s_warp);
+        const int ex = block_exclusive_scan(v, &total, sm.warp);
         const int f = (tid < E && v > 0) ? 1 : 0;
-        const int exf = block_exclusive_scan(f, &nu, s_warp);
+        const int exf = block_exclusive_scan(f, &nu, sm.warp);
         if (tid < E) {
             s_off[tid] = ex;
             offsets[tid] = ex;
             counts[tid] = v;
-            if (f) uniq[exf] = tid;
+            if (f) {
+                uniq[exf] = tid;
+                sm.uniq[exf] = tid;
+            }
         }
         if (tid == 0) {
+            s_off[E] = total;
             offsets[E] = total;
             *n_uniq = nu;
+            *sm.nu = nu;
         }
     }
     __syncthreads();
@@ -200,6 +255,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(
             tok[pos] = t;
             slot[pos] = (int)p;
         }
+        if (o.pair_of && p < P) o.pair_of[p] = e >= 0 ? s_off[e] + s_base[e] + s_wt[wid][e] + rank : -1;
         __syncthreads();
         for (int x = tid; x < E; x += blockDim.x) {
             s_base[x] += s_tot[x];
@@ -210,27 +266,131 @@ __global__ void __launch_bounds__(1024) permute_kernel(
     }
 }
 
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t *__restrict__ ids,
+                                                       const int32_t *__restrict__ keff, int T,
+                                                       int K, int E, PermuteOut o)
+{
+    __shared__ __align__(16) char pool[kPermuteSmemBytes];
+    pdl_wait();
+    pdl_launch_dependents();
+    permute_block(ids, keff, T, K, E, o, carve_permute_smem(pool));
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams pp, const int32_t *offsets,
                                                     const int32_t *uniq, const int32_t *n_uniq,
                                                     FfnPlan *plan)
 {
     __shared__ int s_warp[33];
+    pdl_wait();
+    pdl_launch_dependents();
     build_plan(pp, offsets, uniq, n_uniq, plan, s_warp);
 }
 
-}  // namespace
-
-cudaError_t launch_permute(const moe_config &c, const int32_t *ids, const int32_t *keff, int T,
-                           int32_t *counts, int32_t *offsets, int32_t *tok, int32_t *slot,
-                           int32_t *uniq, int32_t *n_uniq, int32_t *err, cudaStream_t st)
+// Batch-union of at most 1024 pairs by a block of 1024 threads, from the routing in shared
+// memory: histogram, one scan of (count, present) packed in an int, a scatter of the pairs
+// into their experts' segments in any order, then each pair's final place from its rank
+// among the segment's pair indices (pair index p = t*K + i, so ascending p is ascending
+// token within an expert).  Fills sm.off[0..E], sm.uniq, *sm.nu besides the global outputs.
+__device__ void permute_small_block(const int *s_ids, const int *s_keff, int T, int K, int E,
+                                    const PermuteOut &o, const PermuteSmem &sm, int *s_stage,
+                                    int *s_fill)
 {
-    permute_kernel<<<1, 1024, 0, st>>>(ids, keff, T, c.top_k, c.n_experts, counts, offsets, tok,
-                                       slot, uniq, n_uniq, err);
-    return cudaGetLastError();
+    const int tid = threadIdx.x;
+    const int P = T * K;
+    int e_mine = -1;
+    if (o.pair_of && tid < P) o.pair_of[tid] = -1;
+    if (tid < P) {
+        const int t = tid / K, i = tid - t * K;
+        const int k = s_keff[t];
+        int bad = 0;
+        if (k < 0 || k > K) bad |= (i == 0) ? kErrBadKeff : 0;
+        if (i < max(0, min(K, k))) {
+            const int e = s_ids[tid];
+            if (e >= 0 && e < E) e_mine = e;
+            else bad |= kErrBadExpertId;
+        }
+        if (bad) atomicOr(o.err, bad);
+        if (e_mine >= 0) atomicAdd(&sm.cnt[e_mine], 1);
+    }
+    __syncthreads();
+    {
+        const int v = tid < E ? sm.cnt[tid] : 0;
+        const int packed = v | ((v > 0 ? 1 : 0) << 16);   // counts <= 1024, experts <= 512
+        int total;
+        const int ex = block_exclusive_scan(packed, &total, sm.warp);
+        if (tid < E) {
+            const int off = ex & 0xffff;
+            sm.off[tid] = off;
+            o.offsets[tid] = off;
+            o.counts[tid] = v;
+            if (v > 0) {
+                sm.uniq[ex >> 16] = tid;
+                o.uniq[ex >> 16] = tid;
+            }
+            s_fill[tid] = 0;
+        }
+        if (tid == 0) {
+            sm.off[E] = total & 0xffff;
+            o.offsets[E] = total & 0xffff;
+            *sm.nu = total >> 16;
+            *o.n_uniq = total >> 16;
+        }
+    }
+    __syncthreads();
+    if (e_mine >= 0) s_stage[sm.off[e_mine] + atomicAdd(&s_fill[e_mine], 1)] = tid;
+    __syncthreads();
+    if (tid < sm.off[E]) {
+        const int p = s_stage[tid];
+        const int e = s_ids[p];
+        const int lo = sm.off[e], hi = sm.off[e + 1];
+        int rank = 0;
+        for (int j = lo; j < hi; ++j) rank += s_stage[j] < p ? 1 : 0;
+        o.tok[lo + rank] = p / K;
+        o.slot[lo + rank] = p;
+        if (o.pair_of) o.pair_of[p] = lo + rank;
+    }
 }
 
-cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_uniq,
-                        FfnPlan *plan, cudaStream_t st)
+// Decode-sized batch (T <= kRouteClusterMaxT, so T * K <= 1024 pairs): one warp per token
+// selects, then the block permutes and plans.  The routing and the lists' heads stay in
+// shared memory between the phases; the global outputs are written alongside.
+constexpr size_t kTailSmemBytes = kPermuteSmemBytes + sizeof(int) * (kRouteClusterMaxT * kMaxTopK) +
+                                  sizeof(int) * kRouteClusterMaxT + 2 * sizeof(int) * 32 * kMaxTopK +
+                                  sizeof(int) * (1024 + kMaxExperts);
+
+__global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restrict__ logits, int T,
+                                                          SelectParams sp, int32_t *ids, float *w,
+                                                          int32_t *keff, int do_permute,
+                                                          PermuteOut o, int do_plan,
+                                                          PlanParams pp, FfnPlan *plan)
+{
+    extern __shared__ __align__(16) char tail_pool[];
+    const PermuteSmem sm = carve_permute_smem(tail_pool);
+    int *s_ids = reinterpret_cast<int *>(tail_pool + kPermuteSmemBytes);
+    int *s_keff = s_ids + kRouteClusterMaxT * kMaxTopK;
+    int *s_sel = s_keff + kRouteClusterMaxT;
+    float *s_g = reinterpret_cast<float *>(s_sel + 32 * kMaxTopK);
+    int *s_stage = reinterpret_cast<int *>(s_g + 32 * kMaxTopK);
+    int *s_fill = s_stage + 1024;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int wid = threadIdx.x >> 5;
+    const int E = sp.E, K = sp.K;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
+    for (int t = wid; t < T; t += 32) {
+        const float *lrow = logits + (size_t)t * E;
+        select_token(sp, [&](int e) { return lrow[e]; }, t, s_sel + wid * kMaxTopK,
+                     s_g + wid * kMaxTopK, ids, w, keff, s_ids + t * K, s_keff + t);
+    }
+    if (!do_permute) return;
+    __syncthreads();
+    permute_small_block(s_ids, s_keff, T, K, E, o, sm, s_stage, s_fill);
+    if (!do_plan) return;
+    __syncthreads();
+    build_plan(pp, sm.off, sm.uniq, sm.nu, plan, sm.warp);
+}
+
+PlanParams plan_params(const FfnArgs &a)
 {
     PlanParams pp;
     pp.T = a.T;
@@ -243,8 +403,45 @@ cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_
         pp.geo_gu[i] = a.geo_gu[i];
         pp.geo_dn[i] = a.geo_dn[i];
     }
-    plan_kernel<<<1, 1024, 0, st>>>(pp, a.offsets, uniq, n_uniq, plan);
-    return cudaGetLastError();
+    return pp;
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const moe_config &c, const int32_t *ids, const int32_t *keff, int T,
+                           const PermuteOut &o, cudaStream_t st)
+{
+    return launch_kernel(permute_kernel, dim3(1), dim3(1024), 0, st, 1, ids, keff, T, c.top_k,
+                         c.n_experts, o);
+}
+
+cudaError_t launch_plan(const FfnArgs &a, const int32_t *uniq, const int32_t *n_uniq,
+                        FfnPlan *plan, cudaStream_t st)
+{
+    return launch_kernel(plan_kernel, dim3(1), dim3(1024), 0, st, 1, plan_params(a), a.offsets,
+                         uniq, n_uniq, plan);
+}
+
+cudaError_t launch_route_tail(const moe_config &c, const float *logits, const float *bias, int T,
+                              int32_t *ids, float *w, int32_t *keff, const PermuteOut *perm,
+                              const FfnArgs *plan_args, cudaStream_t st)
+{
+    if (T <= 0) return cudaSuccess;
+    const PermuteOut o = perm ? *perm : PermuteOut{};
+    const PlanParams pp = plan_args ? plan_params(*plan_args) : PlanParams{};
+    FfnPlan *plan = plan_args ? const_cast<FfnPlan *>(plan_args->plan) : nullptr;
+    static std::atomic<bool> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !configured[dev].load()) {
+        const cudaError_t e = cudaFuncSetAttribute(route_tail_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kTailSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(true);
+    }
+    return launch_kernel(route_tail_kernel, dim3(1), dim3(1024), kTailSmemBytes, st, 1, logits, T,
+                         select_params(c, bias), ids, w, keff, perm ? 1 : 0, o,
+                         (perm && plan_args) ? 1 : 0, pp, plan);
 }
 
 }  // namespace moe

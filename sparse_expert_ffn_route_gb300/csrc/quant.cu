@@ -3,6 +3,7 @@
 // activation quantisation hoisted to the layer], and of h = SiLU(gate)*up before the down
 // projection.  One CTA per row.
 #include "device_util.cuh"
+#include "launch.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -64,28 +65,50 @@ __device__ void quant_row_block(const float *__restrict__ v, int n, int8_t *__re
 __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__restrict__ src,
                                                                int n, int stride, QuantRows dst)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int row = blockIdx.x;
     quant_row_block(src + (size_t)row * stride, n, dst.q + (size_t)row * dst.q_ld,
                     dst.csum + (size_t)row * dst.c_ld, dst.scale + row, nullptr, nullptr);
 }
 
 // h rows: [0, first) of n_first values (the shared expert), then the routed pair rows,
-// as many as *rest_count (device value; null = none), of n_rest values.
+// as many as *rest_count (device value; null = none), of n_rest values.  With S > 1 the
+// gate/up rows were sliced: h = SiLU(gate) * up is formed here from the S partial planes
+// (added in slice order) into shared memory, then quantised.
 __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restrict__ h, int ld,
                                                             int first, int n_first, int n_rest,
                                                             const int32_t *rest_count,
                                                             int routed_rowbase, QuantRows dst,
-                                                            int8_t *probe_hq, float *probe_hs)
+                                                            int8_t *probe_hq, float *probe_hs,
+                                                            const float *__restrict__ gpart,
+                                                            const float *__restrict__ upart,
+                                                            int S, int64_t plane)
 {
+    extern __shared__ __align__(16) float s_h[];
+    pdl_wait();
+    pdl_launch_dependents();
     const int row = blockIdx.x;
     const int rest = rest_count ? *rest_count : 0;
     if (row >= first + rest) return;
     const bool routed = row >= first;
     const int n = routed ? n_rest : n_first;
     const size_t pr = (size_t)(row - routed_rowbase);
-    quant_row_block(h + (size_t)row * ld, n, dst.q + (size_t)row * dst.q_ld,
-                    dst.csum + (size_t)row * dst.c_ld, dst.scale + row,
-                    (routed && probe_hq) ? probe_hq + pr * n : nullptr,
+    const float *v = h + (size_t)row * ld;
+    if (S > 1) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            float gate = 0.0f, up = 0.0f;
+            for (int s = 0; s < S; ++s) {
+                gate += gpart[s * plane + (int64_t)row * ld + i];
+                up += upart[s * plane + (int64_t)row * ld + i];
+            }
+            s_h[i] = gate / (1.0f + expf(-gate)) * up;
+        }
+        __syncthreads();
+        v = s_h;
+    }
+    quant_row_block(v, n, dst.q + (size_t)row * dst.q_ld, dst.csum + (size_t)row * dst.c_ld,
+                    dst.scale + row, (routed && probe_hq) ? probe_hq + pr * n : nullptr,
                     (routed && probe_hs) ? probe_hs + pr : nullptr);
 }
 
@@ -95,8 +118,8 @@ cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride,
                               cudaStream_t st)
 {
     if (rows <= 0) return cudaSuccess;
-    quant_rows_kernel<<<rows, kQThreads, 0, st>>>(src, n, src_stride, dst);
-    return cudaGetLastError();
+    return launch_kernel(quant_rows_kernel, dim3(rows), dim3(kQThreads), 0, st, 1, src, n,
+                         src_stride, dst);
 }
 
 cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_rest,
@@ -104,10 +127,19 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
 {
     if (max_rows <= 0) return cudaSuccess;
     const int32_t *rest = a.include_routed ? a.offsets + a.E : nullptr;
-    quant_h_kernel<<<max_rows, kQThreads, 0, st>>>(a.h, a.hstride, first_rows, n_first, n_rest,
-                                                    rest, a.routed_rowbase, a.hq, a.probe.hq,
-                                                    a.probe.h_scale);
-    return cudaGetLastError();
+    const int S = a.slice_gu ? a.geo_gu[0].S : 1;
+    const size_t smem = S > 1 ? sizeof(float) * (size_t)a.hstride : 0;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(quant_h_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(quant_h_kernel, dim3(max_rows), dim3(kQThreads), smem, st, 1,
+                         (const float *)a.h, a.hstride, first_rows, n_first, n_rest, rest,
+                         a.routed_rowbase, a.hq, a.probe.hq, a.probe.h_scale,
+                         (const float *)a.gpart, (const float *)a.upart, S,
+                         (int64_t)a.plane_rows * a.hstride);
 }
 
 }  // namespace moe

@@ -2,16 +2,29 @@
 // iterated-argmax top-k, adaptive top-p, norm_topk_prob, routed_scaling_factor
 // ["MoE 路由与专家流式加载" §1.1, §1.2].
 //
-// Two kernels:
-//   router_logits_kernel  fp32 x . W_router^T, tiled 64 tokens x 64 experts, split along H
-//                         so that even one token spreads the 4*E*H router bytes over the
-//                         whole GPU; partial sums go to workspace [S][T][E].
-//   router_select_kernel  one warp per token: sums the S partials in a fixed order, then
-//                         sigmoid, + bias, K rounds of warp argmax, top-p, norm, scale.
+// Decode-sized batches (T <= kRouteClusterMaxT):
+//   router_cluster_kernel  one cluster of CS CTAs per 16 experts; CTA rank r holds the r-th
+//                          slice of H, each warp two experts x all tokens, so a lane keeps
+//                          its experts' router weights in registers and streams x (the eight
+//                          warps of a CTA read the same x slice, from L1 after the first).
+//                          The CS partial logits are summed in rank order through distributed
+//                          shared memory.  It also quantises x to int8 (the layer's activation
+//                          quantisation): cluster c takes tokens t = c (mod clusters), the
+//                          ranks' partial |x| maxima meet the same way.
+//   route_tail_kernel      (permute.cu) selection, batch-union and FFN plan in one CTA.
+// Larger batches:
+//   router_logits_kernel   fp32 x . W_router^T, tiled 64 tokens x 64 experts, split along H
+//                          so that the grid covers the GPU; partial sums to [S][T][E].
+//   router_select_kernel   one warp per token: sums the S partials in a fixed order, then
+//                          selects (router_select.cuh).
 #include <float.h>
 
+#include <cooperative_groups.h>
+
 #include "device_util.cuh"
+#include "launch.cuh"
 #include "moe_internal.cuh"
+#include "router_select.cuh"
 
 namespace moe {
 
@@ -29,6 +42,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
 {
     __shared__ float xs[kBK][kBT + 4];
     __shared__ float ws[kBK][kBE + 4];
+    pdl_wait();
+    pdl_launch_dependents();
     const int t0 = blockIdx.x * kBT, e0 = blockIdx.y * kBE, s = blockIdx.z;
     const int nch = H / kBK;
     const int c0 = (int)((long long)s * nch / S), c1 = (int)((long long)(s + 1) * nch / S);
@@ -81,119 +96,154 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
     }
 }
 
-constexpr int kPerLane = kMaxExperts / 32;
+constexpr int kExpertsPerCluster = 16;
 
-struct Cand {
-    float v;   // choice = sig + bias
-    float g;   // sig (the applied gate)
-    int e;     // expert id, INT_MAX = none
-};
-
-__device__ __forceinline__ bool better(const Cand &a, const Cand &b)
+// Decode-sized batches: logits of 16 experts x all T tokens per cluster, x quantisation.
+// MAXU bounds the float4 units of the H slice that one lane holds per expert.
+template <int MAXU>
+__global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__restrict__ x,
+                                                                const float *__restrict__ wr,
+                                                                int T, int H, int E,
+                                                                float *__restrict__ logits,
+                                                                QuantRows xq, int quant)
 {
-    // a beats b: any candidate beats none; larger choice wins; equal choice -> lower id
-    if (b.e == 0x7fffffff) return a.e != 0x7fffffff;
-    if (a.e == 0x7fffffff) return false;
-    return a.v > b.v || (a.v == b.v && a.e < b.e);
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    __shared__ float s_part[kRouteClusterMaxT][kExpertsPerCluster];
+    __shared__ float s_amax[kRouteClusterMaxT];
+    __shared__ float s_red[8];
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int CS = (int)cl.num_blocks(), r = (int)cl.block_rank();
+    const int c = blockIdx.x / CS, ncl = gridDim.x / CS;
+    const int L = H / CS, k0 = r * L, nunit = L / 4;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int e0 = c * kExpertsPerCluster + 2 * wid;
+
+    float4 wv[2][MAXU];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = e0 + j;
+#pragma unroll
+        for (int u = 0; u < MAXU; ++u) {
+            const int idx = u * 32 + lane;
+            wv[j][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < E && idx < nunit) {
+                const uint4 q = ld_stream_v4(wr + (size_t)e * H + k0 + idx * 4);
+                wv[j][u] = make_float4(__uint_as_float(q.x), __uint_as_float(q.y),
+                                       __uint_as_float(q.z), __uint_as_float(q.w));
+            }
+        }
+    }
+    for (int t = 0; t < T; ++t) {
+        const float *xr = x + (size_t)t * H + k0;
+        float acc[2] = {0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < MAXU; ++u) {
+            const int idx = u * 32 + lane;
+            if (idx < nunit) {
+                const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr + idx * 4));
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    acc[j] = fmaf(xv.x, wv[j][u].x, acc[j]);
+                    acc[j] = fmaf(xv.y, wv[j][u].y, acc[j]);
+                    acc[j] = fmaf(xv.z, wv[j][u].z, acc[j]);
+                    acc[j] = fmaf(xv.w, wv[j][u].w, acc[j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+        if (lane == 0) {
+            s_part[t][2 * wid] = acc[0];
+            s_part[t][2 * wid + 1] = acc[1];
+        }
+    }
+    // |x| maximum of this slice for the tokens this cluster quantises
+    if (quant) {
+        for (int i = 0, t = c; t < T; ++i, t += ncl) {
+            float m = 0.0f;
+            for (int idx = tid; idx < nunit; idx += blockDim.x) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + k0 + idx * 4));
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) s_red[wid] = m;
+            __syncthreads();
+            if (tid == 0) {
+                float v = s_red[0];
+                for (int q = 1; q < 8; ++q) v = fmaxf(v, s_red[q]);
+                s_amax[i] = v;
+            }
+            __syncthreads();
+        }
+    }
+    cl.sync();
+
+    // logits of the tokens t = r (mod CS): the CS slices summed in rank order
+    const int mine = r < T ? (T - r + CS - 1) / CS : 0;
+    for (int pidx = tid; pidx < mine * kExpertsPerCluster; pidx += blockDim.x) {
+        const int t = r + (pidx / kExpertsPerCluster) * CS, j = pidx % kExpertsPerCluster;
+        const int e = c * kExpertsPerCluster + j;
+        if (e >= E) continue;
+        float sum = 0.0f;
+        for (int q = 0; q < CS; ++q) sum += *cl.map_shared_rank(&s_part[t][j], q);
+        logits[(size_t)t * E + e] = sum;
+    }
+    // int8 codes of this slice for the cluster's tokens (runs of 8 as [e0 e2 e4 e6|e1 e3 e5 e7],
+    // code sums per 32-element chunk), the row scale from rank 0
+    if (quant) {
+        for (int i = 0, t = c; t < T; ++i, t += ncl) {
+            float amax = 0.0f;
+            for (int q = 0; q < CS; ++q) amax = fmaxf(amax, *cl.map_shared_rank(&s_amax[i], q));
+            const float inv = quant_inv(amax);
+            const int runs = L / 8;
+            for (int base = 0; base < runs; base += blockDim.x) {
+                const int run = base + tid;
+                if (base + (tid & ~31) >= runs) break;   // whole warp past the end
+                int sum = 0;
+                if (run < runs) {
+                    const float *v = x + (size_t)t * H + k0 + run * 8;
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(v));
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(v + 4));
+                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    const uint2 pk = quant_pack8(xv, inv, sum);
+                    *reinterpret_cast<uint2 *>(xq.q + (size_t)t * xq.q_ld + k0 + run * 8) = pk;
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if ((lane & 3) == 0 && run < runs) xq.csum[(size_t)t * xq.c_ld + (k0 + run * 8) / 32] = sum;
+            }
+            if (r == 0 && tid == 0) xq.scale[t] = quant_scale(amax);
+        }
+    }
+    cl.sync();   // no CTA leaves while another still reads its shared memory
 }
 
-__global__ void __launch_bounds__(256) router_select_kernel(
-    const float *__restrict__ part, int S, int T, int E, int K, const float *__restrict__ bias,
-    int norm, float scale, float top_p, int32_t *__restrict__ ids, float *__restrict__ w,
-    int32_t *__restrict__ keff)
+__global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ part, int S,
+                                                            int T, SelectParams p,
+                                                            int32_t *__restrict__ ids,
+                                                            float *__restrict__ w,
+                                                            int32_t *__restrict__ keff)
 {
     __shared__ int s_sel[8][kMaxTopK];
     __shared__ float s_g[8][kMaxTopK];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int wid = threadIdx.x >> 5;
     const int t = blockIdx.x * 8 + wid;
     if (t >= T) return;
-
-    float sig[kPerLane], ch[kPerLane];
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) {
-        const int e = lane + 32 * j;
-        sig[j] = 0.0f;
-        ch[j] = 0.0f;
-        if (e < E) {
-            float l = 0.0f;
-            for (int s = 0; s < S; ++s) l += part[((size_t)s * T + t) * E + e];
-            sig[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-            ch[j] = __fadd_rn(sig[j], bias[e]);
-        }
-    }
-
-    unsigned taken = 0;
-    for (int k = 0; k < K; ++k) {
-        Cand best{0.0f, 0.0f, 0x7fffffff};
-#pragma unroll
-        for (int j = 0; j < kPerLane; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u)) {
-                Cand c{ch[j], sig[j], e};
-                if (better(c, best)) best = c;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            Cand o;
-            o.v = __shfl_xor_sync(0xffffffffu, best.v, off);
-            o.g = __shfl_xor_sync(0xffffffffu, best.g, off);
-            o.e = __shfl_xor_sync(0xffffffffu, best.e, off);
-            if (better(o, best)) best = o;
-        }
-        if ((best.e & 31) == lane) taken |= 1u << (best.e >> 5);
-        if (lane == 0) {
-            s_sel[wid][k] = best.e;
-            s_g[wid][k] = best.g;
-        }
-    }
-    __syncwarp();
-
-    if (lane == 0) {
-        int *sel = s_sel[wid];
-        float *g = s_g[wid];
-        int m = K;
-        if (top_p > 0.0f && top_p < 1.0f) {
-            // stable insertion sort of the kept gates, descending
-            for (int i = 1; i < K; ++i) {
-                const float gv = g[i];
-                const int sv = sel[i];
-                int j = i;
-                while (j > 0 && g[j - 1] < gv) {
-                    g[j] = g[j - 1];
-                    sel[j] = sel[j - 1];
-                    --j;
-                }
-                g[j] = gv;
-                sel[j] = sv;
-            }
-            float tot = 0.0f;
-            for (int i = 0; i < K; ++i) tot = __fadd_rn(tot, g[i]);
-            const float thr = __fmul_rn(top_p, tot);
-            float cum = 0.0f;
-            for (int i = 0; i < K; ++i) {
-                cum = __fadd_rn(cum, g[i]);
-                if (cum >= thr) {
-                    m = i + 1;
-                    break;
-                }
-            }
-        }
-        float ssum = 0.0f;
-        for (int i = 0; i < m; ++i) ssum = __fadd_rn(ssum, g[i]);
-        for (int i = 0; i < K; ++i) {
-            const size_t o = (size_t)t * K + i;
-            if (i < m) {
-                const float v = norm ? __fdiv_rn(g[i], ssum) : g[i];
-                w[o] = __fmul_rn(v, scale);
-                ids[o] = sel[i];
-            } else {
-                w[o] = 0.0f;
-                ids[o] = -1;
-            }
-        }
-        keff[t] = m;
-    }
+    const int E = p.E;
+    auto logit = [&](int e) {
+        float l = 0.0f;
+        for (int s = 0; s < S; ++s) l += part[((size_t)s * T + t) * E + e];
+        return l;
+    };
+    select_token(p, logit, t, s_sel[wid], s_g[wid], ids, w, keff);
 }
 
 }  // namespace
@@ -208,21 +258,61 @@ int router_splits(const moe_config &c, int T)
     return (int)s;
 }
 
+int route_cluster_size(int H)
+{
+    for (int cs = 8; cs > 1; cs >>= 1)
+        if ((H / cs) % 32 == 0) return cs;
+    return 1;
+}
+
+cudaError_t launch_router_logits(const moe_config &c, const float *x, const float *wr, int T,
+                                 float *scratch, const QuantRows *xq, int *splits, cudaStream_t st)
+{
+    *splits = 1;
+    if (T <= 0) return cudaSuccess;
+    const int H = c.hidden, E = c.n_experts;
+    if (T <= kRouteClusterMaxT) {
+        const int cs = route_cluster_size(H);
+        const int units = (H / cs / 4 + 31) / 32;   // float4 units per lane and expert
+        const dim3 grid(cs * ((E + kExpertsPerCluster - 1) / kExpertsPerCluster));
+        const QuantRows q = xq ? *xq : QuantRows{};
+        const int quant = xq ? 1 : 0;
+        if (units <= 2)
+            return launch_kernel(router_cluster_kernel<2>, grid, dim3(256), 0, st, cs, x, wr, T, H,
+                                 E, scratch, q, quant);
+        if (units <= 4)
+            return launch_kernel(router_cluster_kernel<4>, grid, dim3(256), 0, st, cs, x, wr, T, H,
+                                 E, scratch, q, quant);
+        return launch_kernel(router_cluster_kernel<8>, grid, dim3(256), 0, st, cs, x, wr, T, H, E,
+                             scratch, q, quant);
+    }
+    const int S = router_splits(c, T);
+    *splits = S;
+    const dim3 grid((T + kBT - 1) / kBT, (E + kBE - 1) / kBE, S);
+    return launch_kernel(router_logits_kernel, grid, dim3(256), 0, st, 1, x, wr, T, H, E, S,
+                         scratch);
+}
+
+cudaError_t launch_router_select(const moe_config &c, const float *scratch, int splits,
+                                 const float *bias, int T, int32_t *ids, float *w, int32_t *keff,
+                                 cudaStream_t st)
+{
+    if (T <= 0) return cudaSuccess;
+    return launch_kernel(router_select_kernel, dim3((T + 7) / 8), dim3(256), 0, st, 1,
+                         (const float *)scratch, splits, T, select_params(c, bias), ids, w, keff);
+}
+
 cudaError_t launch_router(const moe_config &c, const float *x, const float *wr, const float *bias,
-                          int T, float *logits_part, int32_t *ids, float *w, int32_t *keff,
+                          int T, float *scratch, int32_t *ids, float *w, int32_t *keff,
                           cudaStream_t st)
 {
     if (T <= 0) return cudaSuccess;
-    const int S = router_splits(c, T);
-    dim3 grid((T + kBT - 1) / kBT, (c.n_experts + kBE - 1) / kBE, S);
-    router_logits_kernel<<<grid, 256, 0, st>>>(x, wr, T, c.hidden, c.n_experts, S, logits_part);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    router_select_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits_part, S, T, c.n_experts, c.top_k,
-                                                      bias, c.norm_topk_prob,
-                                                      c.routed_scaling_factor, c.top_p, ids, w,
-                                                      keff);
-    return cudaGetLastError();
+    int S = 1;
+    cudaError_t e = launch_router_logits(c, x, wr, T, scratch, nullptr, &S, st);
+    if (e != cudaSuccess) return e;
+    if (T <= kRouteClusterMaxT)
+        return launch_route_tail(c, scratch, bias, T, ids, w, keff, nullptr, nullptr, st);
+    return launch_router_select(c, scratch, S, bias, T, ids, w, keff, st);
 }
 
 }  // namespace moe
