@@ -15,6 +15,7 @@ namespace moe {
 namespace {
 
 constexpr int kCThreads = 256;
+constexpr int kMaxPlanes = kMaxCombinePlanes;
 
 __global__ void __launch_bounds__(kCThreads) combine_kernel(
     const float *__restrict__ y_routed, int64_t rstride, const float *__restrict__ y_shared,
@@ -51,29 +52,49 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     __syncthreads();
     const int c = (blockIdx.x * kCThreads + threadIdx.x) * 4;
     if (c >= H) return;
+    // every pair's (and the shared expert's) planes are loaded before the ordered sums
+    float4 v[kMaxTopK][kMaxPlanes];
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i) {
+#pragma unroll
+        for (int s = 0; s < kMaxPlanes; ++s) {
+            v[i][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < k && s < S_r && s_pair[i] >= 0)
+                v[i][s] = *reinterpret_cast<const float4 *>(y_routed + (size_t)s_pair[i] * rstride + c + s * plane);
+        }
+    }
+    float4 sv[kMaxPlanes];
+#pragma unroll
+    for (int s = 0; s < kMaxPlanes; ++s) {
+        sv[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (y_shared && s < S_s) sv[s] = *reinterpret_cast<const float4 *>(y_shared + (size_t)t * H + c + s * plane);
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < k; ++i) {
-        if (s_pair[i] < 0) continue;
-        const float *src = y_routed + (size_t)s_pair[i] * rstride + c;
-        float4 v = *reinterpret_cast<const float4 *>(src);
-        for (int s = 1; s < S_r; ++s) {
-            const float4 q = *reinterpret_cast<const float4 *>(src + s * plane);
-            v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i) {
+        if (i >= k || s_pair[i] < 0) continue;
+        float4 e = v[i][0];
+#pragma unroll
+        for (int s = 1; s < kMaxPlanes; ++s) {
+            if (s < S_r) {
+                e.x += v[i][s].x; e.y += v[i][s].y; e.z += v[i][s].z; e.w += v[i][s].w;
+            }
         }
         const float wi = s_w[i];
-        acc.x = fmaf(wi, v.x, acc.x);
-        acc.y = fmaf(wi, v.y, acc.y);
-        acc.z = fmaf(wi, v.z, acc.z);
-        acc.w = fmaf(wi, v.w, acc.w);
+        acc.x = fmaf(wi, e.x, acc.x);
+        acc.y = fmaf(wi, e.y, acc.y);
+        acc.z = fmaf(wi, e.z, acc.z);
+        acc.w = fmaf(wi, e.w, acc.w);
     }
     if (y_shared) {
-        const float *src = y_shared + (size_t)t * H + c;
-        float4 v = *reinterpret_cast<const float4 *>(src);
-        for (int s = 1; s < S_s; ++s) {
-            const float4 q = *reinterpret_cast<const float4 *>(src + s * plane);
-            v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+        float4 e = sv[0];
+#pragma unroll
+        for (int s = 1; s < kMaxPlanes; ++s) {
+            if (s < S_s) {
+                e.x += sv[s].x; e.y += sv[s].y; e.z += sv[s].z; e.w += sv[s].w;
+            }
         }
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        acc.x += e.x; acc.y += e.y; acc.z += e.z; acc.w += e.w;
     }
     *reinterpret_cast<float4 *>(y + (size_t)t * H + c) = acc;
 }

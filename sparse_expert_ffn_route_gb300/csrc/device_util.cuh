@@ -31,6 +31,34 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
     return d;
 }
 
+// Sums each of n values (n a power of two, <= 32) over the 32 lanes: at offsets 16, 8, ...
+// a lane keeps one half of its values, sends the other half to its partner and adds what
+// it receives; once one value is left the remaining offsets add it up.  Lane l ends with the
+// total of value l >> (5 - log2 n).
+template <int n, int d>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int lane)
+    {
+        if constexpr (d > 0) {
+            if constexpr (n > 1) {
+                const bool up = (lane & d) != 0;
+#pragma unroll
+                for (int i = 0; i < n / 2; ++i) {
+                    const float send = up ? v[i] : v[i + n / 2];
+                    const float keep = up ? v[i + n / 2] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+                }
+                ReduceScatter<n / 2, d / 2>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], d);
+                ReduceScatter<1, d / 2>::run(v, lane);
+            }
+        }
+    }
+};
+
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
 __device__ __forceinline__ unsigned lanemask_lt()
 {
     unsigned m;

@@ -39,27 +39,9 @@ Chosen choose(bool gu, int nc, int tc, bool probe)
 
 int max_nc(const Geo (&g)[2], bool both) { return both && g[1].nc > g[0].nc ? g[1].nc : g[0].nc; }
 
-// raises a kernel's dynamic shared memory limit to what its ring needs (once per kernel and
-// device)
-cudaError_t allow_smem(FfnKernel k, size_t bytes)
-{
-    static std::mutex mu;
-    static std::map<std::pair<int, FfnKernel>, bool> done;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (done.count({dev, k})) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)bytes);
-    if (e == cudaSuccess) done[{dev, k}] = true;
-    return e;
-}
-
 cudaError_t launch(Chosen c, const FfnArgs &a, cudaStream_t st)
 {
     if (!c.k) return cudaErrorInvalidConfiguration;
-    const cudaError_t e = allow_smem(c.k, c.smem);
-    if (e != cudaSuccess) return e;
     // one CTA of 8 warps per SM (the rings take most of shared memory)
     return launch_kernel(c.k, dim3(num_sms()), dim3(kFfnThreads), c.smem, st, 1, a);
 }
@@ -89,7 +71,8 @@ void ffn_configure(FfnArgs &a)
     const bool small = a.T <= kRouteClusterMaxT;
     const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;
     const bool sgu = small && a.slice_gu && a.H > 32 * kSliceChunks;
-    const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks;
+    const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks &&
+                     fmax <= 32 * kSliceChunks * kMaxCombinePlanes;
     a.slice_gu = sgu ? 1 : 0;
     a.slice_dn = sdn ? 1 : 0;
     // gate/up: both matrices reduce over H

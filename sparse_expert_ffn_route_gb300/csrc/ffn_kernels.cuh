@@ -125,33 +125,6 @@ __device__ __forceinline__ int lpr_of(const Geo &g)
     return NC >= 2 ? 32 : g.lpr;
 }
 
-// Sums each of n values (n a power of two, <= 32) over the 32 lanes: at offsets 16, 8, ...
-// a lane keeps one half of its values, sends the other half to its partner and adds what
-// it receives; once one value is left the remaining offsets add it up.  Lane l ends with the
-// total of value l >> (5 - log2 n).
-template <int n, int d>
-struct ReduceScatter {
-    static __device__ __forceinline__ void run(float *v, int lane)
-    {
-        if constexpr (d > 0) {
-            if constexpr (n > 1) {
-                const bool up = (lane & d) != 0;
-#pragma unroll
-                for (int i = 0; i < n / 2; ++i) {
-                    const float send = up ? v[i] : v[i + n / 2];
-                    const float keep = up ? v[i + n / 2] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
-                }
-                ReduceScatter<n / 2, d / 2>::run(v, lane);
-            } else {
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], d);
-                ReduceScatter<1, d / 2>::run(v, lane);
-            }
-        }
-    }
-};
-
-constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
 // one lane's ring slots: [stage][u][m][c] x 32 lanes
 template <int NC, int RU, int NM>
@@ -343,12 +316,14 @@ __device__ int task_at(const FfnArgs &a, long long c)
 template <int NC, int RU, bool GU>
 constexpr int ring_slots() { return RU * (GU ? 2 : 1) * NC; }
 
-// stages of the ring: about 36 slots per lane (~184 KB for 8 warps), at least 2, at most 4
+// stages of the ring: as many as fit about 224 KB of shared memory for the CTA's 8 warps
+// (at most 8, at least 2)
 template <int NC, int RU, bool GU>
 constexpr int ring_depth()
 {
-    constexpr int d = 36 / ring_slots<NC, RU, GU>();
-    return d < 2 ? 2 : (d > 4 ? 4 : d);
+    constexpr int per_stage = kFfnWarpsPerCta * ring_slots<NC, RU, GU>() * 32 * 20;
+    constexpr int d = 224 * 1024 / per_stage;
+    return d < 2 ? 2 : (d > 8 ? 8 : d);
 }
 
 template <int NC, int RU, bool GU>
@@ -484,17 +459,17 @@ Variant variant_tc()
             ring_bytes<NC, RU, GU>()};
 }
 
-// largest tokens-per-chunk whose activations fit the registers
-constexpr int tc_max(int nc) { return nc <= 2 ? 8 : (nc <= 4 ? 4 : 2); }
+// largest tokens-per-chunk whose activations (8 * tc * nc registers) leave room for the rest
+// within the 170 registers a thread of a 12-warp CTA has
+constexpr int tc_max(int nc) { return nc <= 1 ? 4 : (nc <= 2 ? 2 : 1); }
 
 template <bool GU, int NC>
 Variant variant_nc(int tc)
 {
     switch (tc) {
     case 1: return variant_tc<GU, NC, 1>();
-    case 2: return variant_tc<GU, NC, 2>();
-    case 4: if constexpr (NC <= 4) return variant_tc<GU, NC, 4>(); else break;
-    case 8: if constexpr (NC <= 2) return variant_tc<GU, NC, 8>(); else break;
+    case 2: if constexpr (tc_max(NC) >= 2) return variant_tc<GU, NC, 2>(); else break;
+    case 4: if constexpr (tc_max(NC) >= 4) return variant_tc<GU, NC, 4>(); else break;
     }
     return {};
 }

@@ -17,7 +17,7 @@
 
 namespace moe {
 
-constexpr int kFfnWarpsPerCta = 8;
+constexpr int kFfnWarpsPerCta = 12;
 constexpr int kFfnThreads = kFfnWarpsPerCta * 32;
 constexpr int kSliceChunks = 32;   // chunks per slice when rows are sliced (1024 inputs)
 

@@ -9,10 +9,18 @@
 
 namespace moe {
 
+// Raises `kernel`'s dynamic shared memory limit to at least `bytes` on the current device
+// (static plus dynamic shared memory above 48 KB needs it); remembered per device and kernel.
+cudaError_t ensure_dynamic_smem(const void *kernel, size_t bytes);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t st, int cluster_x, Args &&...args)
 {
+    if (smem > 0) {
+        const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kernel), smem);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

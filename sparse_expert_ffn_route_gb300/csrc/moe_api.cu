@@ -6,6 +6,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "ffn_tiles.cuh"
@@ -278,6 +281,21 @@ int set_error(int code, const char *fmt, ...)
 }
 
 int require_device() { return check_device(); }
+
+cudaError_t ensure_dynamic_smem(const void *kernel, size_t bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> set;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &have = set[{dev, kernel}];
+    if (have >= bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
 
 int validate_route_args(const moe_config *cfg, const float *x, const float *w_router,
                         const float *bias, int T, const int32_t *ids, const float *w,

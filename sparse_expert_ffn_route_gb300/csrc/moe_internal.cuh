@@ -18,6 +18,9 @@ constexpr int kMaxDim = 8192;
 // batches up to this many tokens take the decode route: cluster router (with the x
 // quantisation) and one CTA for selection, batch-union and FFN plan
 constexpr int kRouteClusterMaxT = 64;
+// the combine adds up to this many slice planes of y, so down rows are sliced only up to
+// this many 1024-input slices
+constexpr int kMaxCombinePlanes = 2;
 
 // device-side error word bits (workspace `err`)
 constexpr int kErrBadExpertId = 1;

@@ -13,8 +13,6 @@
 // plan_kernel: slot table and tile prefix sums of the FFN kernels.
 // route_tail_kernel: decode-sized batches -- selection from the final router logits
 // (router_select.cuh), the batch-union and the plan, all in one CTA of 1024 threads.
-#include <atomic>
-
 #include "device_util.cuh"
 #include "ffn_tiles.cuh"
 #include "launch.cuh"
@@ -355,8 +353,7 @@ __device__ void permute_small_block(const int *s_ids, const int *s_keff, int T, 
 // selects, then the block permutes and plans.  The routing and the lists' heads stay in
 // shared memory between the phases; the global outputs are written alongside.
 constexpr size_t kTailSmemBytes = kPermuteSmemBytes + sizeof(int) * (kRouteClusterMaxT * kMaxTopK) +
-                                  sizeof(int) * kRouteClusterMaxT + 2 * sizeof(int) * 32 * kMaxTopK +
-                                  sizeof(int) * (1024 + kMaxExperts);
+                                  sizeof(int) * kRouteClusterMaxT + sizeof(int) * (1024 + kMaxExperts);
 
 __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restrict__ logits, int T,
                                                           SelectParams sp, int32_t *ids, float *w,
@@ -368,9 +365,7 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     const PermuteSmem sm = carve_permute_smem(tail_pool);
     int *s_ids = reinterpret_cast<int *>(tail_pool + kPermuteSmemBytes);
     int *s_keff = s_ids + kRouteClusterMaxT * kMaxTopK;
-    int *s_sel = s_keff + kRouteClusterMaxT;
-    float *s_g = reinterpret_cast<float *>(s_sel + 32 * kMaxTopK);
-    int *s_stage = reinterpret_cast<int *>(s_g + 32 * kMaxTopK);
+    int *s_stage = s_keff + kRouteClusterMaxT;
     int *s_fill = s_stage + 1024;
     pdl_wait();
     pdl_launch_dependents();
@@ -379,8 +374,8 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
     for (int t = wid; t < T; t += 32) {
         const float *lrow = logits + (size_t)t * E;
-        select_token(sp, [&](int e) { return lrow[e]; }, t, s_sel + wid * kMaxTopK,
-                     s_g + wid * kMaxTopK, ids, w, keff, s_ids + t * K, s_keff + t);
+        select_token(sp, [&](int e) { return lrow[e]; }, t, ids, w, keff, s_ids + t * K,
+                     s_keff + t);
     }
     if (!do_permute) return;
     __syncthreads();
@@ -430,15 +425,6 @@ cudaError_t launch_route_tail(const moe_config &c, const float *logits, const fl
     const PermuteOut o = perm ? *perm : PermuteOut{};
     const PlanParams pp = plan_args ? plan_params(*plan_args) : PlanParams{};
     FfnPlan *plan = plan_args ? const_cast<FfnPlan *>(plan_args->plan) : nullptr;
-    static std::atomic<bool> configured[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && !configured[dev].load()) {
-        const cudaError_t e = cudaFuncSetAttribute(route_tail_kernel,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)kTailSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured[dev].store(true);
-    }
     return launch_kernel(route_tail_kernel, dim3(1), dim3(1024), kTailSmemBytes, st, 1, logits, T,
                          select_params(c, bias), ids, w, keff, perm ? 1 : 0, o,
                          (perm && plan_args) ? 1 : 0, pp, plan);

@@ -11,6 +11,7 @@ namespace moe {
 namespace {
 
 constexpr int kQThreads = 256;
+constexpr int kMaxSlices = kMaxDim / (32 * kSliceChunks);   // slices of a row of kMaxDim inputs
 
 // Quantises one row of n values (n a multiple of 32) with the whole block: codes in runs of
 // 8 stored [e0 e2 e4 e6 | e1 e3 e5 e7], the code sum of every 32-element chunk, the scale.
@@ -72,10 +73,91 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
                     dst.csum + (size_t)row * dst.c_ld, dst.scale + row, nullptr, nullptr);
 }
 
+// Sliced gate/up rows: h = SiLU(gate) * up of the row, gate and up each the sum of the S
+// slice planes in slice order, formed in registers -- run r (8 consecutive values) by thread
+// r % 256 -- and quantised from there like quant_row_block does.
+__device__ void quant_h_planes_block(const float *__restrict__ gp, const float *__restrict__ up,
+                                     int S, int64_t plane, int n, int8_t *__restrict__ q,
+                                     int32_t *__restrict__ csum, float *__restrict__ scale,
+                                     int8_t *__restrict__ canon, float *__restrict__ canon_scale)
+{
+    constexpr int kRuns = kMaxDim / 8 / kQThreads;   // runs per thread, at most
+    __shared__ float s_max[kQThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int runs = n / 8;
+    float h[kRuns][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kRuns; ++k) {
+        const int run = tid + kQThreads * k;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[k][i] = 0.0f;
+        if (run >= runs) continue;
+        float4 g[kMaxSlices][2], u[kMaxSlices][2];
+#pragma unroll
+        for (int s = 0; s < kMaxSlices; ++s) {   // every plane's loads first
+            if (s < S) {
+                const float4 *gs = reinterpret_cast<const float4 *>(gp + s * plane + run * 8);
+                const float4 *us = reinterpret_cast<const float4 *>(up + s * plane + run * 8);
+                g[s][0] = gs[0]; g[s][1] = gs[1];
+                u[s][0] = us[0]; u[s][1] = us[1];
+            }
+        }
+        float gv[8] = {g[0][0].x, g[0][0].y, g[0][0].z, g[0][0].w, g[0][1].x, g[0][1].y, g[0][1].z, g[0][1].w};
+        float uv[8] = {u[0][0].x, u[0][0].y, u[0][0].z, u[0][0].w, u[0][1].x, u[0][1].y, u[0][1].z, u[0][1].w};
+#pragma unroll
+        for (int s = 1; s < kMaxSlices; ++s) {
+            if (s < S) {
+                const float ga[8] = {g[s][0].x, g[s][0].y, g[s][0].z, g[s][0].w, g[s][1].x, g[s][1].y, g[s][1].z, g[s][1].w};
+                const float ua[8] = {u[s][0].x, u[s][0].y, u[s][0].z, u[s][0].w, u[s][1].x, u[s][1].y, u[s][1].z, u[s][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    gv[i] += ga[i];
+                    uv[i] += ua[i];
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            h[k][i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i];
+            amax = fmaxf(amax, fabsf(h[k][i]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) s_max[wid] = amax;
+    __syncthreads();
+    amax = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
+    const float inv = quant_inv(amax);
+#pragma unroll
+    for (int k = 0; k < kRuns; ++k) {
+        const int run = tid + kQThreads * k;
+        if (kQThreads * k >= runs) break;   // uniform: the whole block is past the end
+        int sum = 0;
+        if (run < runs) {
+            const uint2 pk = quant_pack8(h[k], inv, sum);
+            *reinterpret_cast<uint2 *>(q + run * 8) = pk;
+            if (canon) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) canon[run * 8 + i] = (int8_t)quant_code(h[k][i], inv);
+            }
+        }
+        // the 4 runs of a 32-element chunk are 4 consecutive lanes
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if ((lane & 3) == 0 && run < runs) csum[run / 4] = sum;
+    }
+    if (tid == 0) {
+        *scale = quant_scale(amax);
+        if (canon_scale) *canon_scale = quant_scale(amax);
+    }
+}
+
 // h rows: [0, first) of n_first values (the shared expert), then the routed pair rows,
 // as many as *rest_count (device value; null = none), of n_rest values.  With S > 1 the
-// gate/up rows were sliced: h = SiLU(gate) * up is formed here from the S partial planes
-// (added in slice order) into shared memory, then quantised.
+// gate/up rows were sliced and h is formed from the slice planes (quant_h_planes_block).
 __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restrict__ h, int ld,
                                                             int first, int n_first, int n_rest,
                                                             const int32_t *rest_count,
@@ -85,7 +167,6 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
                                                             const float *__restrict__ upart,
                                                             int S, int64_t plane)
 {
-    extern __shared__ __align__(16) float s_h[];
     pdl_wait();
     pdl_launch_dependents();
     const int row = blockIdx.x;
@@ -94,22 +175,15 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
     const bool routed = row >= first;
     const int n = routed ? n_rest : n_first;
     const size_t pr = (size_t)(row - routed_rowbase);
-    const float *v = h + (size_t)row * ld;
-    if (S > 1) {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            float gate = 0.0f, up = 0.0f;
-            for (int s = 0; s < S; ++s) {
-                gate += gpart[s * plane + (int64_t)row * ld + i];
-                up += upart[s * plane + (int64_t)row * ld + i];
-            }
-            s_h[i] = gate / (1.0f + expf(-gate)) * up;
-        }
-        __syncthreads();
-        v = s_h;
-    }
-    quant_row_block(v, n, dst.q + (size_t)row * dst.q_ld, dst.csum + (size_t)row * dst.c_ld,
-                    dst.scale + row, (routed && probe_hq) ? probe_hq + pr * n : nullptr,
-                    (routed && probe_hs) ? probe_hs + pr : nullptr);
+    int8_t *canon = (routed && probe_hq) ? probe_hq + pr * n : nullptr;
+    float *canon_scale = (routed && probe_hs) ? probe_hs + pr : nullptr;
+    if (S > 1)
+        quant_h_planes_block(gpart + (size_t)row * ld, upart + (size_t)row * ld, S, plane, n,
+                             dst.q + (size_t)row * dst.q_ld, dst.csum + (size_t)row * dst.c_ld,
+                             dst.scale + row, canon, canon_scale);
+    else
+        quant_row_block(h + (size_t)row * ld, n, dst.q + (size_t)row * dst.q_ld,
+                        dst.csum + (size_t)row * dst.c_ld, dst.scale + row, canon, canon_scale);
 }
 
 }  // namespace
@@ -128,14 +202,7 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
     if (max_rows <= 0) return cudaSuccess;
     const int32_t *rest = a.include_routed ? a.offsets + a.E : nullptr;
     const int S = a.slice_gu ? a.geo_gu[0].S : 1;
-    const size_t smem = S > 1 ? sizeof(float) * (size_t)a.hstride : 0;
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(quant_h_kernel,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_kernel(quant_h_kernel, dim3(max_rows), dim3(kQThreads), smem, st, 1,
+    return launch_kernel(quant_h_kernel, dim3(max_rows), dim3(kQThreads), 0, st, 1,
                          (const float *)a.h, a.hstride, first_rows, n_first, n_rest, rest,
                          a.routed_rowbase, a.hq, a.probe.hq, a.probe.h_scale,
                          (const float *)a.gpart, (const float *)a.upart, S,

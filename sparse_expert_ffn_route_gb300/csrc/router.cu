@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const float *__restr
 }
 
 constexpr int kExpertsPerCluster = 16;
+constexpr int kRouteStageT = 32;   // tokens of x staged in shared memory at a time
+
+size_t router_stage_bytes(int H, int cs) { return sizeof(float) * kRouteStageT * (H / cs); }
 
 // Decode-sized batches: logits of 16 experts x all T tokens per cluster, x quantisation.
 // MAXU bounds the float4 units of the H slice that one lane holds per expert.
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__r
 {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
+    extern __shared__ __align__(16) char router_smem[];
     __shared__ float s_part[kRouteClusterMaxT][kExpertsPerCluster];
     __shared__ float s_amax[kRouteClusterMaxT];
     __shared__ float s_red[8];
@@ -136,31 +140,48 @@ __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__r
             }
         }
     }
-    for (int t = 0; t < T; ++t) {
-        const float *xr = x + (size_t)t * H + k0;
-        float acc[2] = {0.f, 0.f};
+    // x slices of kRouteStageT tokens at a time, staged in shared memory by cp.async; each
+    // warp then forms its two experts' partial logits for 16 tokens at once and sums the 32
+    // values over its lanes with one reduce-scatter (lane l: expert l / 16, token l % 16)
+    float4 *s_x = reinterpret_cast<float4 *>(router_smem);
+    for (int t0 = 0; t0 < T; t0 += kRouteStageT) {
+        const int nt = min(kRouteStageT, T - t0);
+        for (int idx = tid; idx < nt * nunit; idx += blockDim.x) {
+            const int tt = idx / nunit, u = idx - tt * nunit;
+            cp_async16(s_x + idx, x + (size_t)(t0 + tt) * H + k0 + u * 4, true);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        for (int tg = 0; tg < nt; tg += 16) {
+            float acc[32];
 #pragma unroll
-        for (int u = 0; u < MAXU; ++u) {
-            const int idx = u * 32 + lane;
-            if (idx < nunit) {
-                const float4 xv = __ldg(reinterpret_cast<const float4 *>(xr + idx * 4));
+            for (int o = 0; o < 32; ++o) acc[o] = 0.0f;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    acc[j] = fmaf(xv.x, wv[j][u].x, acc[j]);
-                    acc[j] = fmaf(xv.y, wv[j][u].y, acc[j]);
-                    acc[j] = fmaf(xv.z, wv[j][u].z, acc[j]);
-                    acc[j] = fmaf(xv.w, wv[j][u].w, acc[j]);
+            for (int u = 0; u < MAXU; ++u) {
+                const int idx = u * 32 + lane;
+                if (idx < nunit) {
+#pragma unroll
+                    for (int tt = 0; tt < 16; ++tt) {
+                        if (tg + tt < nt) {
+                            const float4 xv = s_x[(tg + tt) * nunit + idx];
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                float &a_ = acc[j * 16 + tt];
+                                a_ = fmaf(xv.x, wv[j][u].x, a_);
+                                a_ = fmaf(xv.y, wv[j][u].y, a_);
+                                a_ = fmaf(xv.z, wv[j][u].z, a_);
+                                a_ = fmaf(xv.w, wv[j][u].w, a_);
+                            }
+                        }
+                    }
                 }
             }
+            ReduceScatter<32, 16>::run(acc, lane);
+            const int tt = lane & 15;
+            if (tg + tt < nt) s_part[t0 + tg + tt][2 * wid + (lane >> 4)] = acc[0];
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-        if (lane == 0) {
-            s_part[t][2 * wid] = acc[0];
-            s_part[t][2 * wid + 1] = acc[1];
-        }
+        __syncthreads();   // before the next slice of x overwrites s_x
     }
     // |x| maximum of this slice for the tokens this cluster quantises
     if (quant) {
@@ -230,8 +251,6 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *__restr
                                                             float *__restrict__ w,
                                                             int32_t *__restrict__ keff)
 {
-    __shared__ int s_sel[8][kMaxTopK];
-    __shared__ float s_g[8][kMaxTopK];
     pdl_wait();
     pdl_launch_dependents();
     const int wid = threadIdx.x >> 5;
@@ -243,7 +262,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *__restr
         for (int s = 0; s < S; ++s) l += part[((size_t)s * T + t) * E + e];
         return l;
     };
-    select_token(p, logit, t, s_sel[wid], s_g[wid], ids, w, keff);
+    select_token(p, logit, t, ids, w, keff);
 }
 
 }  // namespace
@@ -277,14 +296,14 @@ cudaError_t launch_router_logits(const moe_config &c, const float *x, const floa
         const dim3 grid(cs * ((E + kExpertsPerCluster - 1) / kExpertsPerCluster));
         const QuantRows q = xq ? *xq : QuantRows{};
         const int quant = xq ? 1 : 0;
-        if (units <= 2)
-            return launch_kernel(router_cluster_kernel<2>, grid, dim3(256), 0, st, cs, x, wr, T, H,
-                                 E, scratch, q, quant);
-        if (units <= 4)
-            return launch_kernel(router_cluster_kernel<4>, grid, dim3(256), 0, st, cs, x, wr, T, H,
-                                 E, scratch, q, quant);
-        return launch_kernel(router_cluster_kernel<8>, grid, dim3(256), 0, st, cs, x, wr, T, H, E,
-                             scratch, q, quant);
+        const size_t smem = router_stage_bytes(H, cs);
+        auto go = [&](auto kernel) {
+            return launch_kernel(kernel, grid, dim3(256), smem, st, cs, x, wr, T, H, E, scratch,
+                                 q, quant);
+        };
+        if (units <= 2) return go(router_cluster_kernel<2>);
+        if (units <= 4) return go(router_cluster_kernel<4>);
+        return go(router_cluster_kernel<8>);
     }
     const int S = router_splits(c, T);
     *splits = S;

@@ -30,111 +30,114 @@ inline SelectParams select_params(const moe_config &c, const float *bias)
     return p;
 }
 
-struct Cand {
-    float v;   // choice = sig + bias
-    float g;   // sig (the applied gate)
-    int e;     // expert id, INT_MAX = none
-};
-
-__device__ __forceinline__ bool cand_better(const Cand &a, const Cand &b)
+// Order-preserving map of an fp32 value (not NaN) to uint32, so that comparing keys as
+// unsigned integers compares the values.  -0 is first turned into +0 (x + 0 in round to
+// nearest), so values that compare equal as fp32 get equal keys.  Every key is above 0,
+// which marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float v)
 {
-    // a beats b: any candidate beats none; larger choice wins; equal choice -> lower id
-    if (b.e == 0x7fffffff) return a.e != 0x7fffffff;
-    if (a.e == 0x7fffffff) return false;
-    return a.v > b.v || (a.v == b.v && a.e < b.e);
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp; logit(e) returns token t's router logit of expert e.  sel / g are this warp's
-// kMaxTopK-entry shared-memory scratch.  Writes ids/w of the token (K entries: the kept ones
-// in order, then -1 / 0) and keff[t]; also the ids to sm_ids[0..K) and keff to *sm_keff
-// when those are non-null.
+// One warp; logit(e) returns token t's router logit of expert e.  Writes ids/w of the token
+// (K entries: the kept ones in order, then -1 / 0) and keff[t]; also the ids to sm_ids[0..K)
+// and keff to *sm_keff when those are non-null.
+//
+// Each of the K rounds takes, over the experts not chosen yet, the largest choice value
+// (ties to the lower id): every lane finds its best candidate among its experts
+// e = lane + 32j, one warp max-reduction finds the best value and one min-reduction the
+// lowest id holding it.  After the rounds lane k holds the k-th choice; top-p, the sums
+// (sequential, in the oracle's order) and the divisions then run on those lanes.
 template <typename LogitFn>
-__device__ void select_token(const SelectParams &p, LogitFn logit, int t, int *sel, float *g,
+__device__ void select_token(const SelectParams &p, LogitFn logit, int t,
                              int32_t *__restrict__ ids, float *__restrict__ w,
                              int32_t *__restrict__ keff, int *sm_ids = nullptr,
                              int *sm_keff = nullptr)
 {
     constexpr int kPerLane = kMaxExperts / 32;
+    constexpr unsigned kAll = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int E = p.E, K = p.K;
 
-    float sig[kPerLane], ch[kPerLane];
+    float sig[kPerLane];
+    uint32_t key[kPerLane];
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) {
         const int e = lane + 32 * j;
         sig[j] = 0.0f;
-        ch[j] = 0.0f;
+        key[j] = 0u;
         if (e < E) {
             const float l = logit(e);
             sig[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-            ch[j] = __fadd_rn(sig[j], p.bias[e]);
+            key[j] = order_key(__fadd_rn(sig[j], p.bias[e]));
         }
     }
 
-    unsigned taken = 0;
+    int my_id = -1;       // lane k < K: the k-th chosen expert
+    float my_g = 0.0f;    // and its gate (the unbiased sigmoid)
     for (int k = 0; k < K; ++k) {
-        Cand best{0.0f, 0.0f, 0x7fffffff};
+        uint32_t bk = 0u;
+        int bj = 0;
+        float bg = 0.0f;
 #pragma unroll
         for (int j = 0; j < kPerLane; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u)) {
-                const Cand c{ch[j], sig[j], e};
-                if (cand_better(c, best)) best = c;
+            if (key[j] > bk) {   // strict: the lower id of this lane wins a tie
+                bk = key[j];
+                bj = j;
+                bg = sig[j];
             }
         }
+        const uint32_t wk = __reduce_max_sync(kAll, bk);
+        const uint32_t mine = (bk == wk && bk != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+        const uint32_t we = __reduce_min_sync(kAll, mine);
+        const float wg = __shfl_sync(kAll, bg, (int)(we & 31u));
+        if (mine == we) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            Cand o;
-            o.v = __shfl_xor_sync(0xffffffffu, best.v, off);
-            o.g = __shfl_xor_sync(0xffffffffu, best.g, off);
-            o.e = __shfl_xor_sync(0xffffffffu, best.e, off);
-            if (cand_better(o, best)) best = o;
+            for (int j = 0; j < kPerLane; ++j)
+                if (j == bj) key[j] = 0u;
         }
-        if ((best.e & 31) == lane) taken |= 1u << (best.e >> 5);
-        if (lane == 0) {
-            sel[k] = best.e;
-            g[k] = best.g;
+        if (lane == k) {
+            my_id = (int)we;
+            my_g = wg;
         }
     }
-    __syncwarp();
 
-    if (lane == 0) {
-        int m = K;
-        if (p.top_p > 0.0f && p.top_p < 1.0f) {
-            // stable insertion sort of the kept gates, descending
-            for (int i = 1; i < K; ++i) {
-                const float gv = g[i];
-                const int sv = sel[i];
-                int j = i;
-                while (j > 0 && g[j - 1] < gv) {
-                    g[j] = g[j - 1];
-                    sel[j] = sel[j - 1];
-                    --j;
-                }
-                g[j] = gv;
-                sel[j] = sv;
-            }
-            float tot = 0.0f;
-            for (int i = 0; i < K; ++i) tot = __fadd_rn(tot, g[i]);
-            const float thr = __fmul_rn(p.top_p, tot);
-            float cum = 0.0f;
-            for (int i = 0; i < K; ++i) {
-                cum = __fadd_rn(cum, g[i]);
-                if (cum >= thr) {
-                    m = i + 1;
-                    break;
-                }
-            }
+    int m = K;
+    if (p.top_p > 0.0f && p.top_p < 1.0f) {
+        // stable sort of the K choices by gate, descending: lane i's rank
+        int rank = 0;
+        for (int j = 0; j < K; ++j) {
+            const float gj = __shfl_sync(kAll, my_g, j);
+            rank += (gj > my_g || (gj == my_g && j < lane)) ? 1 : 0;
         }
-        float ssum = 0.0f;
-        for (int i = 0; i < m; ++i) ssum = __fadd_rn(ssum, g[i]);
+        int src = 0;
+        for (int j = 0; j < K; ++j) src = __shfl_sync(kAll, rank, j) == lane ? j : src;
+        my_g = __shfl_sync(kAll, my_g, src);
+        my_id = __shfl_sync(kAll, my_id, src);
+        // sequential sums, in every lane alike
+        float tot = 0.0f;
+        for (int i = 0; i < K; ++i) tot = __fadd_rn(tot, __shfl_sync(kAll, my_g, i));
+        const float thr = __fmul_rn(p.top_p, tot);
+        float cum = 0.0f;
         for (int i = 0; i < K; ++i) {
-            const size_t o = (size_t)t * K + i;
-            const int id = i < m ? sel[i] : -1;
-            w[o] = i < m ? __fmul_rn(p.norm ? __fdiv_rn(g[i], ssum) : g[i], p.scale) : 0.0f;
-            ids[o] = id;
-            if (sm_ids) sm_ids[i] = id;
+            cum = __fadd_rn(cum, __shfl_sync(kAll, my_g, i));
+            if (cum >= thr) {
+                m = i + 1;
+                break;
+            }
         }
+    }
+    float ssum = 0.0f;
+    for (int i = 0; i < m; ++i) ssum = __fadd_rn(ssum, __shfl_sync(kAll, my_g, i));
+    if (lane < K) {
+        const size_t o = (size_t)t * K + lane;
+        const int id = lane < m ? my_id : -1;
+        w[o] = lane < m ? __fmul_rn(p.norm ? __fdiv_rn(my_g, ssum) : my_g, p.scale) : 0.0f;
+        ids[o] = id;
+        if (sm_ids) sm_ids[lane] = id;
+    }
+    if (lane == 0) {
         keff[t] = m;
         if (sm_keff) *sm_keff = m;
     }
