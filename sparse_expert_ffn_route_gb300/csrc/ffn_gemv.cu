@@ -69,6 +69,18 @@ void ffn_configure(FfnArgs &a)
 {
     const bool sh = a.n_shared != 0;
     const bool small = a.T <= kRouteClusterMaxT;
+    // batches beyond the decode route: the tensor-core grouped GEMM (ffn_tc.cu)
+    a.tensor = (!small && ffn_tc_supported(a)) ? 1 : 0;
+    if (a.tensor) {
+        a.slice_gu = 0;
+        a.slice_dn = 0;
+        a.tc_gu = a.tc_dn = 128;
+        a.geo_gu[0] = make_tc_geo(a.H, a.F, 2);
+        a.geo_gu[1] = make_tc_geo(a.H, a.Fs, 2);
+        a.geo_dn[0] = make_tc_geo(a.F, a.H, 1);
+        a.geo_dn[1] = make_tc_geo(a.Fs, a.H, 1);
+        return;
+    }
     const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;
     const bool sgu = small && a.slice_gu && a.H > 32 * kSliceChunks;
     const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks &&
@@ -92,11 +104,13 @@ void ffn_configure(FfnArgs &a)
 
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st)
 {
+    if (a.tensor) return launch_ffn_tc(true, a, st);
     return launch(choose(true, max_nc(a.geo_gu, a.n_shared != 0), a.tc_gu, probes_gu(a)), a, st);
 }
 
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st)
 {
+    if (a.tensor) return launch_ffn_tc(false, a, st);
     return launch(choose(false, max_nc(a.geo_dn, a.n_shared != 0), a.tc_dn, probes_dn(a)), a, st);
 }
 

@@ -54,6 +54,25 @@ __host__ __device__ inline Geo make_geo(int kdim, int nrows, int ru, bool full, 
     return g;
 }
 
+// Geometry of the tensor-core path: 128-row tiles of `matrices` matrices (gate and up, or
+// down) over the whole reduction; the matrix index takes the place of the slice.
+__host__ __device__ inline Geo make_tc_geo(int kdim, int nrows, int matrices)
+{
+    Geo g;
+    g.kdim = kdim;
+    g.nrows = nrows;
+    g.S = matrices;
+    g.sch = kdim / 32;
+    g.lpr = 32;
+    g.rpw = 1;
+    g.nc = 1;
+    g.ru = 128;
+    g.rb = 128;
+    g.rowbytes = kdim / 2;
+    g.G = kdim / 64;
+    return g;
+}
+
 // Tasks of a slot: (token chunk of at most tc tokens, slice, row block), in that order of
 // significance.
 __host__ __device__ __forceinline__ int tasks_of(const Geo &g, int ntok, int tc)

@@ -171,7 +171,7 @@ size_t logits_rows(const moe_config &c, int T)
 int fmax_of(const moe_config &c) { return c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff; }
 
 // Fields common to every FFN call; the caller sets n_shared / include_routed / weights /
-// lists / outputs and then calls ffn_configure().
+// lists / outputs and then calls configure_ffn().
 FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
 {
     FfnArgs a;
@@ -200,6 +200,16 @@ FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
     a.hq.q_ld = a.hstride;
     a.hq.c_ld = a.hstride / 32;
     return a;
+}
+
+// the bf16 copies of the codes feed the tensor-core path only
+void configure_ffn(FfnArgs &a, void *ws, const WsLayout &L)
+{
+    ffn_configure(a);
+    a.xq.bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.xbf) : nullptr;
+    a.hq.bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.hbf) : nullptr;
+    a.x_bf16 = a.xq.bf16;
+    a.h_bf16 = a.hq.bf16;
 }
 
 // gate/up -> quantise h -> down, each stage optionally bracketed by events
@@ -356,8 +366,14 @@ WsLayout ws_layout(const moe_config &c, int T)
     const size_t s_gu = (H + 32 * kSliceChunks - 1) / (32 * kSliceChunks);
     const size_t s_dn = (fm + 32 * kSliceChunks - 1) / (32 * kSliceChunks);
     L.h = take(rows * fm * 4);
-    L.hp_plane_floats = s_gu > 1 ? s_gu * rows_s * fm : 0;
+    // gate/up planes: per-slice planes of the decode route, or one plane per matrix on the
+    // tensor-core path (batches beyond kRouteClusterMaxT)
+    const size_t hp_sliced = s_gu > 1 ? s_gu * rows_s * fm : 0;
+    const size_t hp_tensor = T > kRouteClusterMaxT ? rows * fm : 0;
+    L.hp_plane_floats = hp_sliced > hp_tensor ? hp_sliced : hp_tensor;
     L.hp = take(2 * L.hp_plane_floats * 4);
+    L.xbf = take(T > kRouteClusterMaxT ? (size_t)T * H * 2 : 0);
+    L.hbf = take(T > kRouteClusterMaxT ? rows * fm * 2 : 0);
     L.hq = take(rows * fm);
     L.hscale = take(rows * 4);
     L.hcsum = take(rows * (fm / 32) * 4);
@@ -458,7 +474,7 @@ int moe_expert_ffn(const moe_config *cfg, const float *x, int T, const moe_exper
     a.plane_rows = T * cfg->top_k;
     a.slice_dn = 0;   // y_pairs holds one plane
     if (probe) a.probe = *probe;
-    ffn_configure(a);
+    configure_ffn(a, workspace, L);
     cudaError_t e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
     if (e == cudaSuccess) e = launch_plan(a, uniq, n_uniq, at<FfnPlan>(workspace, L.plan), st);
     if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 0, true, false, st);
@@ -503,7 +519,7 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
         a.routed_rowbase = T;
         a.plane_rows = T;
         a.slice_dn = 1;
-        ffn_configure(a);
+        configure_ffn(a, workspace, L);
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
         if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 1, false, false, st);
@@ -582,7 +598,7 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     a.routed_rowbase = T * ns;
     a.plane_rows = T * ns + T * cfg->top_k;
     a.slice_dn = 1;
-    ffn_configure(a);
+    configure_ffn(a, workspace, L);
 
     const bool ev = (flags & MOE_FLAG_STAGE_EVENTS) != 0;
     float *logits = at<float>(workspace, L.logits);

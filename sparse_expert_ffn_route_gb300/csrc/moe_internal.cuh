@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda_bf16.h>
+
 #include "moe.h"
 #include "ffn_tiles.cuh"
 
@@ -25,6 +27,7 @@ constexpr int kMaxCombinePlanes = 2;
 // device-side error word bits (workspace `err`)
 constexpr int kErrBadExpertId = 1;
 constexpr int kErrBadKeff = 2;
+constexpr int kErrTimeout = 4;     // a bounded device-side wait gave up
 
 // ---------------------------------------------------------------------------
 // Work plan of the grouped expert FFN.  A "slot" is one expert applied to its
@@ -51,11 +54,13 @@ struct FfnPlan {
 // elements as [e0 e2 e4 e6 | e1 e3 e5 e7] (the even/odd split that the packed
 // nibbles' low/high halves line up with), the row scale, and the sum of the
 // codes of every 32-element chunk (for the zero-point-8 correction).
+// (cuda_bf16.h is included above)
 struct QuantRows {
     int8_t *q;       // [rows][q_ld]
     float *scale;    // [rows]
     int32_t *csum;   // [rows][c_ld], c_ld >= n/32
     int q_ld, c_ld;
+    __nv_bfloat16 *bf16;   // nullable: [rows][q_ld] the codes again as bf16, element order
 };
 
 struct FfnArgs {
@@ -78,6 +83,9 @@ struct FfnArgs {
     float *gpart, *upart;             // [S_gate/up][plane_rows][hstride] partial gate / up
     int plane_rows;                   // output rows of the call (shared rows + routed pairs)
     int slice_gu, slice_dn;           // rows cut into 1024-input slices
+    int tensor;                       // the tcgen05 path (ffn_tc.cu) runs gate/up and down
+    const __nv_bfloat16 *x_bf16;      // [T][H] the codes of x as bf16 (tensor path)
+    __nv_bfloat16 *h_bf16;            // [rows][hstride] the codes of h as bf16 (tensor path)
     int tc_gu, tc_dn;                 // token chunk per task
     Geo geo_gu[2], geo_dn[2];         // task geometry: [0] routed experts, [1] shared expert
     moe_ffn_probe probe;              // routed pairs only; row index = pair
@@ -94,6 +102,7 @@ struct WsLayout {
     size_t xq, xscale, xcsum;         // quantised x
     size_t h;                         // [rows][Fmax] fp32
     size_t hp, hp_plane_floats;       // partial gate planes then partial up planes
+    size_t xbf, hbf;                  // bf16 codes of x and h (tensor path)
     size_t hq, hscale, hcsum;         // quantised h
     size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
     size_t plan;                      // FfnPlan
@@ -141,6 +150,9 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
 // host-side choice of the FFN kernels' tile shape and pipeline depth
 void ffn_configure(FfnArgs &a);
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);
+// tensor-core path (ffn_tc.cu): whole 128-row tiles of every matrix of the call
+bool ffn_tc_supported(const FfnArgs &a);
+cudaError_t launch_ffn_tc(bool gate_up, const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 // pair_of (nullable) gives each (t, i) its list position directly; without it the position
 // is found by binary search in the expert's token list.  S_r / S_s slice planes (plane

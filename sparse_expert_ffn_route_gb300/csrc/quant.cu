@@ -2,6 +2,8 @@
 // layer and shared by every expert that reads the token ["colibri 开发演进实录" §2.2:
 // activation quantisation hoisted to the layer], and of h = SiLU(gate)*up before the down
 // projection.  One CTA per row.
+#include <cuda_bf16.h>
+
 #include "device_util.cuh"
 #include "launch.cuh"
 #include "moe_internal.cuh"
@@ -11,6 +13,16 @@ namespace moe {
 namespace {
 
 constexpr int kQThreads = 256;
+
+// the int8 codes of 8 consecutive values as bf16 (exact), element order, 16 bytes
+__device__ __forceinline__ void store_codes_bf16(__nv_bfloat16 *dst, const float v[8], float inv)
+{
+    __nv_bfloat162 p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p[i] = __floats2bfloat162_rn((float)quant_code(v[2 * i], inv), (float)quant_code(v[2 * i + 1], inv));
+    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(p);
+}
 constexpr int kMaxSlices = kMaxDim / (32 * kSliceChunks);   // slices of a row of kMaxDim inputs
 
 // Quantises one row of n values (n a multiple of 32) with the whole block: codes in runs of
@@ -18,7 +30,8 @@ constexpr int kMaxSlices = kMaxDim / (32 * kSliceChunks);   // slices of a row o
 // canon (nullable) receives the codes in element order.
 __device__ void quant_row_block(const float *__restrict__ v, int n, int8_t *__restrict__ q,
                                 int32_t *__restrict__ csum, float *__restrict__ scale,
-                                int8_t *__restrict__ canon, float *__restrict__ canon_scale)
+                                int8_t *__restrict__ canon, float *__restrict__ canon_scale,
+                                __nv_bfloat16 *__restrict__ qb)
 {
     __shared__ float s_max[kQThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -51,6 +64,7 @@ __device__ void quant_row_block(const float *__restrict__ v, int n, int8_t *__re
 #pragma unroll
                 for (int i = 0; i < 8; ++i) canon[run * 8 + i] = (int8_t)quant_code(x[i], inv);
             }
+            if (qb) store_codes_bf16(qb + run * 8, x, inv);
         }
         // the 4 runs of a 32-element chunk are 4 consecutive lanes
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -70,7 +84,8 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
     pdl_launch_dependents();
     const int row = blockIdx.x;
     quant_row_block(src + (size_t)row * stride, n, dst.q + (size_t)row * dst.q_ld,
-                    dst.csum + (size_t)row * dst.c_ld, dst.scale + row, nullptr, nullptr);
+                    dst.csum + (size_t)row * dst.c_ld, dst.scale + row, nullptr, nullptr,
+                    dst.bf16 ? dst.bf16 + (size_t)row * dst.q_ld : nullptr);
 }
 
 // Sliced gate/up rows: h = SiLU(gate) * up of the row, gate and up each the sum of the S
@@ -79,7 +94,8 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
 __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *__restrict__ up,
                                      int S, int64_t plane, int n, int8_t *__restrict__ q,
                                      int32_t *__restrict__ csum, float *__restrict__ scale,
-                                     int8_t *__restrict__ canon, float *__restrict__ canon_scale)
+                                     int8_t *__restrict__ canon, float *__restrict__ canon_scale,
+                                     __nv_bfloat16 *__restrict__ qb)
 {
     constexpr int kRuns = kMaxDim / 8 / kQThreads;   // runs per thread, at most
     __shared__ float s_max[kQThreads / 32];
@@ -143,6 +159,7 @@ __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *
 #pragma unroll
                 for (int i = 0; i < 8; ++i) canon[run * 8 + i] = (int8_t)quant_code(h[k][i], inv);
             }
+            if (qb) store_codes_bf16(qb + run * 8, h[k], inv);
         }
         // the 4 runs of a 32-element chunk are 4 consecutive lanes
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -156,8 +173,9 @@ __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *
 }
 
 // h rows: [0, first) of n_first values (the shared expert), then the routed pair rows,
-// as many as *rest_count (device value; null = none), of n_rest values.  With S > 1 the
-// gate/up rows were sliced and h is formed from the slice planes (quant_h_planes_block).
+// as many as *rest_count (device value; null = none), of n_rest values.  With `planes` the
+// gate/up kernel left gate and up in planes (S per-slice planes of sliced rows, or one plane
+// each from the tensor-core path) and h is formed from them (quant_h_planes_block).
 __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restrict__ h, int ld,
                                                             int first, int n_first, int n_rest,
                                                             const int32_t *rest_count,
@@ -165,7 +183,7 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
                                                             int8_t *probe_hq, float *probe_hs,
                                                             const float *__restrict__ gpart,
                                                             const float *__restrict__ upart,
-                                                            int S, int64_t plane)
+                                                            int planes, int S, int64_t plane)
 {
     pdl_wait();
     pdl_launch_dependents();
@@ -177,13 +195,14 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
     const size_t pr = (size_t)(row - routed_rowbase);
     int8_t *canon = (routed && probe_hq) ? probe_hq + pr * n : nullptr;
     float *canon_scale = (routed && probe_hs) ? probe_hs + pr : nullptr;
-    if (S > 1)
+    __nv_bfloat16 *qb = dst.bf16 ? dst.bf16 + (size_t)row * dst.q_ld : nullptr;
+    if (planes)
         quant_h_planes_block(gpart + (size_t)row * ld, upart + (size_t)row * ld, S, plane, n,
                              dst.q + (size_t)row * dst.q_ld, dst.csum + (size_t)row * dst.c_ld,
-                             dst.scale + row, canon, canon_scale);
+                             dst.scale + row, canon, canon_scale, qb);
     else
         quant_row_block(h + (size_t)row * ld, n, dst.q + (size_t)row * dst.q_ld,
-                        dst.csum + (size_t)row * dst.c_ld, dst.scale + row, canon, canon_scale);
+                        dst.csum + (size_t)row * dst.c_ld, dst.scale + row, canon, canon_scale, qb);
 }
 
 }  // namespace
@@ -201,11 +220,13 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
 {
     if (max_rows <= 0) return cudaSuccess;
     const int32_t *rest = a.include_routed ? a.offsets + a.E : nullptr;
-    const int S = a.slice_gu ? a.geo_gu[0].S : 1;
+    // gate/up left per-slice planes (sliced rows) or one plane per matrix (tensor path)
+    const int S = a.tensor ? 1 : (a.slice_gu ? a.geo_gu[0].S : 1);
+    const int planes = (a.tensor || S > 1) ? 1 : 0;
     return launch_kernel(quant_h_kernel, dim3(max_rows), dim3(kQThreads), 0, st, 1,
                          (const float *)a.h, a.hstride, first_rows, n_first, n_rest, rest,
                          a.routed_rowbase, a.hq, a.probe.hq, a.probe.h_scale,
-                         (const float *)a.gpart, (const float *)a.upart, S,
+                         (const float *)a.gpart, (const float *)a.upart, planes, S,
                          (int64_t)a.plane_rows * a.hstride);
 }
 

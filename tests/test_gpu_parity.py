@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from helpers import device_experts, moe_cfg, oracle_tokens, rel_err, routing_margins
+from helpers import tokens_within, device_experts, moe_cfg, oracle_tokens, rel_err, routing_margins
 
 pytestmark = pytest.mark.gpu
 
@@ -188,7 +188,8 @@ def _ffn_both(moe, wl, T, batch=0, probes=True):
     return g, ref, perm
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 3), ("a3b_decode", 64)])
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 3), ("a3b_decode", 64),
+                                    ("a3b_decode", 96), ("a3b_decode", 200)])
 def test_expert_ffn_exact_accumulators(moe, name, T):
     wl = synth.WORKLOADS[name]
     g, ref, perm = _ffn_both(moe, wl, T)
@@ -202,7 +203,11 @@ def test_expert_ffn_exact_accumulators(moe, name, T):
     assert same.mean() > 0.9
     assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
     np.testing.assert_allclose(g["h_scale"], ref["hs"], rtol=1e-5)
-    assert rel_err(g["y"], ref["y_pairs"]) <= TOL
+    # identical codes: the outputs differ only by fp32 rounding of the scale arithmetic
+    assert rel_err(g["y"][same], ref["y_pairs"][same]) <= TOL
+    # a code one step away (h at a rounding boundary) moves the row by about one code's
+    # share, hs * |w| of a few elements out of F
+    assert rel_err(g["y"], ref["y_pairs"]) <= 20 * TOL
 
 
 def test_expert_ffn_glm_full_width(moe):
@@ -213,7 +218,8 @@ def test_expert_ffn_glm_full_width(moe):
     assert np.array_equal(g["acc_up"], ref["acc_up"])
     same = np.all(g["hq"] == ref["hq"], axis=1)
     assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
-    assert rel_err(g["y"], ref["y_pairs"]) <= TOL
+    assert rel_err(g["y"][same], ref["y_pairs"][same]) <= TOL
+    assert rel_err(g["y"], ref["y_pairs"]) <= 20 * TOL
 
 
 def _layer_gpu(moe, wl, x, wr, bias, routing=True):
@@ -230,7 +236,8 @@ def _layer_gpu(moe, wl, x, wr, bias, routing=True):
     return y.cpu().numpy(), {k: v.cpu().numpy() for k, v in rt.items()}
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("a3b_decode", 64)])
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("a3b_decode", 64),
+                                    ("a3b_decode", 128)])
 def test_layer_forward(moe, name, T):
     wl = synth.WORKLOADS[name]
     x, wr, bias = _inputs(wl, T)
@@ -241,7 +248,7 @@ def test_layer_forward(moe, name, T):
     clear = routing_margins(logits, bias.numpy(), wl.top_k, wl.top_p) > TIE
     assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
     assert np.isfinite(y).all()
-    assert rel_err(y[clear], ref["y"][clear]) <= TOL
+    tokens_within(y[clear], ref["y"][clear], TOL)
 
 
 @pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 32, [0, 13, 31]),
@@ -260,7 +267,7 @@ def test_layer_forward_full_size_sampled(moe, name, T, sample):
     rows = [t for t in sample if margin[t] > TIE]
     assert rows
     yref = oracle_tokens(wl, x.numpy()[rows], ref["ids"][rows], ref["w"][rows], ref["keff"][rows])
-    assert rel_err(y[rows], yref) <= TOL
+    tokens_within(y[rows], yref, TOL)
 
 
 def test_combine_with_shared(moe):
@@ -313,7 +320,7 @@ def test_edge_cases(moe, case):
     logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
     clear = routing_margins(logits, bias.numpy(), K, top_p) > TIE
     assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
-    assert rel_err(y[clear], ref["y"][clear]) <= TOL
+    tokens_within(y[clear], ref["y"][clear], TOL)
     g, refp, _ = _ffn_both(moe, wl, T)
     assert np.array_equal(g["acc_gate"], refp["acc_gate"])
     assert np.array_equal(g["acc_up"], refp["acc_up"])
