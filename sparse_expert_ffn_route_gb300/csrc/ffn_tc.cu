@@ -10,20 +10,28 @@
 // acc += s[row][g] * A.  The token's activation scale multiplies at the end.
 //
 // Tile: 128 weight rows (one matrix of one expert) x up to 128 tokens of the expert's list;
-// one task per tile, all K groups.  Warp roles in a CTA of 9 warps:
+// one task per tile, all K groups.  Warp roles in a CTA of 14 warps:
 //   warps 0-3  one weight row each per thread: load the row's nibbles of the next groups
-//              from HBM (16-byte non-allocating loads, 8 groups ahead in registers),
-//              convert them to bf16 (u - 8) and store them into the group's A buffer in
-//              TMEM; copy the B tile (the tile's token rows of the bf16 activation codes,
-//              128 bytes per row per group) into a 128-byte-swizzled shared-memory stage
-//              with cp.async, kPre groups ahead.
-//   warp 4     allocates TMEM; one thread issues the 4 MMAs of each group
-//              (A from TMEM, B from shared memory) and commits them to mbarriers.
-//   warps 5-8  the epilogue: per group, the accumulator (32 TMEM lanes = 32 rows each) is
-//              loaded 32 columns at a time and added into registers with the group scale.
-// A groups' stages rotate through kStages A buffers / B stages and 2 accumulators.  Every
-// wait is bounded; a timeout sets the error word, and every role leaves its loops.
+//              from HBM (16-byte non-allocating loads, kNibAhead groups ahead in registers),
+//              convert them to bf16 (u - 8) and store them into the group's A buffer in TMEM.
+//   warp 4     allocates TMEM; one thread issues the 4 MMAs of each group (A from TMEM, B
+//              from shared memory) and commits them to the rings' mbarriers.
+//   warp 5     one thread loads the B tiles: the tile's activation rows (bf16 codes, laid out
+//              in output-row order, 128 bytes per row per group) by 2-D TMA in 16-row boxes
+//              with the 128-byte swizzle, into a ring of kBStages shared-memory stages.
+//   warps 6-13 the epilogue, two warps per 32 TMEM lanes (32 rows), 64 token columns each:
+//              per group the accumulator is loaded 16 columns at a time (the next load in
+//              flight) and added into registers with the group scale (packed fp32x2 FMAs).
+// Groups rotate through kAStages A buffers, kBStages B stages and kDBuf accumulators, each
+// ring with a full and an empty mbarrier; warps arrive once each.  Within every run of 8
+// inputs the contraction runs in the order e0 e4 e1 e5 e2 e6 e3 e7 on both operands (the
+// order in which nibbles unpack cheapest); a group sum does not depend on it.  Every wait is
+// bounded; a timeout sets the error word, and every role leaves its loops.
+#include <cuda.h>           // CUtensorMap and its enums (types only: the encoder is looked up)
+#include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "device_util.cuh"
 #include "ffn_tiles.cuh"
@@ -38,18 +46,22 @@ namespace {
 constexpr int kM = 128;             // weight rows per tile (MMA M)
 constexpr int kN = 128;             // tokens per tile, at most (MMA N)
 constexpr int kGK = 64;             // inputs per group (one scale; 4 MMAs of K = 16)
-constexpr int kStages = 6;          // A buffers (TMEM) and B stages (shared memory)
-constexpr int kPre = kStages - 2;   // B copies run this many groups ahead
-constexpr int kNibAhead = 8;        // groups of nibbles held in registers ahead of use
-constexpr int kThreads = 9 * 32;
+constexpr int kAStages = 4;         // A buffers in TMEM
+constexpr int kBStages = 10;        // B stages in shared memory
+constexpr int kDBuf = 3;            // accumulators in TMEM
+constexpr int kNibAhead = 6;        // groups of nibbles held in registers ahead of use
+constexpr int kBoxRows = 16;        // rows per B copy (one TMA box)
+constexpr int kWarpMma = 4, kWarpTma = 5, kWarpEpi0 = 6;
+constexpr int kEpiWarps = 8;        // two per TMEM lane quarter, 64 token columns each
+constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD = 0;                  // 2 accumulators of kN columns
-constexpr uint32_t kColA = 2 * kN;             // kStages A buffers of 32 columns (64 bf16)
+constexpr uint32_t kColD = 0;                  // kDBuf accumulators of kN columns
+constexpr uint32_t kColA = kDBuf * kN;         // kAStages A buffers of 32 columns (64 bf16)
 constexpr int kBStageBytes = kN * 128;         // 16 KB, 1024-byte aligned
-constexpr int kSmemBytes = kStages * kBStageBytes + 128 * 16 * 4 /* epilogue scales */ +
-                           1024 /* alignment */ + 256 /* barriers */;
+constexpr int kSclFloats = kEpiWarps * 32 * 16;   // the epilogue's scale slots
 
-static_assert(kColA + kStages * 32 <= kTmemCols, "TMEM budget");
+static_assert(kColA + kAStages * 32 <= kTmemCols, "TMEM budget");
+
 
 struct TcTask {
     int slot, e, sh, m, r0, j0, nt, np, rowbase, tokbase, ngroups;
@@ -58,36 +70,41 @@ struct TcTask {
     int rowbytes, G;
 };
 
+// the plan's per-slot arrays, copied into shared memory once per CTA
+struct PlanSmem {
+    int n_slots;
+    int32_t prefix[kMaxSlots + 1], expert[kMaxSlots], ntok[kMaxSlots], tokbase[kMaxSlots],
+        rowbase[kMaxSlots];
+};
+
 // task = (slot, token chunk of kN, matrix, block of 128 rows), numbered like the GEMV tasks
 // (geo: rb = 128, S = matrices, tc = kN)
 template <bool GU>
-__device__ __forceinline__ TcTask tc_task(const FfnArgs &a, int task)
+__device__ __forceinline__ TcTask tc_task(const FfnArgs &a, const PlanSmem &ps, int task)
 {
-    const FfnPlan *plan = a.plan;
-    const int32_t *prefix = GU ? plan->gu_prefix : plan->dn_prefix;
-    int lo = 0, hi = plan->n_slots;
+    int lo = 0, hi = ps.n_slots;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= task) lo = mid;
+        if (ps.prefix[mid] <= task) lo = mid;
         else hi = mid;
     }
     TcTask t;
     t.slot = lo;
-    t.e = plan->expert[lo];
+    t.e = ps.expert[lo];
     t.sh = t.e < 0 ? 1 : 0;
     const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
     const int nblk = g.nrows / kM;
-    const int local = task - prefix[lo];
+    const int local = task - ps.prefix[lo];
     const int cs = local / nblk, blk = local - cs * nblk;
     const int ch = cs / g.S;
     t.m = cs - ch * g.S;
     t.r0 = blk * kM;
     t.j0 = ch * kN;
-    const int ntok = plan->ntok[lo];
+    const int ntok = ps.ntok[lo];
     t.nt = min(kN, ntok - t.j0);
     t.np = (t.nt + 15) & ~15;
-    t.rowbase = plan->rowbase[lo] + t.j0;
-    t.tokbase = plan->tokbase[lo];
+    t.rowbase = ps.rowbase[lo] + t.j0;
+    t.tokbase = ps.tokbase[lo];
     t.ngroups = g.kdim / kGK;
     t.rowbytes = g.rowbytes;
     t.G = g.G;
@@ -101,13 +118,19 @@ __device__ __forceinline__ TcTask tc_task(const FfnArgs &a, int task)
 }
 
 struct TcShared {
-    uint64_t full[kStages];    // A stored + B landed (128 converter threads)
-    uint64_t sfree[kStages];   // the group's MMAs are done with A buffer / B stage
-    uint64_t dfull[2];         // accumulator ready (MMA commit)
-    uint64_t dempty[2];        // accumulator read (128 epilogue threads)
+    uint64_t afull[kAStages];    // A buffer stored (one arrival per converter warp)
+    uint64_t aempty[kAStages];   // the MMAs that read the A buffer are done (commit)
+    uint64_t bfull[kBStages];    // B stage landed (TMA transaction bytes)
+    uint64_t bempty[kBStages];   // the MMAs that read the B stage are done (commit)
+    uint64_t dfull[kDBuf];       // accumulator ready (commit)
+    uint64_t dempty[kDBuf];      // accumulator read (one arrival per epilogue warp)
+    uint64_t mfinal;             // every MMA of the CTA is done (commit before TMEM is freed)
     uint32_t tmem;
     int abort;
 };
+
+constexpr int kSmemBytes = 1024 /* alignment */ + kBStages * kBStageBytes + kSclFloats * 4 +
+                           (int)((sizeof(TcShared) + 15) / 16 * 16) + (int)sizeof(PlanSmem);
 
 __device__ __forceinline__ bool aborted(const TcShared *sh) { return *(volatile const int *)&sh->abort != 0; }
 
@@ -122,50 +145,110 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, TcShared
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t *>(&v); }
 
-// 8 nibbles (elements 8c .. 8c+7: element 2b in the low nibble of byte b, 2b+1 in the high)
-// -> 4 words of bf16 pairs holding u - 8, element order
+// 8 nibbles (elements 8c .. 8c+7 of a row; element n in bits 4n .. 4n+3) -> 4 words of
+// bf16 pairs holding u - 8: word k = (element k, element k + 4), the low half first
 __device__ __forceinline__ void nibbles_to_bf16(uint32_t w, uint32_t *out)
 {
-    const uint32_t L = w & 0x0F0F0F0Fu, Hh = (w >> 4) & 0x0F0F0F0Fu;
-    const uint32_t p01 = __byte_perm(L, Hh, 0x5140);   // lo0 hi0 lo1 hi1
-    const uint32_t p23 = __byte_perm(L, Hh, 0x7362);   // lo2 hi2 lo3 hi3
-    constexpr uint32_t C = 0x43434343u;                // bf16 0x43XX = 128 + XX for XX < 128
-    const uint32_t t[4] = {__byte_perm(p01, C, 0x4140), __byte_perm(p01, C, 0x4342),
-                           __byte_perm(p23, C, 0x4140), __byte_perm(p23, C, 0x4342)};
     const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t[i]);
-        out[i] = bf16x2_bits(__hsub2(v, k136));   // (128 + u) - 136 = u - 8, exact
+    for (int k = 0; k < 4; ++k) {
+        // bf16 0x43XX = 128 + XX for XX < 128: both nibbles become 128 + u
+        const uint32_t t = ((w >> (4 * k)) & 0x000F000Fu) | 0x43004300u;
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+        out[k] = bf16x2_bits(__hsub2(v, k136));   // (128 + u) - 136 = u - 8, exact
     }
 }
 
+// acc0 += s * d0, acc1 += s * d1 as one packed fp32x2 FMA (each lane rounded like fmaf);
+// s2 holds s in both halves
+__device__ __forceinline__ void ffma2(float &acc0, float &acc1, uint64_t s2, uint32_t d0, uint32_t d1)
+{
+    asm("{\n\t.reg .b64 c, b, r;\n\t"
+        "mov.b64 c, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "fma.rn.f32x2 r, %4, b, c;\n\t"
+        "mov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(d0), "r"(d1), "l"(s2));
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing as transaction bytes on bar;
+// executed by a converged warp, issued by one elected lane
+__device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// mbarrier arrival with an expected transaction count, by one elected lane of a converged warp
+__device__ __forceinline__ void arrive_expect_tx_elect(uint32_t bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+// bounded wait by every lane of a converged warp; false (for all lanes) if any lane gave up
+__device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, TcShared *sh, int32_t *err)
+{
+    return __all_sync(0xffffffffu, tc_wait(bar, parity, sh, err));
+}
+
 template <bool GU, bool PROBE>
-__global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_constant__ FfnArgs a)
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_tc_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ CUtensorMap bmap)
 {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     pdl_wait();
     pdl_launch_dependents();
-    // B stages on a 1024-byte boundary (128-byte swizzle atoms), then the control block
+    // B stages on a 1024-byte boundary (128-byte swizzle atoms), the epilogue's scale slots,
+    // the control block, the plan
     uint8_t *bstage = reinterpret_cast<uint8_t *>(((uintptr_t)tc_smem_raw + 1023) & ~(uintptr_t)1023);
-    float *escl = reinterpret_cast<float *>(bstage + kStages * kBStageBytes);   // [128][2][8]
-    TcShared *sh = reinterpret_cast<TcShared *>(escl + 128 * 16);
+    float *escl = reinterpret_cast<float *>(bstage + kBStages * kBStageBytes);
+    TcShared *sh = reinterpret_cast<TcShared *>(escl + kSclFloats);
+    PlanSmem *ps = reinterpret_cast<PlanSmem *>(reinterpret_cast<uint8_t *>(sh) +
+                                                (sizeof(TcShared) + 15) / 16 * 16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = GU ? a.plan->gu_tiles : a.plan->dn_tiles;
+    {
+        const FfnPlan *plan = a.plan;
+        const int ns = plan->n_slots;
+        const int32_t *pre = GU ? plan->gu_prefix : plan->dn_prefix;
+        if (tid == 0) ps->n_slots = ns;
+        for (int k = tid; k <= ns; k += blockDim.x) {
+            ps->prefix[k] = pre[k];
+            if (k < ns) {
+                ps->expert[k] = plan->expert[k];
+                ps->ntok[k] = plan->ntok[k];
+                ps->tokbase[k] = plan->tokbase[k];
+                ps->rowbase[k] = plan->rowbase[k];
+            }
+        }
+    }
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sh->full[i], 128);
-            mbar_init(&sh->sfree[i], 1);
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&sh->afull[i], 4);
+            mbar_init(&sh->aempty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kBStages; ++i) {
+            mbar_init(&sh->bfull[i], 1);
+            mbar_init(&sh->bempty[i], 1);
+        }
+        for (int i = 0; i < kDBuf; ++i) {
             mbar_init(&sh->dfull[i], 1);
-            mbar_init(&sh->dempty[i], 128);
+            mbar_init(&sh->dempty[i], kEpiWarps);
         }
+        mbar_init(&sh->mfinal, 1);
         sh->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kWarpMma) {
         tc::tmem_alloc(&sh->tmem, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -175,142 +258,153 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const uint32_t tmem = sh->tmem;
 
     if (warp < 4) {
-        // ---------------- converters / loaders: thread i owns weight row r0 + i ----------
+        // ---------------- converters: thread i owns weight row r0 + i ---------------------
         const int i = tid;
-        const __nv_bfloat16 *act = GU ? a.x_bf16 : a.h_bf16;
-        const int act_ld = GU ? a.H : a.hstride;
-        // B-copy cursor (kPre groups ahead of the conversion cursor)
-        int ptask = blockIdx.x, pg = 0;
-        TcTask pt;
-        if (ptask < total) pt = tc_task<GU>(a, ptask);
-        long long pit = 0;   // global group index of the B copy cursor
-        auto issue_b = [&]() {
-            // copy B of (ptask, pg) into stage pit % kStages
-            if (ptask < total) {
-                const int st = (int)(pit % kStages);
-                if (pit >= kStages &&
-                    !tc_wait(&sh->sfree[st], (uint32_t)((pit / kStages - 1) & 1), sh, a.err))
-                    return;
-                uint8_t *dst = bstage + st * kBStageBytes;
-                const bool valid = i < pt.nt;
-                int row = 0;
-                if (valid) {
-                    if (GU) row = pt.sh ? pt.j0 + i : a.tok[pt.tokbase + pt.j0 + i];
-                    else row = pt.rowbase + i;
-                }
-                const __nv_bfloat16 *s = act + (size_t)row * act_ld + pg * kGK;
-                if (i < pt.np) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        cp_async16(dst + (i >> 3) * 1024 + (i & 7) * 128 + ((c ^ (i & 7)) << 4),
-                                   s + c * 8, valid);
-                }
-                if (++pg == pt.ngroups) {
-                    pg = 0;
-                    ptask += gridDim.x;
-                    if (ptask < total) pt = tc_task<GU>(a, ptask);
-                }
-                ++pit;
+        // nibble cursor: the next group to load into registers, kNibAhead ahead of the
+        // conversion cursor, across task boundaries
+        int ntask = blockIdx.x, ng = 0, nng = 0;
+        const uint8_t *nw = nullptr;
+        auto enter_n = [&]() {
+            if (ntask < total) {
+                const TcTask t = tc_task<GU>(a, *ps, ntask);
+                nw = t.w + (size_t)i * t.rowbytes;
+                nng = t.ngroups;
             }
         };
-        for (int k = 0; k < kPre; ++k) {
-            issue_b();
-            cp_async_commit();
-        }
-        long long it = 0;
-        for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
-            const TcTask t = tc_task<GU>(a, task);
-            const uint8_t *wrow = t.w + (size_t)i * t.rowbytes;
-            // nibbles of the next kNibAhead groups in registers (2 x 16 bytes per group)
-            uint4 nib[kNibAhead][2];
+        auto next_n = [&](uint4 (&slot)[2]) {
+            if (ntask >= total) return;
+            slot[0] = ld_stream_v4(nw + ng * 32);
+            slot[1] = ld_stream_v4(nw + ng * 32 + 16);
+            if (++ng == nng) {
+                ng = 0;
+                ntask += gridDim.x;
+                enter_n();
+            }
+        };
+        enter_n();
+        uint4 nib[kNibAhead][2];
+#pragma unroll
+        for (int q = 0; q < kNibAhead; ++q) next_n(nib[q]);
+        // conversion cursor
+        int ctask = blockIdx.x, cg = 0, cng = ctask < total ? tc_task<GU>(a, *ps, ctask).ngroups : 0;
+        uint32_t it = 0;
+        while (ctask < total && !aborted(sh)) {
 #pragma unroll
             for (int q = 0; q < kNibAhead; ++q) {
-                if (q < t.ngroups) {
-                    nib[q][0] = ld_stream_v4(wrow + q * 32);
-                    nib[q][1] = ld_stream_v4(wrow + q * 32 + 16);
+                if (ctask >= total || aborted(sh)) break;
+                const uint32_t st = it % kAStages;
+                // this A buffer was last read by the MMAs of group it - kAStages
+                if (it >= kAStages) {
+                    if (!tc_wait_warp(&sh->aempty[st], ((it / kAStages) - 1) & 1, sh, a.err)) break;
+                    tc::fence_after_sync();
                 }
-            }
-            for (int g0 = 0; g0 < t.ngroups && !aborted(sh); g0 += kNibAhead) {
+                uint32_t av[32];
+                const uint32_t wv[8] = {nib[q][0].x, nib[q][0].y, nib[q][0].z, nib[q][0].w,
+                                        nib[q][1].x, nib[q][1].y, nib[q][1].z, nib[q][1].w};
 #pragma unroll
-                for (int q = 0; q < kNibAhead; ++q) {
-                    const int g = g0 + q;
-                    if (g >= t.ngroups || aborted(sh)) break;
-                    const int st = (int)(it % kStages);
-                    // the B copy kPre groups ahead; its stage was freed by the MMA of an
-                    // earlier group, which also freed this group's A buffer
-                    issue_b();
-                    cp_async_commit();
-                    if (it >= kStages &&
-                        !tc_wait(&sh->sfree[st], (uint32_t)((it / kStages - 1) & 1), sh, a.err))
-                        break;
-                    uint32_t av[32];
-                    const uint32_t wv[8] = {nib[q][0].x, nib[q][0].y, nib[q][0].z, nib[q][0].w,
-                                            nib[q][1].x, nib[q][1].y, nib[q][1].z, nib[q][1].w};
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) nibbles_to_bf16(wv[c], av + 4 * c);
-                    // refill this register slot with the group kNibAhead further on
-                    if (g + kNibAhead < t.ngroups) {
-                        nib[q][0] = ld_stream_v4(wrow + (g + kNibAhead) * 32);
-                        nib[q][1] = ld_stream_v4(wrow + (g + kNibAhead) * 32 + 16);
-                    }
-                    tc::st32(tmem + ((uint32_t)(warp * 32) << 16) + kColA + st * 32, av);
-                    tc::wait_st();
-                    cp_async_wait<kPre>();          // this group's B rows have landed
-                    tc::fence_proxy_async_smem();   // ... and are visible to the MMA
-                    tc::fence_before_sync();
-                    mbar_arrive(&sh->full[st]);
-                    ++it;
+                for (int c = 0; c < 8; ++c) nibbles_to_bf16(wv[c], av + 4 * c);
+                next_n(nib[q]);   // this register slot now takes the group kNibAhead on
+                tc::st32(tmem + ((uint32_t)(warp * 32) << 16) + kColA + st * 32, av);
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh->afull[st]);
+                ++it;
+                if (++cg == cng) {
+                    cg = 0;
+                    ctask += gridDim.x;
+                    cng = ctask < total ? tc_task<GU>(a, *ps, ctask).ngroups : 0;
                 }
             }
         }
-        cp_async_wait<0>();
-    } else if (warp == 4) {
-        // ---------------- MMA issue ---------------------------------------------------
-        long long it = 0;
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issue: the whole warp runs the loop, one lane issues ----------
+        const uint64_t bdesc0 = tc::sdesc_kmajor_sw128(smem_u32(bstage));
+        uint32_t it = 0;
         for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
-            const TcTask t = tc_task<GU>(a, task);
+            const TcTask t = tc_task<GU>(a, *ps, task);
             const uint32_t idesc = tc::idesc_bf16_f32(kM, t.np);
             for (int g = 0; g < t.ngroups && !aborted(sh); ++g, ++it) {
-                const int st = (int)(it % kStages), buf = (int)(it & 1);
-                bool ok = true;
-                if (lane == 0) {
-                    ok = tc_wait(&sh->full[st], (uint32_t)((it / kStages) & 1), sh, a.err);
-                    if (ok && it >= 2) ok = tc_wait(&sh->dempty[buf], (uint32_t)((it / 2 - 1) & 1), sh, a.err);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                const uint32_t sa = it % kAStages, sb = it % kBStages, buf = it % kDBuf;
+                if (!tc_wait_warp(&sh->afull[sa], (it / kAStages) & 1, sh, a.err) ||
+                    !tc_wait_warp(&sh->bfull[sb], (it / kBStages) & 1, sh, a.err) ||
+                    (it >= kDBuf && !tc_wait_warp(&sh->dempty[buf], ((it / kDBuf) - 1) & 1, sh, a.err)))
+                    break;
                 tc::fence_after_sync();
-                if (lane == 0) {
-                    const uint32_t bsaddr = smem_u32(bstage + st * kBStageBytes);
+                // B descriptor: the stage's start address advanced 32 bytes per K step of 16
+                const uint64_t bd = bdesc0 + (uint64_t)((sb * kBStageBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(tmem + kColD + buf * kN, tmem + kColA + st * 32 + kk * 8,
-                                   tc::sdesc_kmajor_sw128(bsaddr + kk * 32), idesc, kk > 0);
-                    tc::commit(&sh->sfree[st]);
-                    tc::commit(&sh->dfull[buf]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_ts_elect(tmem + kColD + buf * kN, tmem + kColA + sa * 32 + kk * 8,
+                                     bd + (uint64_t)(kk * 2), idesc, kk > 0);
+                tc::commit_elect(&sh->aempty[sa]);
+                tc::commit_elect(&sh->bempty[sb]);
+                tc::commit_elect(&sh->dfull[buf]);
             }
         }
-    } else {
-        // ---------------- epilogue: warp q reads TMEM lanes 32q .. 32q+31 = rows ------
-        const int q = warp & 3;
-        const int i = q * 32 + lane;   // row within the tile
-        const QuantRows &src = GU ? a.xq : a.hq;
-        long long it = 0;
+        // every MMA issued here completes before TMEM is freed
+        tc::commit_elect(&sh->mfinal);
+        tc_wait_warp(&sh->mfinal, 0, sh, a.err);
+    } else if (warp == kWarpTma) {
+        // ---------------- B tiles by TMA: the whole warp runs the loop, one lane issues -----
+        const uint32_t bs0 = smem_u32(bstage);
+        uint32_t it = 0;
         for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
-            const TcTask t = tc_task<GU>(a, task);
+            const TcTask t = tc_task<GU>(a, *ps, task);
+            const uint32_t bytes = (uint32_t)t.np * 128u;
+            bool ok = true;
+            for (int g = 0; g < t.ngroups && !aborted(sh); ++g, ++it) {
+                const uint32_t sb = it % kBStages;
+                if (it >= kBStages && !(ok = tc_wait_warp(&sh->bempty[sb], ((it / kBStages) - 1) & 1, sh, a.err)))
+                    break;
+                const uint32_t full = smem_u32(&sh->bfull[sb]);
+                arrive_expect_tx_elect(full, bytes);
+                // rows rowbase .. rowbase + np - 1 of the activation codes (rows past nt feed
+                // only the padding columns of the accumulator)
+                for (int r = 0; r < t.np; r += kBoxRows)
+                    tma_load_2d_elect(bs0 + sb * kBStageBytes + r * 128, &bmap, g * kGK, t.rowbase + r, full);
+            }
+            if (!ok) break;
+        }
+        // copies still in flight (after a timeout elsewhere) land before the CTA exits
+        for (uint32_t j = it > (uint32_t)kBStages ? it - kBStages : 0; j < it; ++j)
+            mbar_wait(&sh->bfull[j % kBStages], (j / kBStages) & 1);
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warp reads TMEM lanes 32q .. 32q+31 (rows), token
+        // columns 64h .. 64h+63 ----------------------------------------------------------
+        const int q = warp & 3, half = (warp - kWarpEpi0) >> 2;
+        const int i = q * 32 + lane;   // row within the tile
+        const int c0 = half * 64;      // first token column
+        const QuantRows &src = GU ? a.xq : a.hq;
+        float *myscl = escl + (size_t)(tid - kWarpEpi0 * 32) * 16;
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+        uint32_t it = 0;
+        for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
+            const TcTask t = tc_task<GU>(a, *ps, task);
             cp_async_wait<0>();   // the last task's scale copies (none pending otherwise)
-            float acc[kN];
+            float acc[64];
 #pragma unroll
-            for (int j = 0; j < kN; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
             // the row's group scales, copied 8 at a time into this thread's two shared slots,
             // one block of 8 ahead (G is a multiple of 8)
             const float *srow = t.s + (size_t)i * t.G;
-            float *myscl = escl + (size_t)i * 16;
             cp_async16(myscl, srow, true);
             cp_async16(myscl + 4, srow + 4, true);
             cp_async_commit();
+            const int ncols = t.np - c0;   // this warp's token columns in the tile (may be <= 0)
+            // activation scales of this warp's 64 token columns: lane l holds columns l, 32 + l
+            float tsc[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int jj = c0 + h2 * 32 + lane;
+                tsc[h2] = 0.0f;
+                if (jj < t.nt) {
+                    const int arow = GU ? (t.sh ? t.j0 + jj : a.tok[t.tokbase + t.j0 + jj]) : t.rowbase + jj;
+                    tsc[h2] = src.scale[arow];
+                }
+            }
+            bool ok = true;
             for (int g = 0; g < t.ngroups; ++g, ++it) {
                 const int gi = g & 7;
                 if (gi == 0) {
@@ -324,36 +418,45 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
                     cp_async_wait<1>();   // this block's 8 scales have landed
                 }
                 const float scl = myscl[((g >> 3) & 1) * 8 + gi];
-                const int buf = (int)(it & 1);
-                if (!tc_wait(&sh->dfull[buf], (uint32_t)((it / 2) & 1), sh, a.err)) break;
+                const uint64_t s2 = ((uint64_t)__float_as_uint(scl) << 32) | __float_as_uint(scl);
+                const uint32_t buf = it % kDBuf;
+                if (!(ok = tc_wait_warp(&sh->dfull[buf], (it / kDBuf) & 1, sh, a.err))) break;
                 tc::fence_after_sync();
+                const uint32_t col = tl + kColD + buf * kN + c0;
+                // 16 columns at a time, the next load in flight while this one is added up
+                uint32_t ra[16], rb[16];
+                if (ncols > 0) tc::ld16(col, ra);
+                tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < kN / 16; ++c) {
-                    if (c * 16 < t.np) {
-                        uint32_t r[16];
-                        tc::ld16(tmem + ((uint32_t)(q * 32) << 16) + kColD + buf * kN + c * 16, r);
-                        tc::wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&cur)[16] = (c & 1) ? rb : ra;
+                    uint32_t (&nxt)[16] = (c & 1) ? ra : rb;
+                    if (c + 1 < 4 && (c + 1) * 16 < ncols) tc::ld16(col + (c + 1) * 16, nxt);
+                    if (c * 16 < ncols) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float d = __uint_as_float(r[j]);
-                            acc[c * 16 + j] = fmaf(scl, d, acc[c * 16 + j]);
-                            if (PROBE) {
-                                const int jj = c * 16 + j;
+                        for (int j = 0; j < 16; j += 2)
+                            ffma2(acc[c * 16 + j], acc[c * 16 + j + 1], s2, cur[j], cur[j + 1]);
+                        if (PROBE) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int jj = c0 + c * 16 + j;
                                 if (jj < t.nt && t.sh == 0) {
                                     const size_t pr = (size_t)(t.rowbase + jj - a.routed_rowbase);
                                     const size_t o = (pr * (size_t)(GU ? a.F : a.H) + t.r0 + i) * t.G + g;
                                     int32_t *dst = GU ? (t.m == 0 ? a.probe.acc_gate : a.probe.acc_up)
                                                       : a.probe.acc_down;
-                                    if (dst) dst[o] = (int32_t)d;   // an exact integer
+                                    if (dst) dst[o] = (int32_t)__uint_as_float(cur[j]);   // exact
                                 }
                             }
                         }
                     }
+                    tc::wait_ld();
                 }
                 tc::fence_before_sync();
-                mbar_arrive(&sh->dempty[buf]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh->dempty[buf]);
             }
-            if (aborted(sh)) break;
+            if (!ok || aborted(sh)) break;
             // outputs: token scale x accumulated row value
             float *dst;
             int ld;
@@ -365,18 +468,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
                 ld = a.H;
             }
 #pragma unroll
-            for (int j = 0; j < kN; ++j) {
-                if (j < t.nt) {
-                    const int arow = GU ? (t.sh ? t.j0 + j : a.tok[t.tokbase + t.j0 + j]) : t.rowbase + j;
-                    dst[(size_t)(t.rowbase + j) * ld + t.r0 + i] = src.scale[arow] * acc[j];
-                }
+            for (int j = 0; j < 64; ++j) {
+                const int jj = c0 + j;
+                const float sx = __shfl_sync(0xffffffffu, tsc[j >> 5], j & 31);
+                if (jj < t.nt) dst[(size_t)(t.rowbase + jj) * ld + t.r0 + i] = sx * acc[j];
             }
         }
+        cp_async_wait<0>();
     }
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kWarpMma) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
@@ -396,16 +499,63 @@ bool ffn_tc_supported(const FfnArgs &a)
 
 size_t ffn_tc_smem_bytes() { return kSmemBytes; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a [rows][ld] bf16 matrix of which the first `cols` columns are read: boxes of
+// 64 columns (128 bytes) x kBoxRows rows, 128-byte swizzle, rows past the end read as zero.
+cudaError_t bf16_rows_map(CUtensorMap *m, const __nv_bfloat16 *base, int cols, int ld, int rows)
+{
+    const auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kGK, (cuuint32_t)kBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_ffn_tc(bool gu, const FfnArgs &a, cudaStream_t st)
 {
     const bool probe = gu ? (a.probe.acc_gate != nullptr || a.probe.acc_up != nullptr)
                           : a.probe.acc_down != nullptr;
+    // B operand rows = output rows of the call: the x codes laid out by launch_gather_x_bf16
+    // (gate/up) or the h codes written by the h quantisation (down)
+    CUtensorMap bmap;
+    const int rows = a.plane_rows > 0 ? a.plane_rows : 1;
+    cudaError_t e = gu ? bf16_rows_map(&bmap, a.x_bf16, a.H, a.H, rows)
+                       : bf16_rows_map(&bmap, a.h_bf16, a.hstride, a.hstride, rows);
+    if (e != cudaSuccess) return e;
+    if (gu) {
+        const int first = a.n_shared ? a.T : 0;
+        e = launch_gather_x_bf16(a, first, first + (a.include_routed ? a.T * a.K : 0), st);
+        if (e != cudaSuccess) return e;
+    }
     const dim3 grid(num_sms()), block(kThreads);
     if (gu)
-        return probe ? launch_kernel(ffn_tc_kernel<true, true>, grid, block, kSmemBytes, st, 1, a)
-                     : launch_kernel(ffn_tc_kernel<true, false>, grid, block, kSmemBytes, st, 1, a);
-    return probe ? launch_kernel(ffn_tc_kernel<false, true>, grid, block, kSmemBytes, st, 1, a)
-                 : launch_kernel(ffn_tc_kernel<false, false>, grid, block, kSmemBytes, st, 1, a);
+        return probe ? launch_kernel(ffn_tc_kernel<true, true>, grid, block, kSmemBytes, st, 1, a, bmap)
+                     : launch_kernel(ffn_tc_kernel<true, false>, grid, block, kSmemBytes, st, 1, a, bmap);
+    return probe ? launch_kernel(ffn_tc_kernel<false, true>, grid, block, kSmemBytes, st, 1, a, bmap)
+                 : launch_kernel(ffn_tc_kernel<false, false>, grid, block, kSmemBytes, st, 1, a, bmap);
 }
 
 }  // namespace moe

@@ -206,9 +206,9 @@ FfnArgs base_args(const moe_config &c, int T, void *ws, const WsLayout &L)
 void configure_ffn(FfnArgs &a, void *ws, const WsLayout &L)
 {
     ffn_configure(a);
-    a.xq.bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.xbf) : nullptr;
+    a.xq.bf16 = nullptr;
     a.hq.bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.hbf) : nullptr;
-    a.x_bf16 = a.xq.bf16;
+    a.x_bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.xbf) : nullptr;
     a.h_bf16 = a.hq.bf16;
 }
 
@@ -218,7 +218,7 @@ cudaError_t run_ffn(const FfnArgs &a, int T, int ns, bool routed_rows, bool ev, 
 {
     cudaError_t e;
     {
-        Scope sc(ev, MOE_STAGE_GATE_UP, st);
+        Scope sc(ev, MOE_STAGE_GATE_UP, st, a.tensor ? 2 : 1);   // tensor path: + x gather
         e = launch_ffn_gate_up(a, st);
         sc.finish();
     }
@@ -372,7 +372,7 @@ WsLayout ws_layout(const moe_config &c, int T)
     const size_t hp_tensor = T > kRouteClusterMaxT ? rows * fm : 0;
     L.hp_plane_floats = hp_sliced > hp_tensor ? hp_sliced : hp_tensor;
     L.hp = take(2 * L.hp_plane_floats * 4);
-    L.xbf = take(T > kRouteClusterMaxT ? (size_t)T * H * 2 : 0);
+    L.xbf = take(T > kRouteClusterMaxT ? rows * H * 2 : 0);
     L.hbf = take(T > kRouteClusterMaxT ? rows * fm * 2 : 0);
     L.hq = take(rows * fm);
     L.hscale = take(rows * 4);

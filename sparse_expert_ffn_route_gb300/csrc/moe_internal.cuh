@@ -84,7 +84,7 @@ struct FfnArgs {
     int plane_rows;                   // output rows of the call (shared rows + routed pairs)
     int slice_gu, slice_dn;           // rows cut into 1024-input slices
     int tensor;                       // the tcgen05 path (ffn_tc.cu) runs gate/up and down
-    const __nv_bfloat16 *x_bf16;      // [T][H] the codes of x as bf16 (tensor path)
+    __nv_bfloat16 *x_bf16;            // [rows][H] the codes of x per output row as bf16 (tensor path)
     __nv_bfloat16 *h_bf16;            // [rows][hstride] the codes of h as bf16 (tensor path)
     int tc_gu, tc_dn;                 // token chunk per task
     Geo geo_gu[2], geo_dn[2];         // task geometry: [0] routed experts, [1] shared expert
@@ -147,6 +147,9 @@ cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride,
 // pair rows (count read on the device from offsets[n_experts]) of n_rest values
 cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_rest,
                            int max_rows, cudaStream_t st);
+// the x codes of every output row of an FFN call as bf16 (tensor-core path): `first_rows`
+// shared-expert rows, then the routed pair rows (count read on the device)
+cudaError_t launch_gather_x_bf16(const FfnArgs &a, int first_rows, int max_rows, cudaStream_t st);
 // host-side choice of the FFN kernels' tile shape and pipeline depth
 void ffn_configure(FfnArgs &a);
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);

@@ -14,13 +14,14 @@ namespace {
 
 constexpr int kQThreads = 256;
 
-// the int8 codes of 8 consecutive values as bf16 (exact), element order, 16 bytes
+// the int8 codes of 8 consecutive values as bf16 (exact), 16 bytes in the tensor-core path's
+// order e0 e4 e1 e5 e2 e6 e3 e7 (the order in which its weight nibbles unpack)
 __device__ __forceinline__ void store_codes_bf16(__nv_bfloat16 *dst, const float v[8], float inv)
 {
     __nv_bfloat162 p[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        p[i] = __floats2bfloat162_rn((float)quant_code(v[2 * i], inv), (float)quant_code(v[2 * i + 1], inv));
+        p[i] = __floats2bfloat162_rn((float)quant_code(v[i], inv), (float)quant_code(v[i + 4], inv));
     *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(p);
 }
 constexpr int kMaxSlices = kMaxDim / (32 * kSliceChunks);   // slices of a row of kMaxDim inputs
@@ -205,7 +206,52 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
                         dst.csum + (size_t)row * dst.c_ld, dst.scale + row, canon, canon_scale, qb);
 }
 
+// The x codes of every output row of an FFN call as bf16, for the tensor-core path's B
+// operand: rows [0, first) are the shared expert's (token = row), rows routed_rowbase + p
+// the routed pairs (token = tok[p], p < *rest_count).  Codes come from the run layout
+// [e0 e2 e4 e6 | e1 e3 e5 e7] and go out in the order e0 e4 e1 e5 e2 e6 e3 e7.
+__global__ void __launch_bounds__(kQThreads) gather_x_bf16_kernel(QuantRows xq, int n, int first,
+                                                                  int routed_rowbase,
+                                                                  const int32_t *rest_count,
+                                                                  const int32_t *tok,
+                                                                  __nv_bfloat16 *dst)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int row = blockIdx.x;
+    int token;
+    if (row < first) {
+        token = row;
+    } else {
+        const int p = row - routed_rowbase;
+        const int rest = rest_count ? *rest_count : 0;
+        if (p < 0 || p >= rest) return;
+        token = tok[p];
+    }
+    const int8_t *src = xq.q + (size_t)token * xq.q_ld;
+    __nv_bfloat16 *out = dst + (size_t)row * n;
+    for (int run = threadIdx.x; run < n / 8; run += kQThreads) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src + run * 8);
+        // v.x bytes: e0 e2 e4 e6, v.y bytes: e1 e3 e5 e7
+        auto code = [](uint32_t w, int b) { return (float)(int8_t)(w >> (8 * b)); };
+        __nv_bfloat162 p[4];
+        p[0] = __floats2bfloat162_rn(code(v.x, 0), code(v.x, 2));   // e0 e4
+        p[1] = __floats2bfloat162_rn(code(v.y, 0), code(v.y, 2));   // e1 e5
+        p[2] = __floats2bfloat162_rn(code(v.x, 1), code(v.x, 3));   // e2 e6
+        p[3] = __floats2bfloat162_rn(code(v.y, 1), code(v.y, 3));   // e3 e7
+        *reinterpret_cast<uint4 *>(out + run * 8) = *reinterpret_cast<const uint4 *>(p);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_x_bf16(const FfnArgs &a, int first_rows, int max_rows, cudaStream_t st)
+{
+    if (max_rows <= 0) return cudaSuccess;
+    const int32_t *rest = a.include_routed ? a.offsets + a.E : nullptr;
+    return launch_kernel(gather_x_bf16_kernel, dim3(max_rows), dim3(kQThreads), 0, st, 1, a.xq, a.H,
+                         first_rows, a.routed_rowbase, rest, a.tok, a.x_bf16);
+}
 
 cudaError_t launch_quant_rows(const float *src, int rows, int n, int src_stride, QuantRows dst,
                               cudaStream_t st)

@@ -72,6 +72,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// The same MMA issued by one elected lane of a converged warp: every lane executes the
+// instruction with warp-uniform operands and elect.sync picks the issuing lane.  A loop run by
+// the whole warp this way issues MMAs at the tensor pipe's rate; a loop inside a one-lane
+// branch is limited by that lane's own instruction stream.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// commit (below) issued by one elected lane of a converged warp
+__device__ __forceinline__ void commit_elect(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
 // the mbarrier gets one arrival once every tcgen05 operation this thread issued so far is done
 __device__ __forceinline__ void commit(uint64_t *bar)
 {
