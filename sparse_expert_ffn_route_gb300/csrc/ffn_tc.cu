@@ -16,9 +16,11 @@
 //              convert them to bf16 (u - 8) and store them into the group's A buffer in TMEM.
 //   warp 4     allocates TMEM; one thread issues the 4 MMAs of each group (A from TMEM, B
 //              from shared memory) and commits them to the rings' mbarriers.
-//   warp 5     one thread loads the B tiles: the tile's activation rows (bf16 codes, laid out
-//              in output-row order, 128 bytes per row per group) by 2-D TMA in 16-row boxes
-//              with the 128-byte swizzle, into a ring of kBStages shared-memory stages.
+//   warp 5     loads the B tiles: the tile's activation rows (bf16 codes, laid out in
+//              output-row order, 128 bytes per row per group) by 2-D TMA with the 128-byte
+//              swizzle, one box per power-of-two part of the tile's height (a TMA instruction
+//              costs the issuing warp about a hundred cycles, so boxes are as large as the
+//              tile allows), into a ring of kBStages shared-memory stages.
 //   warps 6-13 the epilogue, two warps per 32 TMEM lanes (32 rows), 64 token columns each:
 //              per group the accumulator is loaded 16 columns at a time (the next load in
 //              flight) and added into registers with the group scale (packed fp32x2 FMAs).
@@ -50,7 +52,7 @@ constexpr int kAStages = 4;         // A buffers in TMEM
 constexpr int kBStages = 10;        // B stages in shared memory
 constexpr int kDBuf = 3;            // accumulators in TMEM
 constexpr int kNibAhead = 6;        // groups of nibbles held in registers ahead of use
-constexpr int kBoxRows = 16;        // rows per B copy (one TMA box)
+constexpr int kBoxMaps = 4;         // B tensor maps with boxes of 16, 32, 64 and 128 rows
 constexpr int kWarpMma = 4, kWarpTma = 5, kWarpEpi0 = 6;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter, 64 token columns each
 constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
@@ -199,9 +201,14 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, TcS
     return __all_sync(0xffffffffu, tc_wait(bar, parity, sh, err));
 }
 
+// the B operand's tensor maps: map k has boxes of 64 columns x (16 << k) rows
+struct alignas(64) BMaps {
+    CUtensorMap m[kBoxMaps];
+};
+
 template <bool GU, bool PROBE>
 __global__ void __launch_bounds__(kThreads, 1)
-    ffn_tc_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ CUtensorMap bmap)
+    ffn_tc_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ BMaps bmaps)
 {
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     pdl_wait();
@@ -360,9 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full = smem_u32(&sh->bfull[sb]);
                 arrive_expect_tx_elect(full, bytes);
                 // rows rowbase .. rowbase + np - 1 of the activation codes (rows past nt feed
-                // only the padding columns of the accumulator)
-                for (int r = 0; r < t.np; r += kBoxRows)
-                    tma_load_2d_elect(bs0 + sb * kBStageBytes + r * 128, &bmap, g * kGK, t.rowbase + r, full);
+                // only the padding columns of the accumulator): np (a multiple of 16, at most
+                // 128) as a sum of boxes of 128, 64, 32 and 16 rows, largest first
+                int r = 0;
+#pragma unroll
+                for (int k = kBoxMaps - 1; k >= 0; --k) {
+                    if (t.np - r >= (16 << k)) {
+                        tma_load_2d_elect(bs0 + sb * kBStageBytes + r * 128, &bmaps.m[k], g * kGK, t.rowbase + r, full);
+                        r += 16 << k;
+                    }
+                }
             }
             if (!ok) break;
         }
@@ -517,14 +531,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // Tensor map of a [rows][ld] bf16 matrix of which the first `cols` columns are read: boxes of
-// 64 columns (128 bytes) x kBoxRows rows, 128-byte swizzle, rows past the end read as zero.
-cudaError_t bf16_rows_map(CUtensorMap *m, const __nv_bfloat16 *base, int cols, int ld, int rows)
+// 64 columns (128 bytes) x box_rows rows, 128-byte swizzle, rows past the end read as zero.
+cudaError_t bf16_rows_map(CUtensorMap *m, const __nv_bfloat16 *base, int cols, int ld, int rows, int box_rows)
 {
     const auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kGK, (cuuint32_t)kBoxRows};
+    const cuuint32_t box[2] = {(cuuint32_t)kGK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(base), dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -540,10 +554,12 @@ cudaError_t launch_ffn_tc(bool gu, const FfnArgs &a, cudaStream_t st)
                           : a.probe.acc_down != nullptr;
     // B operand rows = output rows of the call: the x codes laid out by launch_gather_x_bf16
     // (gate/up) or the h codes written by the h quantisation (down)
-    CUtensorMap bmap;
+    BMaps bmaps;
     const int rows = a.plane_rows > 0 ? a.plane_rows : 1;
-    cudaError_t e = gu ? bf16_rows_map(&bmap, a.x_bf16, a.H, a.H, rows)
-                       : bf16_rows_map(&bmap, a.h_bf16, a.hstride, a.hstride, rows);
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < kBoxMaps && e == cudaSuccess; ++k)
+        e = gu ? bf16_rows_map(&bmaps.m[k], a.x_bf16, a.H, a.H, rows, 16 << k)
+               : bf16_rows_map(&bmaps.m[k], a.h_bf16, a.hstride, a.hstride, rows, 16 << k);
     if (e != cudaSuccess) return e;
     if (gu) {
         const int first = a.n_shared ? a.T : 0;
@@ -552,10 +568,10 @@ cudaError_t launch_ffn_tc(bool gu, const FfnArgs &a, cudaStream_t st)
     }
     const dim3 grid(num_sms()), block(kThreads);
     if (gu)
-        return probe ? launch_kernel(ffn_tc_kernel<true, true>, grid, block, kSmemBytes, st, 1, a, bmap)
-                     : launch_kernel(ffn_tc_kernel<true, false>, grid, block, kSmemBytes, st, 1, a, bmap);
-    return probe ? launch_kernel(ffn_tc_kernel<false, true>, grid, block, kSmemBytes, st, 1, a, bmap)
-                 : launch_kernel(ffn_tc_kernel<false, false>, grid, block, kSmemBytes, st, 1, a, bmap);
+        return probe ? launch_kernel(ffn_tc_kernel<true, true>, grid, block, kSmemBytes, st, 1, a, bmaps)
+                     : launch_kernel(ffn_tc_kernel<true, false>, grid, block, kSmemBytes, st, 1, a, bmaps);
+    return probe ? launch_kernel(ffn_tc_kernel<false, true>, grid, block, kSmemBytes, st, 1, a, bmaps)
+                 : launch_kernel(ffn_tc_kernel<false, false>, grid, block, kSmemBytes, st, 1, a, bmaps);
 }
 
 }  // namespace moe
