@@ -437,38 +437,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = tc_wait_warp(&sh->dfull[buf], (it / kDBuf) & 1, sh, a.err))) break;
                 tc::fence_after_sync();
                 const uint32_t col = tl + kColD + buf * kN + c0;
-                // 16 columns at a time, the next load in flight while this one is added up
-                uint32_t ra[16], rb[16];
-                if (ncols > 0) tc::ld16(col, ra);
-                tc::wait_ld();
+                // the warp's 64 columns in two halves of two loads each (both in flight at
+                // once); the accumulator is released once the second half has landed
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t (&cur)[16] = (c & 1) ? rb : ra;
-                    uint32_t (&nxt)[16] = (c & 1) ? ra : rb;
-                    if (c + 1 < 4 && (c + 1) * 16 < ncols) tc::ld16(col + (c + 1) * 16, nxt);
-                    if (c * 16 < ncols) {
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t ra[16], rb[16];
+                    const int cb = hh * 32;
+                    if (cb < ncols) tc::ld16(col + cb, ra);
+                    if (cb + 16 < ncols) tc::ld16(col + cb + 16, rb);
+                    tc::wait_ld();
+                    if (hh == 1) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh->dempty[buf]);
+                    }
+                    if (cb < ncols) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2)
-                            ffma2(acc[c * 16 + j], acc[c * 16 + j + 1], s2, cur[j], cur[j + 1]);
-                        if (PROBE) {
+                        for (int j = 0; j < 16; j += 2) ffma2(acc[cb + j], acc[cb + j + 1], s2, ra[j], ra[j + 1]);
+                    }
+                    if (cb + 16 < ncols) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int jj = c0 + c * 16 + j;
-                                if (jj < t.nt && t.sh == 0) {
-                                    const size_t pr = (size_t)(t.rowbase + jj - a.routed_rowbase);
-                                    const size_t o = (pr * (size_t)(GU ? a.F : a.H) + t.r0 + i) * t.G + g;
-                                    int32_t *dst = GU ? (t.m == 0 ? a.probe.acc_gate : a.probe.acc_up)
-                                                      : a.probe.acc_down;
-                                    if (dst) dst[o] = (int32_t)__uint_as_float(cur[j]);   // exact
-                                }
+                        for (int j = 0; j < 16; j += 2) ffma2(acc[cb + 16 + j], acc[cb + 17 + j], s2, rb[j], rb[j + 1]);
+                    }
+                    if (PROBE) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int jj = c0 + cb + j;
+                            if (jj < t.nt && t.sh == 0) {
+                                const size_t pr = (size_t)(t.rowbase + jj - a.routed_rowbase);
+                                const size_t o = (pr * (size_t)(GU ? a.F : a.H) + t.r0 + i) * t.G + g;
+                                int32_t *dst = GU ? (t.m == 0 ? a.probe.acc_gate : a.probe.acc_up) : a.probe.acc_down;
+                                const uint32_t d = j < 16 ? ra[j] : rb[j - 16];
+                                if (dst) dst[o] = (int32_t)__uint_as_float(d);   // an exact integer
                             }
                         }
                     }
-                    tc::wait_ld();
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh->dempty[buf]);
             }
             if (!ok || aborted(sh)) break;
             // outputs: token scale x accumulated row value
