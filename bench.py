@@ -132,6 +132,18 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- peaks
 
+def tensor_peak():
+    """Dense bf16 TFLOP/s of this GPU as measured by the driver: the sustained figure (a
+    kernel timed inside a long layer step), else the recipe's fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured (bf16 sustained)"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback (bf16 sustained)"
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -201,6 +213,16 @@ def algorithmic_bytes(wl, T, U, pairs):
     layer = U * wl.expert_bytes() + ns * wl.expert_bytes(True) + wl.n_experts * H * 4 \
         + T * H * 4 * 2
     return {"gate_up": gu, "down": dn, "layer": layer}
+
+
+def algorithmic_flops(wl, T, pairs):
+    """Multiply-add FLOPs (2 per MAC) of the expert FFN per layer call: every routed pair and
+    shared-expert row against its expert's matrices, no padding counted."""
+    ns = wl.n_shared
+    H, F, Fs = wl.hidden, wl.d_ff, wl.d_ff_shared
+    gu = 2.0 * (pairs * 2 * F * H + T * ns * 2 * Fs * H)
+    dn = 2.0 * (pairs * F * H + T * ns * Fs * H)
+    return {"gate_up": gu, "down": dn}
 
 
 def run_ours(args, world, rank, local):
@@ -285,12 +307,30 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = hbm_peak()
     achieved = tot_bytes[dom] / (st[dom][0] / 1e3) / 1e9
     traffic = recorded_traffic("ffn_" + dom, "%s_T%d" % (wl.name, T))
-    roofline = {"bound": "hbm", "kernel": "ffn_" + dom, "achieved": round(achieved, 1),
-                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "algorithmic_bytes_per_launch": round(tot_bytes[dom] / args.steps),
-                "launch_ms": round(st[dom][0] / args.steps, 4),
-                "layer_frac": round(tot_bytes["layer"] / (ms / 1e3) / 1e9 / peak, 4)}
+    if moe.moe_ffn_uses_tensor_cores(cfg, T) == 1:
+        # a dense contraction: tensor-pipe roofline on the useful FLOPs (the stage also holds
+        # the x-code gather launch, so this is a lower bound on the GEMM kernel's own rate)
+        tot_flops = {"gate_up": 0.0, "down": 0.0}
+        for k in range(args.steps):
+            _, P = stats[k % N_BATCHES]
+            for key, v in algorithmic_flops(wl, T, P).items():
+                tot_flops[key] += v
+        tpeak, tpeak_kind = tensor_peak()
+        tf = tot_flops[dom] / (st[dom][0] / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "ffn_" + dom, "achieved": round(tf, 1),
+                    "peak": tpeak, "peak_kind": tpeak_kind, "unit": "TFLOP/s",
+                    "frac": round(tf / tpeak, 4), "traffic": traffic,
+                    "algorithmic_flops_per_launch": round(tot_flops[dom] / args.steps),
+                    "launch_ms": round(st[dom][0] / args.steps, 4),
+                    "hbm_achieved_gbs": round(achieved, 1), "hbm_peak": peak,
+                    "layer_hbm_frac": round(tot_bytes["layer"] / (ms / 1e3) / 1e9 / peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": "ffn_" + dom, "achieved": round(achieved, 1),
+                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "algorithmic_bytes_per_launch": round(tot_bytes[dom] / args.steps),
+                    "launch_ms": round(st[dom][0] / args.steps, 4),
+                    "layer_frac": round(tot_bytes["layer"] / (ms / 1e3) / 1e9 / peak, 4)}
     stages = {s: round(v[0] / args.steps, 4) for s, v in st.items()}
     launches = sum(v[1] for v in st.values())
 

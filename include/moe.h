@@ -123,6 +123,14 @@ typedef struct moe_routing {
  * tokens.  Returns 0 for an invalid config or max_tokens < 0. */
 size_t moe_workspace_size(const moe_config *cfg, int max_tokens);
 
+/* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
+ * device work): 1 = the tcgen05 tensor-core grouped GEMM (batches beyond the
+ * decode route, T > 64, with hidden, d_ff and d_ff_shared multiples of 512),
+ * 0 = the GEMV-shaped kernels.  Returns -1 for an invalid config or T < 0.
+ * ["MoE 路由与专家流式加载" §1.3: the expert FFN turns from a weight-streaming
+ * GEMV into a dense contraction once tokens per expert grow.] */
+int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
+
 /* Router ["MoE 路由与专家流式加载" §1.1, §1.2].
  *   x [T][H] fp32, w_router [E][H] fp32, bias [E] fp32 (selection only).
  *   ids [T][K] int32: kept experts first, in selection order (descending

@@ -33,7 +33,7 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
-           "moe_route_noalloc")
+           "moe_route_noalloc", "moe_ffn_uses_tensor_cores")
 
 
 class MoeError(RuntimeError):
@@ -91,6 +91,8 @@ def load_library():
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.moe_workspace_size.argtypes = [vp, i32]
     L.moe_workspace_size.restype = sz
+    L.moe_ffn_uses_tensor_cores.argtypes = [vp, i32]
+    L.moe_ffn_uses_tensor_cores.restype = i32
     L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -128,6 +130,12 @@ def last_error() -> str:
 
 def moe_workspace_size(cfg: MoeConfig, max_tokens: int) -> int:
     return int(load_library().moe_workspace_size(ctypes.byref(cfg), max_tokens))
+
+
+def moe_ffn_uses_tensor_cores(cfg: MoeConfig, T: int) -> int:
+    """1 if a call with T tokens runs the tensor-core grouped GEMM, 0 for the GEMV kernels,
+    -1 for an invalid config or T."""
+    return int(load_library().moe_ffn_uses_tensor_cores(ctypes.byref(cfg), T))
 
 
 def alloc_workspace(cfg: MoeConfig, max_tokens: int, device="cuda") -> torch.Tensor:

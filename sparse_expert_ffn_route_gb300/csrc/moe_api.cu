@@ -397,6 +397,18 @@ size_t moe_workspace_size(const moe_config *cfg, int max_tokens)
 
 const char *moe_last_error_string(void) { return g_err; }
 
+int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
+{
+    if (check_config(cfg) != MOE_OK || T < 0) return -1;
+    FfnArgs a;
+    memset(&a, 0, sizeof a);
+    a.H = cfg->hidden;
+    a.F = cfg->d_ff;
+    a.n_shared = cfg->n_shared;
+    a.Fs = cfg->n_shared ? cfg->d_ff_shared : cfg->d_ff;
+    return (T > kRouteClusterMaxT && ffn_tc_supported(a)) ? 1 : 0;
+}
+
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
               int T, int32_t *ids, float *w, int32_t *keff, void *workspace,
               size_t workspace_bytes, void *stream)

@@ -47,6 +47,18 @@ def test_workspace_size(lib):
     assert moe.moe_workspace_size(cfg, -1) == 0
 
 
+def test_ffn_path_query(lib):
+    # the tensor-core grouped GEMM takes batches beyond the 64-token decode route when every
+    # matrix of the layer has dimensions in multiples of 512
+    glm = _cfg(hidden=6144, n_experts=256, top_k=8, d_ff=2048, d_ff_shared=2048)
+    assert [moe.moe_ffn_uses_tensor_cores(glm, t) for t in (0, 1, 64, 65, 4096)] == [0, 0, 0, 1, 1]
+    tiny = _cfg()   # d_ff = 128: GEMV kernels at every batch size
+    assert [moe.moe_ffn_uses_tensor_cores(tiny, t) for t in (1, 65, 5000)] == [0, 0, 0]
+    assert moe.moe_ffn_uses_tensor_cores(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 100) == 0
+    assert moe.moe_ffn_uses_tensor_cores(glm, -1) == -1
+    assert moe.moe_ffn_uses_tensor_cores(_cfg(top_k=9), 16) == -1
+
+
 FAKE = 1 << 20   # aligned, never dereferenced: validation fails before any use
 
 
