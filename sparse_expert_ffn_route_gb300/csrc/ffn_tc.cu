@@ -202,7 +202,7 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, TcS
 }
 
 // the B operand's tensor maps: map k has boxes of 64 columns x (16 << k) rows
-struct alignas(64) BMaps {
+struct BMaps {
     CUtensorMap m[kBoxMaps];
 };
 
