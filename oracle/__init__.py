@@ -66,6 +66,9 @@ def lib():
         L.moe_ref_combine.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp]
         L.moe_ref_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_ref_threads.argtypes = []
+        L.moe_ref_rmsnorm.argtypes = [vp, vp, ctypes.c_float, i32, i32, vp]
+        L.moe_ref_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp]
+        L.moe_ref_topk_hits.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -131,6 +134,44 @@ def route(cfg: Config, x, w_router, bias, with_logits: bool = False):
     if with_logits:
         out["logits"] = logits
     return out
+
+
+def rmsnorm(x, g, eps: float):
+    """RMSNorm of each row of x [T][H] with weight g [H] (["MoE 路由与专家流式加载" §5])."""
+    x = _np(x, np.float32); g = _np(g, np.float32)
+    T, H = x.shape
+    out = np.zeros((T, H), np.float32)
+    _check(lib().moe_ref_rmsnorm(_p(x), _p(g), float(eps), T, H, _p(out)), "moe_ref_rmsnorm")
+    return out
+
+
+def route_lookahead(cfg: Config, x, norm_w, eps: float, w_router, bias, with_logits: bool = False):
+    """The router applied to RMSNorm(x): a later layer's predicted top-K (la_predict)."""
+    x = _np(x, np.float32); g = _np(norm_w, np.float32)
+    wr = _np(w_router, np.float32); b = _np(bias, np.float32)
+    T = x.shape[0]
+    K, E = cfg.top_k, cfg.n_experts
+    ids = np.zeros((T, K), np.int32); w = np.zeros((T, K), np.float32)
+    keff = np.zeros(T, np.int32)
+    logits = np.zeros((T, E), np.float32) if with_logits else None
+    _check(lib().moe_ref_route_lookahead(ctypes.byref(cfg), _p(x), _p(g), float(eps), _p(wr),
+                                         _p(b), T, _p(ids), _p(w), _p(keff), _p(logits)),
+           "moe_ref_route_lookahead")
+    out = {"ids": ids, "w": w, "keff": keff}
+    if with_logits:
+        out["logits"] = logits
+    return out
+
+
+def topk_hits(ids_pred, keff_pred, ids_true, keff_true):
+    """Per token, the number of experts kept by both routings."""
+    ip = _np(ids_pred, np.int32); kp = _np(keff_pred, np.int32)
+    it = _np(ids_true, np.int32); kt = _np(keff_true, np.int32)
+    T, K = ip.shape
+    hits = np.zeros(T, np.int32)
+    _check(lib().moe_ref_topk_hits(T, K, _p(ip), _p(kp), _p(it), _p(kt), _p(hits)),
+           "moe_ref_topk_hits")
+    return hits
 
 
 def permute(cfg: Config, ids, keff):

@@ -22,6 +22,9 @@
  *             "MoE 路由与专家流式加载" §1.3]
  *   shared    always-on shared expert added to the output
  *             ["MoE 路由与专家流式加载" §1.4]
+ *   lookahead RMSNorm then the router, predicting a later layer's top-K from
+ *             a residual state, and the recall of such a prediction
+ *             ["MoE 路由与专家流式加载" §5]
  *
  * Precision: the router runs in fp32 because the pages' router is float
  * (`sigmoidf`, float32 router gate); the expert FFN combination of group
@@ -128,6 +131,18 @@ int moe_ref_layer_forward(const moe_ref_config *c, const float *x, int T,
 
 /* Number of OpenMP threads the parallel loops use (1 without OpenMP). */
 int moe_ref_threads(void);
+
+/* Router look-ahead ["MoE 路由与专家流式加载" §5, la_predict]: RMSNorm of the
+ * residual state x [T][H] with norm_w [H] and eps, then moe_ref_route on the
+ * result.  moe_ref_rmsnorm alone writes out [T][H].  moe_ref_topk_hits writes,
+ * per token, how many experts the predicted kept set (ids_pred [T][K], first
+ * keff_pred[t]) shares with the true one. */
+int moe_ref_rmsnorm(const float *x, const float *g, float eps, int T, int H, float *out);
+int moe_ref_route_lookahead(const moe_ref_config *c, const float *x, const float *norm_w,
+                            float eps, const float *w_router, const float *bias, int T,
+                            int32_t *ids, float *w, int32_t *keff, float *logits);
+int moe_ref_topk_hits(int T, int K, const int32_t *ids_pred, const int32_t *keff_pred,
+                      const int32_t *ids_true, const int32_t *keff_true, int32_t *hits);
 
 #ifdef __cplusplus
 }

@@ -393,3 +393,88 @@ def test_tiny_layer_regression(ref):
     assert out["ids"].tolist() == doc["ids"] and out["keff"].tolist() == doc["keff"]
     np.testing.assert_allclose(out["w"], doc["w"], rtol=1e-6)
     np.testing.assert_allclose(out["y"][:, :8], doc["y_first8"], rtol=1e-9, atol=1e-9 * doc["y_rms"])
+
+
+# ----------------------------------------------------------------------------------------------
+# Router look-ahead ["MoE 路由与专家流式加载" §5, la_predict]: RMSNorm, then the router.
+# ----------------------------------------------------------------------------------------------
+
+def test_rmsnorm_hand_case(ref):
+    # x = (1, 2, 3, 4): mean of squares 30/4 = 7.5, sqrt(7.5) = 2.7386127875258306
+    x = np.array([[1.0, 2.0, 3.0, 4.0]], np.float32)
+    out = ref.rmsnorm(x, np.ones(4, np.float32), 0.0)
+    np.testing.assert_allclose(out[0], [0.36514837167011072, 0.73029674334022144,
+                                        1.0954451150103321, 1.4605934866804429], rtol=1e-7)
+    # a weight per column multiplies the normalised value
+    out = ref.rmsnorm(x, np.array([2.0, 0.5, -1.0, 0.0], np.float32), 0.0)
+    np.testing.assert_allclose(out[0], [0.73029674334022144, 0.36514837167011072,
+                                        -1.0954451150103321, 0.0], rtol=1e-7)
+    # eps enters under the root: (1, 1, 1, 1) with eps 3 -> 1 / sqrt(1 + 3) = 0.5
+    out = ref.rmsnorm(np.ones((1, 4), np.float32), np.ones(4, np.float32), 3.0)
+    np.testing.assert_allclose(out[0], [0.5] * 4, rtol=1e-7)
+
+
+def test_rmsnorm_invariants(ref):
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(5, 64)).astype(np.float32) * 3.0
+    g = np.ones(64, np.float32)
+    out = ref.rmsnorm(x, g, 0.0)
+    # unit mean square per row (a wrong divisor, H-1 or a sum, breaks this)
+    np.testing.assert_allclose((out.astype(np.float64) ** 2).mean(axis=1), 1.0, rtol=1e-6)
+    # invariant to a positive scale of the row, odd in its sign
+    np.testing.assert_allclose(ref.rmsnorm(x * 37.5, g, 0.0), out, rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(ref.rmsnorm(-x, g, 0.0), -out, rtol=0, atol=0)
+    # a zero row stays zero, with or without eps
+    z = np.zeros((2, 64), np.float32)
+    assert not ref.rmsnorm(z, g, 0.0).any() and not ref.rmsnorm(z, g, 1e-5).any()
+
+
+def test_route_lookahead_brute_force(ref):
+    # numpy fp64 restatement of la_predict on tiny inputs: normalise, logits, sigmoid, + bias,
+    # top-K by a stable sort of -choice (equal choices -> the lower expert id)
+    rng = np.random.default_rng(11)
+    H, E, K, T = 64, 12, 3, 40
+    cfg = ref.make_config(H, E, K, 64, norm_topk_prob=1, routed_scaling_factor=1.0)
+    x = (rng.normal(size=(T, H)) * rng.uniform(0.1, 50.0, size=(T, 1))).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, size=H).astype(np.float32)
+    wr = rng.normal(size=(E, H)).astype(np.float32) / 8.0
+    bias = rng.normal(size=E).astype(np.float32) * 0.1
+    got = ref.route_lookahead(cfg, x, g, 1e-5, wr, bias)
+    xd = x.astype(np.float64)
+    xn = xd / np.sqrt((xd ** 2).mean(axis=1, keepdims=True) + 1e-5) * g.astype(np.float64)
+    sig = _sig64(xn @ wr.astype(np.float64).T)
+    choice = sig + bias.astype(np.float64)
+    for t in range(T):
+        order = np.argsort(-choice[t], kind="stable")[:K]
+        srt = np.sort(-choice[t])
+        if srt[K] - srt[K - 1] < 1e-5:
+            continue   # near tie: fp32 and fp64 may order it differently
+        assert got["ids"][t].tolist() == order.tolist()
+        gates = sig[t, order]
+        np.testing.assert_allclose(got["w"][t], gates / gates.sum(), rtol=1e-5)
+    # with a unit-RMS input and unit weights the look-ahead is the plain router
+    xu = (xn / g.astype(np.float64)).astype(np.float32)
+    direct = ref.route(cfg, xu, wr, bias)
+    ahead = ref.route_lookahead(cfg, xu * 9.0, np.ones(H, np.float32), 0.0, wr, bias)
+    assert np.array_equal(direct["ids"], ahead["ids"])
+
+
+def test_topk_hits_brute_force(ref):
+    rng = np.random.default_rng(5)
+    T, K, E = 300, 8, 20
+    def rand_routing():
+        ids = np.full((T, K), -1, np.int32)
+        keff = rng.integers(0, K + 1, size=T).astype(np.int32)
+        for t in range(T):
+            ids[t, :keff[t]] = rng.choice(E, size=keff[t], replace=False)
+        return ids, keff
+    ip, kp = rand_routing()
+    it, kt = rand_routing()
+    hits = ref.topk_hits(ip, kp, it, kt)
+    for t in range(T):
+        want = len(set(ip[t, :kp[t]].tolist()) & set(it[t, :kt[t]].tolist()))
+        assert hits[t] == want
+    # a routing shares all of its kept experts with itself, none with a disjoint one
+    assert np.array_equal(ref.topk_hits(ip, kp, ip, kp), kp)
+    other = np.where(ip >= 0, ip + E, -1).astype(np.int32)
+    assert not ref.topk_hits(ip, kp, other, kp).any()
