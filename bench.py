@@ -358,6 +358,37 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(T * k2 * world / (ms_e2e / 1e3), 1), "unit": UNIT,
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
 
+    # router look-ahead ["MoE 路由与专家流式加载" §5]: RMSNorm of a residual state + the next
+    # layer's router, timed alone at the workload's batch (HBM-bound: the router weights)
+    lookahead = None
+    if rank == 0 and world == 1:
+        hh, gg, wn, bn = synth.gen_lookahead(wl, T, batch=rank)
+        hh, gg, wn, bn = hh.to(dev), gg.to(dev), wn.to(dev), bn.to(dev)
+        ids_p = torch.empty(T, wl.top_k, dtype=torch.int32, device=dev)
+        w_p = torch.empty(T, wl.top_k, dtype=torch.float32, device=dev)
+        k_p = torch.empty(T, dtype=torch.int32, device=dev)
+        # copies of the router weights cycled call by call, twice the L2 size in all, so every
+        # call reads its weights from HBM
+        n_copies = max(1, min(64, -(-2 * 129 * 2 ** 20 // wn.numel() // 4)))
+        wns = [wn.clone() for _ in range(n_copies)]
+        for k in range(5):
+            moe.moe_route_lookahead(cfg, hh, gg, 1e-5, wns[k % n_copies], bn, ids_p, w_p, k_p, ws)
+        n_la = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for k in range(n_la):
+            moe.moe_route_lookahead(cfg, hh, gg, 1e-5, wns[k % n_copies], bn, ids_p, w_p, k_p, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n_la
+        la_bytes = wl.n_experts * wl.hidden * 4 + wl.hidden * 4 + 2 * T * wl.hidden * 4
+        lookahead = {"tokens": T, "us_per_call": round(us, 2),
+                     "algorithmic_bytes": la_bytes,
+                     "hbm_frac": round(la_bytes / (us / 1e6) / 1e9 / peak, 4),
+                     "l2": "router weights cycled over %d copies (> 2x L2)" % n_copies}
+        del wns
+
     sweep = None
     if not args.no_sweep and rank == 0 and world == 1 and len(wl.tokens) > 1:
         sweep = {}
@@ -401,6 +432,8 @@ def run_ours(args, world, rank, local):
     }
     if sweep:
         out["sweep"] = sweep
+    if lookahead:
+        out["router_lookahead"] = lookahead
     return out
 
 

@@ -123,6 +123,31 @@ typedef struct moe_routing {
  * tokens.  Returns 0 for an invalid config or max_tokens < 0. */
 size_t moe_workspace_size(const moe_config *cfg, int max_tokens);
 
+/* Router look-ahead ["MoE 路由与专家流式加载" §5, la_predict]: predicts a
+ * layer's top-K from a residual state with the layer's own routing pipeline.
+ *   x [T][H] fp32: the residual state (e.g. an earlier layer's
+ *     post-attention state); norm_w [H] fp32: the layer's RMSNorm weight;
+ *     eps: the RMSNorm epsilon, finite and >= 0.
+ *   The rows are normalised, x / sqrt(mean(x^2) + eps) * norm_w, into the
+ *   workspace (a row with mean square + eps = 0 becomes zeros), and routed
+ *   exactly like moe_route with w_router / bias (the layer's router).
+ *   ids, w, keff: as moe_route writes them.
+ * Same errors as moe_route, plus MOE_ERR_ARG for a bad eps. */
+int moe_route_lookahead(const moe_config *cfg, const float *x, const float *norm_w, float eps,
+                        const float *w_router, const float *bias, int T, int32_t *ids, float *w,
+                        int32_t *keff, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Hit count of a predicted routing against the true one, per token, behind
+ * the pages' recall figure ["MoE 路由与专家流式加载" §5: 71.6% of the true
+ * top-8].  ids_* [T][K] int32 and keff_* [T] int32 as moe_route writes them
+ * (keff values are clamped to [0, K]).  hits [T] int32: how many of the
+ * first keff_pred[t] predicted ids appear among the first keff_true[t] true
+ * ids.  recall = sum(hits) / sum(keff_true).  No workspace; device
+ * pointers; asynchronous on stream. */
+int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t *keff_pred,
+                  const int32_t *ids_true, const int32_t *keff_true, int T, int32_t *hits,
+                  void *stream);
+
 /* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
  * device work): 1 = the tcgen05 tensor-core grouped GEMM (batches beyond the
  * decode route, T > 64, with hidden, d_ff and d_ff_shared multiples of 512),

@@ -33,7 +33,8 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
-           "moe_route_noalloc", "moe_ffn_uses_tensor_cores")
+           "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
+           "moe_topk_hits")
 
 
 class MoeError(RuntimeError):
@@ -94,6 +95,8 @@ def load_library():
     L.moe_ffn_uses_tensor_cores.argtypes = [vp, i32]
     L.moe_ffn_uses_tensor_cores.restype = i32
     L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
     L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -151,6 +154,24 @@ def moe_route(cfg, x, w_router, bias, ids, w, keff, workspace, stream=None):
     _check(load_library().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), T,
                                      _ptr(ids), _ptr(w), _ptr(keff), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "moe_route")
+
+
+def moe_route_lookahead(cfg, x, norm_w, eps, w_router, bias, ids, w, keff, workspace, stream=None):
+    """A layer's top-K predicted from the residual state x: RMSNorm with norm_w and eps, then
+    the layer's router (w_router, bias); outputs as moe_route."""
+    T = x.shape[0]
+    _check(load_library().moe_route_lookahead(ctypes.byref(cfg), _ptr(x), _ptr(norm_w), float(eps),
+                                               _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
+                                               _ptr(keff), _ptr(workspace), workspace.numel(),
+                                               _stream(stream)), "moe_route_lookahead")
+
+
+def moe_topk_hits(cfg, ids_pred, keff_pred, ids_true, keff_true, hits, stream=None):
+    """Per token, how many experts the predicted and the true routing both keep."""
+    T = keff_pred.shape[0]
+    _check(load_library().moe_topk_hits(ctypes.byref(cfg), _ptr(ids_pred), _ptr(keff_pred),
+                                         _ptr(ids_true), _ptr(keff_true), T, _ptr(hits),
+                                         _stream(stream)), "moe_topk_hits")
 
 
 def moe_route_noalloc(cfg, x, w_router, bias, ids, w, keff, stream=None):

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -378,6 +379,7 @@ WsLayout ws_layout(const moe_config &c, int T)
     L.hscale = take(rows * 4);
     L.hcsum = take(rows * (fm / 32) * 4);
     L.y = take((rows > s_dn * rows_s ? rows : s_dn * rows_s) * H * 4);
+    L.xn = take((size_t)T * H * 4);
     L.total = off;
     return L;
 }
@@ -396,6 +398,45 @@ size_t moe_workspace_size(const moe_config *cfg, int max_tokens)
 }
 
 const char *moe_last_error_string(void) { return g_err; }
+
+int moe_route_lookahead(const moe_config *cfg, const float *x, const float *norm_w, float eps,
+                        const float *w_router, const float *bias, int T, int32_t *ids, float *w,
+                        int32_t *keff, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc;
+    if ((rc = validate_route_args(cfg, x, w_router, bias, T, ids, w, keff))) return rc;
+    if (T == 0) return ok();
+    REQUIRE_PTR(norm_w, 16);
+    if (!(eps >= 0.0f) || std::isinf(eps)) return fail(MOE_ERR_ARG, "eps must be finite and >= 0 (got %g)", (double)eps);
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *xn = at<float>(workspace, L.xn);
+    cudaError_t e = launch_rmsnorm(x, norm_w, eps, T, cfg->hidden, xn, st);
+    if (e == cudaSuccess)
+        e = launch_router(*cfg, xn, w_router, bias, T, at<float>(workspace, L.logits), ids, w, keff, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router look-ahead launch");
+    return ok();
+}
+
+int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t *keff_pred,
+                  const int32_t *ids_true, const int32_t *keff_true, int T, int32_t *hits,
+                  void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    REQUIRE_PTR(ids_pred, 4);
+    REQUIRE_PTR(keff_pred, 4);
+    REQUIRE_PTR(ids_true, 4);
+    REQUIRE_PTR(keff_true, 4);
+    REQUIRE_PTR(hits, 4);
+    if ((rc = check_device())) return rc;
+    const cudaError_t e = launch_topk_hits(ids_pred, keff_pred, ids_true, keff_true, T, cfg->top_k,
+                                           hits, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k hit count launch");
+    return ok();
+}
 
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
 {

@@ -103,6 +103,7 @@ struct WsLayout {
     size_t h;                         // [rows][Fmax] fp32
     size_t hp, hp_plane_floats;       // partial gate planes then partial up planes
     size_t xbf, hbf;                  // bf16 codes of x and h (tensor path)
+    size_t xn;                        // [T][H] fp32 RMSNorm output (router look-ahead)
     size_t hq, hscale, hcsum;         // quantised h
     size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
     size_t plan;                      // FfnPlan
@@ -165,6 +166,14 @@ cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t r
                            const float *w, const int32_t *offsets, const int32_t *tok,
                            const int32_t *pair_of, int S_r, int S_s, int64_t plane, int T,
                            float *y, cudaStream_t st);
+
+// router look-ahead (lookahead.cu): RMSNorm of [T][H] rows, and the per-token count of the
+// experts two routings both keep
+cudaError_t launch_rmsnorm(const float *x, const float *g, float eps, int T, int H, float *out,
+                           cudaStream_t st);
+cudaError_t launch_topk_hits(const int32_t *ids_pred, const int32_t *keff_pred,
+                             const int32_t *ids_true, const int32_t *keff_true, int T, int K,
+                             int32_t *hits, cudaStream_t st);
 
 // host helpers shared with the entry points outside moe_api.cu
 int set_error(int code, const char *fmt, ...);   // records the thread's last error message

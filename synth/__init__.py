@@ -37,6 +37,8 @@ T_X = 1
 T_ROUTER_W = 2
 T_BIAS = 3
 T_ZIPF_PERM = 4
+T_RESID, T_RESID_SCALE, T_NORM_W = 5, 6, 7   # router look-ahead inputs
+T_NEXT_ROUTER_W, T_NEXT_BIAS = 8, 9
 T_GATE_CODES, T_GATE_SCALES = 10, 11
 T_UP_CODES, T_UP_SCALES = 12, 13
 T_DOWN_CODES, T_DOWN_SCALES = 14, 15
@@ -192,6 +194,20 @@ def gen_router(wl: Workload) -> Tuple[torch.Tensor, torch.Tensor]:
     else:
         bias = normal(stream_key(wl.seed, T_BIAS), E, wl.bias_std)
     return w, bias
+
+
+def gen_lookahead(wl: Workload, T: int, batch: int = 0):
+    """Inputs of the router look-ahead: a residual state [T, H] (N(0, 1) rows times a per-token
+    magnitude U(0.5, 20), as residual streams grow across layers), an RMSNorm weight [H] ~
+    U(0.5, 1.5), and a later layer's router of the workload's shape (its own weights and bias,
+    drawn like gen_router's).  All float32 on the CPU."""
+    H, E = wl.hidden, wl.n_experts
+    z = normal(stream_key(wl.seed, T_RESID, batch), T * H).view(T, H)
+    mag = uniform_range(stream_key(wl.seed, T_RESID_SCALE, batch), T, 0.5, 20.0).view(T, 1)
+    g = uniform_range(stream_key(wl.seed, T_NORM_W), H, 0.5, 1.5)
+    w = normal(stream_key(wl.seed, T_NEXT_ROUTER_W), E * H, wl.router_std).view(E, H)
+    bias = normal(stream_key(wl.seed, T_NEXT_BIAS), E, wl.bias_std if wl.bias_std > 0 else 0.1)
+    return z * mag, g, w, bias
 
 
 def _matrix_keys(shared: bool) -> Sequence[Tuple[str, int, int, bool]]:

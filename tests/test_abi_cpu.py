@@ -59,6 +59,20 @@ def test_ffn_path_query(lib):
     assert moe.moe_ffn_uses_tensor_cores(_cfg(top_k=9), 16) == -1
 
 
+def test_lookahead_validation(lib):
+    cfg = _cfg()
+    args = lambda eps, norm=FAKE: (ctypes.byref(cfg), FAKE, norm, ctypes.c_float(eps), FAKE, FAKE, 4,
+                                   FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert lib.moe_route_lookahead(*args(-1.0)) == moe.MOE_ERR_ARG
+    assert lib.moe_route_lookahead(*args(float("nan"))) == moe.MOE_ERR_ARG
+    assert lib.moe_route_lookahead(*args(float("inf"))) == moe.MOE_ERR_ARG
+    assert lib.moe_route_lookahead(*args(1e-5, norm=None)) == moe.MOE_ERR_ARG
+    assert lib.moe_route_lookahead(*args(1e-5, norm=FAKE + 4)) == moe.MOE_ERR_ALIGN
+    assert lib.moe_topk_hits(ctypes.byref(cfg), FAKE, FAKE, None, FAKE, 4, FAKE, None) == moe.MOE_ERR_ARG
+    assert lib.moe_topk_hits(ctypes.byref(_cfg(top_k=9)), FAKE, FAKE, FAKE, FAKE, 4, FAKE, None) \
+        == moe.MOE_ERR_SHAPE
+
+
 FAKE = 1 << 20   # aligned, never dereferenced: validation fails before any use
 
 

@@ -347,3 +347,75 @@ def test_generator_identical_on_gpu(moe):
     h = synth.gen_experts(wl, experts=[0, 77, 255])
     for k in h:
         assert torch.equal(d[k][[0, 77, 255]].cpu(), h[k])
+
+
+# ----------------------------------------------------------------------------------------------
+# Router look-ahead ["MoE 路由与专家流式加载" §5]: RMSNorm of a residual state, then the router.
+# ----------------------------------------------------------------------------------------------
+
+LOOKAHEAD_CASES = [("tiny", 16), ("glm_decode", 1), ("glm_decode", 32), ("a3b_decode", 64),
+                   ("wide", 512), ("prefill", 4096)]
+
+
+@pytest.mark.parametrize("name,T", LOOKAHEAD_CASES)
+def test_route_lookahead(moe, name, T):
+    wl = synth.WORKLOADS[name]
+    h, g, wr, bias = synth.gen_lookahead(wl, T, batch=1)
+    eps = 1e-5
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    K = wl.top_k
+    ids = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    keff = torch.empty(T, dtype=torch.int32, device="cuda")
+    moe.moe_route_lookahead(cfg, h.cuda(), g.cuda(), eps, wr.cuda(), bias.cuda(), ids, w, keff, ws)
+    torch.cuda.synchronize()
+    ref = oracle.route_lookahead(oracle.config_of(wl), h, g, eps, wr, bias, with_logits=True)
+    margin = routing_margins(ref["logits"], bias.numpy(), K, wl.top_p)
+    near = _check_routing(wl, (ids.cpu().numpy(), w.cpu().numpy(), keff.cpu().numpy()), ref, margin)
+    if name == "tiny":
+        assert near == 0
+    assert near <= max(1, T // 50)
+
+
+def test_route_lookahead_zero_rows_and_eps(moe):
+    # all-zero rows normalise to zeros (mean square + eps = 0 with eps 0): every logit is 0,
+    # so the choice is the bias alone on both sides
+    wl = synth.WORKLOADS["tiny"]
+    h, g, wr, bias = synth.gen_lookahead(wl, 8)
+    h[2] = 0.0
+    h[5] = 0.0
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, 8)
+    K = wl.top_k
+    for eps in (0.0, 0.25):
+        ids = torch.empty(8, K, dtype=torch.int32, device="cuda")
+        w = torch.empty(8, K, dtype=torch.float32, device="cuda")
+        keff = torch.empty(8, dtype=torch.int32, device="cuda")
+        moe.moe_route_lookahead(cfg, h.cuda(), g.cuda(), eps, wr.cuda(), bias.cuda(), ids, w, keff, ws)
+        ref = oracle.route_lookahead(oracle.config_of(wl), h, g, eps, wr, bias, with_logits=True)
+        assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+        assert np.array_equal(keff.cpu().numpy(), ref["keff"])
+        np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=2e-5, atol=1e-7)
+    with pytest.raises(moe.MoeError):
+        moe.moe_route_lookahead(cfg, h.cuda(), g.cuda(), -1.0, wr.cuda(), bias.cuda(), ids, w, keff, ws)
+
+
+def test_topk_hits(moe):
+    # the look-ahead prediction against the routing of a later state (the same state plus a
+    # perturbation), and against itself: integer counts, compared exactly
+    wl = synth.WORKLOADS["glm_decode"]
+    T, K = 32, wl.top_k
+    h, g, wr, bias = synth.gen_lookahead(wl, T, batch=2)
+    pert, _, _, _ = synth.gen_lookahead(wl, T, batch=3)
+    cfg = oracle.config_of(wl)
+    pred = oracle.route_lookahead(cfg, h, g, 1e-5, wr, bias)
+    true = oracle.route_lookahead(cfg, h + 0.5 * pert, g, 1e-5, wr, bias)
+    true["keff"][::5] = np.minimum(true["keff"][::5], 3)   # some shorter kept sets
+    mcfg = moe_cfg(wl)
+    for (ip, kp, it, kt) in ((pred["ids"], pred["keff"], true["ids"], true["keff"]),
+                             (pred["ids"], pred["keff"], pred["ids"], pred["keff"])):
+        hits = torch.full((T,), -9, dtype=torch.int32, device="cuda")
+        moe.moe_topk_hits(mcfg, torch.from_numpy(ip).cuda(), torch.from_numpy(kp).cuda(),
+                          torch.from_numpy(it).cuda(), torch.from_numpy(kt).cuda(), hits)
+        assert np.array_equal(hits.cpu().numpy(), oracle.topk_hits(ip, kp, it, kt))
