@@ -69,6 +69,7 @@ def lib():
         L.moe_ref_rmsnorm.argtypes = [vp, vp, ctypes.c_float, i32, i32, vp]
         L.moe_ref_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp]
         L.moe_ref_topk_hits.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.moe_ref_quantize_int4.argtypes = [vp, i32, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -134,6 +135,16 @@ def route(cfg: Config, x, w_router, bias, with_logits: bool = False):
     if with_logits:
         out["logits"] = logits
     return out
+
+
+def quantize_int4(w):
+    """fp32 weights [rows][K] -> (packed nibbles [rows][K/2] u8, scales [rows][K/64] fp32)."""
+    w = _np(w, np.float32)
+    rows, K = w.shape
+    packed = np.zeros((rows, K // 2), np.uint8)
+    scales = np.zeros((rows, K // 64), np.float32)
+    _check(lib().moe_ref_quantize_int4(_p(w), rows, K, _p(packed), _p(scales)), "moe_ref_quantize_int4")
+    return packed, scales
 
 
 def rmsnorm(x, g, eps: float):

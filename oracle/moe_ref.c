@@ -523,3 +523,49 @@ int moe_ref_topk_hits(int T, int K, const int32_t *ids_pred, const int32_t *keff
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Offline weight quantiser: fp32 -> int4-gs64 (the container format the pages
+ * recommend, "colibri 开发演进实录" §2.1 int4-gs64; the conversion tool is
+ * `coli convert`, ibid. §9).  The scale rule is not stated; the reading
+ * taken is the symmetric absmax one of the activations, per 64-weight group:
+ *   amax  = max |w|   over the group
+ *   scale = amax / 7                  (fp32)
+ *   u     = clamp(rint(w * (7 / amax)), -7, 7) + 8   (round half to even, fp32)
+ * so the group's largest magnitude lands on +-7 and value = scale * (u - 8);
+ * an all-zero group gets scale 0 and codes 8.  Packing as the layer reads it:
+ * byte j of a row holds element 2j in the low nibble and 2j+1 in the high.
+ *   w [rows][K] fp32, K a multiple of 64 -> packed [rows][K/2] u8,
+ *   scales [rows][K/64] fp32.
+ * ------------------------------------------------------------------------ */
+int moe_ref_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales)
+{
+    if (rows < 0 || K <= 0 || K % GS) return -2;
+    if (rows > 0 && (!w || !packed || !scales)) return -1;
+    const int G = K / GS;
+    for (int r = 0; r < rows; ++r) {
+        for (int g = 0; g < G; ++g) {
+            const float *v = w + (size_t)r * K + (size_t)g * GS;
+            float amax = 0.0f;
+            for (int k = 0; k < GS; ++k) {
+                const float a = fabsf(v[k]);
+                if (a > amax) amax = a;
+            }
+            const float inv = amax > 0.0f ? 7.0f / amax : 0.0f;
+            scales[(size_t)r * G + g] = amax / 7.0f;
+            uint8_t *out = packed + (size_t)r * (K / 2) + (size_t)g * (GS / 2);
+            for (int j = 0; j < GS / 2; ++j) {
+                int u[2];
+                for (int h = 0; h < 2; ++h) {
+                    const float p = v[2 * j + h] * inv;
+                    float q = rintf(p);
+                    if (q > 7.0f) q = 7.0f;
+                    if (q < -7.0f) q = -7.0f;
+                    u[h] = (int)q + 8;
+                }
+                out[j] = (uint8_t)(u[0] | (u[1] << 4));
+            }
+        }
+    }
+    return 0;
+}

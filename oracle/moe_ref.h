@@ -22,6 +22,8 @@
  *             "MoE 路由与专家流式加载" §1.3]
  *   shared    always-on shared expert added to the output
  *             ["MoE 路由与专家流式加载" §1.4]
+ *   quantise  offline fp32 -> int4-gs64 weights, symmetric absmax per group
+ *             ["colibri 开发演进实录" §2.1]
  *   lookahead RMSNorm then the router, predicting a later layer's top-K from
  *             a residual state, and the recall of such a prediction
  *             ["MoE 路由与专家流式加载" §5]
@@ -143,6 +145,12 @@ int moe_ref_route_lookahead(const moe_ref_config *c, const float *x, const float
                             int32_t *ids, float *w, int32_t *keff, float *logits);
 int moe_ref_topk_hits(int T, int K, const int32_t *ids_pred, const int32_t *keff_pred,
                       const int32_t *ids_true, const int32_t *keff_true, int32_t *hits);
+
+/* Offline fp32 -> int4-gs64 weight quantiser ("colibri 开发演进实录" §2.1):
+ * per 64-weight group, scale = amax / 7 and u = clamp(rint(w * 7 / amax), -7, 7)
+ * + 8 (fp32, round half to even); w [rows][K] -> packed [rows][K/2] (element
+ * 2j low nibble) and scales [rows][K/64].  Returns -2 unless K % 64 == 0. */
+int moe_ref_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales);
 
 #ifdef __cplusplus
 }

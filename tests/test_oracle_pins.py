@@ -478,3 +478,60 @@ def test_topk_hits_brute_force(ref):
     assert np.array_equal(ref.topk_hits(ip, kp, ip, kp), kp)
     other = np.where(ip >= 0, ip + E, -1).astype(np.int32)
     assert not ref.topk_hits(ip, kp, other, kp).any()
+
+
+# ----------------------------------------------------------------------------------------------
+# Offline fp32 -> int4-gs64 weight quantiser ("colibri 开发演进实录" §2.1; reading: symmetric
+# absmax per group, scale = amax / 7, codes rint(w * 7 / amax) + 8).
+# ----------------------------------------------------------------------------------------------
+
+def test_quantize_int4_hand_case(ref):
+    w = np.zeros((1, 128), np.float32)
+    w[0, :6] = [7.0, -7.0, 3.5, 2.5, -0.5, 0.49]   # group 0: amax 7, scale 1
+    w[0, 64:68] = [0.0, 1.0, -2.0, 0.25]             # group 1: amax 2, scale 2/7
+    packed, scales = ref.quantize_int4(w)
+    np.testing.assert_array_equal(scales[0], np.float32([1.0, np.float32(2.0) / np.float32(7.0)]))
+    # u = q + 8, element 2j low nibble: (7,-7) -> 15,1; (3.5, 2.5) -> 4, 2 (half to even);
+    # (-0.5, 0.49) -> -0 (half to even), 0
+    assert packed[0, 0] == 15 | (1 << 4)
+    assert packed[0, 1] == 12 | (10 << 4)
+    assert packed[0, 2] == 8 | (8 << 4)
+    assert (packed[0, 3:32] == 0x88).all()
+    # group 1: 0 -> 0; 1 * 3.5 = 3.5 -> 4; -2 * 3.5 = -7; 0.25 * 3.5 = 0.875 -> 1
+    assert packed[0, 32] == 8 | (12 << 4)
+    assert packed[0, 33] == 1 | (9 << 4)
+    # an all-zero row: scale 0, every code the zero point
+    p0, s0 = ref.quantize_int4(np.zeros((2, 64), np.float32))
+    assert (p0 == 0x88).all() and (s0 == 0).all()
+
+
+def _dequant(packed, scales):
+    lo = (packed & 0x0F).astype(np.int32)
+    hi = (packed >> 4).astype(np.int32)
+    u = np.empty((packed.shape[0], packed.shape[1] * 2), np.int32)
+    u[:, 0::2], u[:, 1::2] = lo, hi
+    return (u - 8).astype(np.float64) * np.repeat(scales.astype(np.float64), 64, axis=1), u
+
+
+def test_quantize_int4_properties(ref):
+    rng = np.random.default_rng(3)
+    w = (rng.normal(size=(40, 256)) * rng.uniform(1e-3, 10.0, size=(40, 1))).astype(np.float32)
+    w[5, 64:128] = 0.0                       # an empty group
+    packed, scales = ref.quantize_int4(w)
+    deq, u = _dequant(packed, scales)
+    s = np.repeat(scales.astype(np.float64), 64, axis=1)
+    # codes within 1..15 (the -8 level is never used), the group's largest magnitude on +-7
+    assert u.min() >= 1 and u.max() <= 15
+    amax = np.abs(w.astype(np.float64)).reshape(40, 4, 64).max(axis=2)
+    np.testing.assert_allclose(scales, amax / 7.0, rtol=1e-7)
+    g_umax = np.abs(u - 8).reshape(40, 4, 64).max(axis=2)
+    assert ((g_umax == 7) | (amax == 0)).all()
+    # round to nearest: every weight within half a step (+ fp32 slack) of its value
+    assert (np.abs(deq - w) <= 0.5 * s * (1 + 1e-5) + 1e-30).all()
+    # values already on the grid come back exactly
+    grid = (rng.integers(-7, 8, size=(8, 128)).astype(np.float32) * np.float32(0.375))
+    grid[:, 0] = 7 * 0.375          # every group's amax on +-7 -> scale exactly 0.375
+    grid[:, 64] = -7 * 0.375
+    pg, sg = ref.quantize_int4(grid)
+    dg, _ = _dequant(pg, sg)
+    np.testing.assert_array_equal(dg, grid.astype(np.float64))
