@@ -505,7 +505,7 @@ def test_quantize_int4_hand_case(ref):
     assert (p0 == 0x88).all() and (s0 == 0).all()
 
 
-def _dequant(packed, scales):
+def _dequant_int4(packed, scales):
     lo = (packed & 0x0F).astype(np.int32)
     hi = (packed >> 4).astype(np.int32)
     u = np.empty((packed.shape[0], packed.shape[1] * 2), np.int32)
@@ -518,7 +518,7 @@ def test_quantize_int4_properties(ref):
     w = (rng.normal(size=(40, 256)) * rng.uniform(1e-3, 10.0, size=(40, 1))).astype(np.float32)
     w[5, 64:128] = 0.0                       # an empty group
     packed, scales = ref.quantize_int4(w)
-    deq, u = _dequant(packed, scales)
+    deq, u = _dequant_int4(packed, scales)
     s = np.repeat(scales.astype(np.float64), 64, axis=1)
     # codes within 1..15 (the -8 level is never used), the group's largest magnitude on +-7
     assert u.min() >= 1 and u.max() <= 15
@@ -533,5 +533,5 @@ def test_quantize_int4_properties(ref):
     grid[:, 0] = 7 * 0.375          # every group's amax on +-7 -> scale exactly 0.375
     grid[:, 64] = -7 * 0.375
     pg, sg = ref.quantize_int4(grid)
-    dg, _ = _dequant(pg, sg)
+    dg, _ = _dequant_int4(pg, sg)
     np.testing.assert_array_equal(dg, grid.astype(np.float64))
