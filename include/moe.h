@@ -148,6 +148,21 @@ int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t 
                   const int32_t *ids_true, const int32_t *keff_true, int T, int32_t *hits,
                   void *stream);
 
+/* Offline weight quantiser: fp32 -> the int4-gs64 layout every call above
+ * reads ["colibri 开发演进实录" §2.1 int4-gs64; the pages' converter is
+ * `coli convert`, §9].
+ *   w [rows][K] fp32 (device, 16-byte aligned), K a multiple of 64.
+ *   packed [rows][K/2] u8 and scales [rows][K/64] fp32 (device, 16-byte
+ *   aligned), written in full: per 64-weight group, scale = amax / 7 and
+ *   u = clamp(rint(w * (7 / amax)), -7, 7) + 8 (fp32, round half to even),
+ *   byte j = element 2j (low nibble) | element 2j+1 (high); an all-zero
+ *   group gets scale 0 and codes 8.
+ * A whole expert set converts in one call: rows = E * F for w_gate / w_up
+ * ([E][F][H], K = H), E * H for w_down (K = F).  MOE_ERR_SHAPE for rows < 0
+ * or a bad K.  Asynchronous on stream. */
+int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                           void *stream);
+
 /* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
  * device work): 1 = the tcgen05 tensor-core grouped GEMM (batches beyond the
  * decode route, T > 64, with hidden, d_ff and d_ff_shared multiples of 512),

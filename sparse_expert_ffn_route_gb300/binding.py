@@ -34,7 +34,7 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
-           "moe_topk_hits")
+           "moe_topk_hits", "moe_quantize_int4_gs64")
 
 
 class MoeError(RuntimeError):
@@ -97,6 +97,7 @@ def load_library():
     L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
+    L.moe_quantize_int4_gs64.argtypes = [vp, i32, i32, vp, vp, vp]
     L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -172,6 +173,15 @@ def moe_topk_hits(cfg, ids_pred, keff_pred, ids_true, keff_true, hits, stream=No
     _check(load_library().moe_topk_hits(ctypes.byref(cfg), _ptr(ids_pred), _ptr(keff_pred),
                                          _ptr(ids_true), _ptr(keff_true), T, _ptr(hits),
                                          _stream(stream)), "moe_topk_hits")
+
+
+def moe_quantize_int4_gs64(w, packed, scales, stream=None):
+    """fp32 weights w [rows][K] (K a multiple of 64) -> int4-gs64: packed [rows][K/2] uint8
+    and scales [rows][K/64] float32 (every leading dimension flattened into rows)."""
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    _check(load_library().moe_quantize_int4_gs64(_ptr(w), rows, K, _ptr(packed), _ptr(scales),
+                                                  _stream(stream)), "moe_quantize_int4_gs64")
 
 
 def moe_route_noalloc(cfg, x, w_router, bias, ids, w, keff, stream=None):

@@ -438,6 +438,22 @@ int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t 
     return ok();
 }
 
+int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                           void *stream)
+{
+    if (rows < 0) return fail(MOE_ERR_SHAPE, "rows must be >= 0 (got %d)", rows);
+    if (K <= 0 || K % kGroup) return fail(MOE_ERR_SHAPE, "K must be a positive multiple of 64 (got %d)", K);
+    if (rows == 0) return ok();
+    REQUIRE_PTR(w, 16);
+    REQUIRE_PTR(packed, 16);
+    REQUIRE_PTR(scales, 16);
+    int rc;
+    if ((rc = check_device())) return rc;
+    const cudaError_t e = launch_quantize_int4(w, rows, K, packed, scales, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "weight quantiser launch");
+    return ok();
+}
+
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
 {
     if (check_config(cfg) != MOE_OK || T < 0) return -1;

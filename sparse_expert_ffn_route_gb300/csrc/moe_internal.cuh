@@ -175,6 +175,10 @@ cudaError_t launch_topk_hits(const int32_t *ids_pred, const int32_t *keff_pred,
                              const int32_t *ids_true, const int32_t *keff_true, int T, int K,
                              int32_t *hits, cudaStream_t st);
 
+// offline fp32 -> int4-gs64 weight quantiser (quantize_weights.cu)
+cudaError_t launch_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                                 cudaStream_t st);
+
 // host helpers shared with the entry points outside moe_api.cu
 int set_error(int code, const char *fmt, ...);   // records the thread's last error message
 int require_device();                            // MOE_OK on a compute capability 10.3 device

@@ -39,6 +39,7 @@ T_BIAS = 3
 T_ZIPF_PERM = 4
 T_RESID, T_RESID_SCALE, T_NORM_W = 5, 6, 7   # router look-ahead inputs
 T_NEXT_ROUTER_W, T_NEXT_BIAS = 8, 9
+T_DENSE_W, T_DENSE_ROW_SCALE = 20, 21        # fp32 weights for the offline quantiser
 T_GATE_CODES, T_GATE_SCALES = 10, 11
 T_UP_CODES, T_UP_SCALES = 12, 13
 T_DOWN_CODES, T_DOWN_SCALES = 14, 15
@@ -208,6 +209,15 @@ def gen_lookahead(wl: Workload, T: int, batch: int = 0):
     w = normal(stream_key(wl.seed, T_NEXT_ROUTER_W), E * H, wl.router_std).view(E, H)
     bias = normal(stream_key(wl.seed, T_NEXT_BIAS), E, wl.bias_std if wl.bias_std > 0 else 0.1)
     return z * mag, g, w, bias
+
+
+def gen_dense_weights(wl: Workload, rows: int, K: int, matrix: int = 0) -> torch.Tensor:
+    """fp32 weights [rows, K] before quantisation: N(0, 1) entries times a per-row magnitude
+    U(0.001, 0.05) (weight rows of trained layers differ in scale); ``matrix`` selects an
+    independent matrix.  CPU."""
+    z = normal(stream_key(wl.seed, T_DENSE_W, matrix), rows * K).view(rows, K)
+    mag = uniform_range(stream_key(wl.seed, T_DENSE_ROW_SCALE, matrix), rows, 0.001, 0.05)
+    return z * mag.view(rows, 1)
 
 
 def _matrix_keys(shared: bool) -> Sequence[Tuple[str, int, int, bool]]:

@@ -21,7 +21,7 @@ def lib():
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -71,6 +71,16 @@ def test_lookahead_validation(lib):
     assert lib.moe_topk_hits(ctypes.byref(cfg), FAKE, FAKE, None, FAKE, 4, FAKE, None) == moe.MOE_ERR_ARG
     assert lib.moe_topk_hits(ctypes.byref(_cfg(top_k=9)), FAKE, FAKE, FAKE, FAKE, 4, FAKE, None) \
         == moe.MOE_ERR_SHAPE
+
+
+def test_quantize_validation(lib):
+    q = lib.moe_quantize_int4_gs64
+    assert q(FAKE, -1, 64, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE
+    assert q(FAKE, 4, 100, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE
+    assert q(FAKE, 4, 0, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE
+    assert q(None, 4, 64, FAKE, FAKE, None) == moe.MOE_ERR_ARG
+    assert q(FAKE, 4, 64, FAKE + 8, FAKE, None) == moe.MOE_ERR_ALIGN
+    assert q(FAKE, 0, 64, None, None, None) == moe.MOE_OK   # nothing to do
 
 
 FAKE = 1 << 20   # aligned, never dereferenced: validation fails before any use

@@ -419,3 +419,63 @@ def test_topk_hits(moe):
         moe.moe_topk_hits(mcfg, torch.from_numpy(ip).cuda(), torch.from_numpy(kp).cuda(),
                           torch.from_numpy(it).cuda(), torch.from_numpy(kt).cuda(), hits)
         assert np.array_equal(hits.cpu().numpy(), oracle.topk_hits(ip, kp, it, kt))
+
+
+# ----------------------------------------------------------------------------------------------
+# Offline fp32 -> int4-gs64 weight quantiser ("colibri 开发演进实录" §2.1): codes and scales are
+# single-rounded fp32 operations on both sides, so they must agree bit for bit.
+# ----------------------------------------------------------------------------------------------
+
+def _quantize_gpu(moe, w):
+    rows, K = w.shape
+    packed = torch.full((rows, K // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    scales = torch.full((rows, K // 64), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_int4_gs64(w.cuda(), packed, scales)
+    torch.cuda.synchronize()
+    return packed.cpu().numpy(), scales.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,K", [(1, 64), (37, 320), (2048, 6144)])
+def test_quantize_int4_exact(moe, rows, K):
+    wl = synth.WORKLOADS["glm_decode"]
+    w = synth.gen_dense_weights(wl, rows, K, matrix=rows)
+    if rows > 1:
+        w[1, 64:128] = 0.0                                     # an empty group
+        w[2, :64] = torch.arange(64, dtype=torch.float32) - 31.5   # half-way products: ties
+        w[3, :64] = -w[3, :64].abs()                          # one-signed group
+    packed, scales = _quantize_gpu(moe, w)
+    ref_p, ref_s = oracle.quantize_int4(w)
+    assert np.array_equal(scales.view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(packed, ref_p)
+
+
+def test_quantize_int4_feeds_the_layer(moe):
+    # weights quantised on the GPU run through the layer exactly like the oracle's own codes
+    from dataclasses import replace
+    wl = synth.WORKLOADS["tiny"]
+    H, F, E = wl.hidden, wl.d_ff, wl.n_experts
+    def quantised(shared):
+        d = {}
+        n = 1 if shared else E
+        for m, (name, rows, K) in enumerate((("gate", F, H), ("up", F, H), ("down", H, F))):
+            w = synth.gen_dense_weights(wl, n * rows, K, matrix=100 * shared + m)
+            p, s = _quantize_gpu(moe, w)
+            rp, rs = oracle.quantize_int4(w)
+            assert np.array_equal(p, rp) and np.array_equal(s.view(np.uint32), rs.view(np.uint32))
+            d["w_" + name] = torch.from_numpy(p.reshape(n, rows, K // 2))
+            d["s_" + name] = torch.from_numpy(s.reshape(n, rows, K // 64))
+        return d
+    routed, shared = quantised(0), quantised(1)
+    T = 16
+    x, wr, bias = _inputs(wl, T)
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    y = torch.empty(T, H, device="cuda")
+    moe.moe_layer_forward(cfg, x.cuda(), wr.cuda(), bias.cuda(),
+                          {k: v.cuda() for k, v in routed.items()},
+                          {k: v.cuda() for k, v in shared.items()}, y, ws)
+    torch.cuda.synchronize()
+    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias, routed, shared)
+    yg = y.cpu().numpy()
+    assert np.isfinite(yg).all()
+    tokens_within(yg, ref["y"], TOL)
