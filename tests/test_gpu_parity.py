@@ -157,11 +157,11 @@ def test_permute_skewed_and_invalid(moe):
     assert int(dev["o"][-1]) == P - 1
 
 
-def _ffn_both(moe, wl, T, batch=0, probes=True):
-    """GPU moe_expert_ffn on the oracle's routing vs the oracle, with probes."""
+def _ffn_both(moe, wl, T, batch=0, probes=True, routing=None):
+    """GPU moe_expert_ffn on the oracle's routing (or a given (ids, keff)) vs the oracle."""
     x, wr, bias = _inputs(wl, T, batch)
     cfg_r = oracle.config_of(wl)
-    r = oracle.route(cfg_r, x, wr, bias)
+    r = oracle.route(cfg_r, x, wr, bias) if routing is None else {"ids": routing[0], "keff": routing[1]}
     perm = oracle.permute(cfg_r, r["ids"], r["keff"])
     P, E, H, F = int(perm["offsets"][-1]), wl.n_experts, wl.hidden, wl.d_ff
     R_dev = device_experts(wl)
@@ -189,10 +189,42 @@ def _ffn_both(moe, wl, T, batch=0, probes=True):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 3), ("a3b_decode", 64),
-                                    ("a3b_decode", 96), ("a3b_decode", 200)])
+                                    ("a3b_decode", 65), ("a3b_decode", 96), ("a3b_decode", 200)])
 def test_expert_ffn_exact_accumulators(moe, name, T):
     wl = synth.WORKLOADS[name]
     g, ref, perm = _ffn_both(moe, wl, T)
+    _check_ffn(g, ref)
+
+
+def test_expert_ffn_tensor_tile_edges(moe):
+    """Tensor-core path (a3b shape, T = 300) on a constructed routing: experts with 129 tokens
+    (a full 128-token tile plus a one-token tile), exactly 128, 127, 1 and 0 tokens."""
+    wl = synth.WORKLOADS["a3b_decode"]
+    T, K, E = 300, wl.top_k, wl.n_experts
+    ids = np.full((T, K), -1, np.int32)
+    keff = np.full(T, K, np.int32)
+    for t in range(T):
+        row = [8 + (t * 7 + 3 * i) % (E - 8) for i in range(K)]
+        ids[t] = row
+    ids[:129, 0] = 0          # expert 0: tokens 0..128
+    ids[:128, 1] = 1          # expert 1: tokens 0..127
+    ids[150:277, 0] = 2       # expert 2: 127 tokens
+    ids[299, 1] = 3           # expert 3: one token; expert 4..7: none
+    for t in range(T):        # keep every row's ids distinct after the overrides
+        seen = set()
+        for i in range(K):
+            while ids[t, i] in seen:
+                ids[t, i] = 8 + (ids[t, i] - 8 + 1) % (E - 8)
+            seen.add(int(ids[t, i]))
+    keff[::17] = 5            # some shorter kept sets
+    ids[::17, 5:] = -1
+    g, ref, perm = _ffn_both(moe, wl, T, routing=(ids, keff))
+    cnt = np.diff(perm["offsets"])
+    assert cnt[0] == 129 and cnt[1] == 128 and cnt[2] >= 127 and cnt[3] >= 1 and (cnt[4:8] == 0).all()
+    _check_ffn(g, ref)
+
+
+def _check_ffn(g, ref):
     assert np.array_equal(g["acc_gate"], ref["acc_gate"])
     assert np.array_equal(g["acc_up"], ref["acc_up"])
     # h is fp32 on both sides but summed in a different order: a code may move by one step
@@ -479,3 +511,21 @@ def test_quantize_int4_feeds_the_layer(moe):
     yg = y.cpu().numpy()
     assert np.isfinite(yg).all()
     tokens_within(yg, ref["y"], TOL)
+
+
+def test_layer_forward_tensor_path_wider_shared_expert(moe):
+    """Tensor-core path with the shared expert wider than the routed ones (d_ff_shared 1024,
+    d_ff 512): the shared slot's tiles reduce over 1024 inputs in the down projection."""
+    from dataclasses import replace
+    wl = replace(synth.WORKLOADS["a3b_decode"], name="a3b_wide_shared", d_ff_shared=1024)
+    T = 100
+    assert moe.moe_ffn_uses_tensor_cores(moe_cfg(wl), T) == 1
+    x, wr, bias = _inputs(wl, T)
+    y, rt = _layer_gpu(moe, wl, x, wr, bias)
+    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
+                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
+    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
+    clear = routing_margins(logits, bias.numpy(), wl.top_k, wl.top_p) > TIE
+    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
+    assert np.isfinite(y).all()
+    tokens_within(y[clear], ref["y"][clear], TOL)
