@@ -15,8 +15,10 @@ namespace moe {
 namespace {
 
 constexpr int kCThreads = 256;
-constexpr int kMaxPlanes = kMaxCombinePlanes;
 
+// MAXK pairs and MAXP slice planes at most (the loads are held in registers, so the bounds
+// set the register count: the launcher takes the smallest instantiation that covers the call)
+template <int MAXK, int MAXP>
 __global__ void __launch_bounds__(kCThreads) combine_kernel(
     const float *__restrict__ y_routed, int64_t rstride, const float *__restrict__ y_shared,
     const int32_t *__restrict__ ids, const int32_t *__restrict__ keff,
@@ -53,29 +55,29 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     const int c = (blockIdx.x * kCThreads + threadIdx.x) * 4;
     if (c >= H) return;
     // every pair's (and the shared expert's) planes are loaded before the ordered sums
-    float4 v[kMaxTopK][kMaxPlanes];
+    float4 v[MAXK][MAXP];
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) {
+    for (int i = 0; i < MAXK; ++i) {
 #pragma unroll
-        for (int s = 0; s < kMaxPlanes; ++s) {
+        for (int s = 0; s < MAXP; ++s) {
             v[i][s] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (i < k && s < S_r && s_pair[i] >= 0)
                 v[i][s] = *reinterpret_cast<const float4 *>(y_routed + (size_t)s_pair[i] * rstride + c + s * plane);
         }
     }
-    float4 sv[kMaxPlanes];
+    float4 sv[MAXP];
 #pragma unroll
-    for (int s = 0; s < kMaxPlanes; ++s) {
+    for (int s = 0; s < MAXP; ++s) {
         sv[s] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (y_shared && s < S_s) sv[s] = *reinterpret_cast<const float4 *>(y_shared + (size_t)t * H + c + s * plane);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) {
+    for (int i = 0; i < MAXK; ++i) {
         if (i >= k || s_pair[i] < 0) continue;
         float4 e = v[i][0];
 #pragma unroll
-        for (int s = 1; s < kMaxPlanes; ++s) {
+        for (int s = 1; s < MAXP; ++s) {
             if (s < S_r) {
                 e.x += v[i][s].x; e.y += v[i][s].y; e.z += v[i][s].z; e.w += v[i][s].w;
             }
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     if (y_shared) {
         float4 e = sv[0];
 #pragma unroll
-        for (int s = 1; s < kMaxPlanes; ++s) {
+        for (int s = 1; s < MAXP; ++s) {
             if (s < S_s) {
                 e.x += sv[s].x; e.y += sv[s].y; e.z += sv[s].z; e.w += sv[s].w;
             }
@@ -109,9 +111,16 @@ cudaError_t launch_combine(const moe_config &c, const float *y_routed, int64_t r
 {
     if (T <= 0) return cudaSuccess;
     dim3 grid((c.hidden / 4 + kCThreads - 1) / kCThreads, T);
-    return launch_kernel(combine_kernel, grid, dim3(kCThreads), 0, st, 1, y_routed,
-                         (int64_t)routed_row_stride, y_shared, ids, keff, w, offsets, tok, pair_of, c.top_k,
-                         c.n_experts, c.hidden, S_r, S_s, plane, y);
+    static_assert(kMaxCombinePlanes == 2 && kMaxTopK == 16, "combine instantiations");
+    const bool k8 = c.top_k <= 8;
+    const bool p1 = S_r <= 1 && (y_shared == nullptr || S_s <= 1);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, grid, dim3(kCThreads), 0, st, 1, y_routed,
+                             (int64_t)routed_row_stride, y_shared, ids, keff, w, offsets, tok,
+                             pair_of, c.top_k, c.n_experts, c.hidden, S_r, S_s, plane, y);
+    };
+    if (k8) return p1 ? go(combine_kernel<8, 1>) : go(combine_kernel<8, 2>);
+    return p1 ? go(combine_kernel<16, 1>) : go(combine_kernel<16, 2>);
 }
 
 }  // namespace moe

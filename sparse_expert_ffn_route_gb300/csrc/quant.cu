@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kQThreads) quant_rows_kernel(const float *__re
 // Sliced gate/up rows: h = SiLU(gate) * up of the row, gate and up each the sum of the S
 // slice planes in slice order, formed in registers -- run r (8 consecutive values) by thread
 // r % 256 -- and quantised from there like quant_row_block does.
+template <int MAXS>
 __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *__restrict__ up,
                                      int S, int64_t plane, int n, int8_t *__restrict__ q,
                                      int32_t *__restrict__ csum, float *__restrict__ scale,
@@ -110,9 +111,9 @@ __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *
 #pragma unroll
         for (int i = 0; i < 8; ++i) h[k][i] = 0.0f;
         if (run >= runs) continue;
-        float4 g[kMaxSlices][2], u[kMaxSlices][2];
+        float4 g[MAXS][2], u[MAXS][2];
 #pragma unroll
-        for (int s = 0; s < kMaxSlices; ++s) {   // every plane's loads first
+        for (int s = 0; s < MAXS; ++s) {   // every plane's loads first
             if (s < S) {
                 const float4 *gs = reinterpret_cast<const float4 *>(gp + s * plane + run * 8);
                 const float4 *us = reinterpret_cast<const float4 *>(up + s * plane + run * 8);
@@ -123,7 +124,7 @@ __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *
         float gv[8] = {g[0][0].x, g[0][0].y, g[0][0].z, g[0][0].w, g[0][1].x, g[0][1].y, g[0][1].z, g[0][1].w};
         float uv[8] = {u[0][0].x, u[0][0].y, u[0][0].z, u[0][0].w, u[0][1].x, u[0][1].y, u[0][1].z, u[0][1].w};
 #pragma unroll
-        for (int s = 1; s < kMaxSlices; ++s) {
+        for (int s = 1; s < MAXS; ++s) {
             if (s < S) {
                 const float ga[8] = {g[s][0].x, g[s][0].y, g[s][0].z, g[s][0].w, g[s][1].x, g[s][1].y, g[s][1].z, g[s][1].w};
                 const float ua[8] = {u[s][0].x, u[s][0].y, u[s][0].z, u[s][0].w, u[s][1].x, u[s][1].y, u[s][1].z, u[s][1].w};
@@ -177,6 +178,8 @@ __device__ void quant_h_planes_block(const float *__restrict__ gp, const float *
 // as many as *rest_count (device value; null = none), of n_rest values.  With `planes` the
 // gate/up kernel left gate and up in planes (S per-slice planes of sliced rows, or one plane
 // each from the tensor-core path) and h is formed from them (quant_h_planes_block).
+// MAXS: slice planes at most (held in registers; 1 for the tensor path and unsliced rows)
+template <int MAXS>
 __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restrict__ h, int ld,
                                                             int first, int n_first, int n_rest,
                                                             const int32_t *rest_count,
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kQThreads) quant_h_kernel(const float *__restr
     float *canon_scale = (routed && probe_hs) ? probe_hs + pr : nullptr;
     __nv_bfloat16 *qb = dst.bf16 ? dst.bf16 + (size_t)row * dst.q_ld : nullptr;
     if (planes)
-        quant_h_planes_block(gpart + (size_t)row * ld, upart + (size_t)row * ld, S, plane, n,
+        quant_h_planes_block<MAXS>(gpart + (size_t)row * ld, upart + (size_t)row * ld, S, plane, n,
                              dst.q + (size_t)row * dst.q_ld, dst.csum + (size_t)row * dst.c_ld,
                              dst.scale + row, canon, canon_scale, qb);
     else
@@ -269,11 +272,14 @@ cudaError_t launch_quant_h(const FfnArgs &a, int first_rows, int n_first, int n_
     // gate/up left per-slice planes (sliced rows) or one plane per matrix (tensor path)
     const int S = a.tensor ? 1 : (a.slice_gu ? a.geo_gu[0].S : 1);
     const int planes = (a.tensor || S > 1) ? 1 : 0;
-    return launch_kernel(quant_h_kernel, dim3(max_rows), dim3(kQThreads), 0, st, 1,
-                         (const float *)a.h, a.hstride, first_rows, n_first, n_rest, rest,
-                         a.routed_rowbase, a.hq, a.probe.hq, a.probe.h_scale,
-                         (const float *)a.gpart, (const float *)a.upart, planes, S,
-                         (int64_t)a.plane_rows * a.hstride);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, dim3(max_rows), dim3(kQThreads), 0, st, 1,
+                             (const float *)a.h, a.hstride, first_rows, n_first, n_rest, rest,
+                             a.routed_rowbase, a.hq, a.probe.hq, a.probe.h_scale,
+                             (const float *)a.gpart, (const float *)a.upart, planes, S,
+                             (int64_t)a.plane_rows * a.hstride);
+    };
+    return S <= 1 ? go(quant_h_kernel<1>) : go(quant_h_kernel<kMaxSlices>);
 }
 
 }  // namespace moe
