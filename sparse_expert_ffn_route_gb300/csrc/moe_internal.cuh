@@ -24,6 +24,10 @@ constexpr int kRouteClusterMaxT = 64;
 // this many 1024-input slices
 constexpr int kMaxCombinePlanes = 2;
 
+// The router's partial logits ([splits][T][E] floats) stay within this many floats whenever
+// one split fits: the bound of the fixed scratch array behind moe_route_noalloc (8 MiB).
+constexpr size_t kRouteScratchFloats = size_t(2) << 20;
+
 // device-side error word bits (workspace `err`)
 constexpr int kErrBadExpertId = 1;
 constexpr int kErrBadKeff = 2;

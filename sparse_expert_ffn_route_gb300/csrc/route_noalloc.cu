@@ -18,7 +18,6 @@ namespace {
 
 // 2,097,152 floats = 8 MiB of router scratch; every GPU that loads libmoe.so holds it
 // until the process exits.
-constexpr size_t kRouteScratchFloats = size_t(2) << 20;
 static __device__ __align__(256) float g_route_scratch[kRouteScratchFloats];
 
 std::mutex g_setup_mu;

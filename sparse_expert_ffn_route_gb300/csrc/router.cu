@@ -13,8 +13,8 @@
 //                          ranks' partial |x| maxima meet the same way.
 //   route_tail_kernel      (permute.cu) selection, batch-union and FFN plan in one CTA.
 // Larger batches:
-//   router_logits_kernel   fp32 x . W_router^T, tiled 64 tokens x 64 experts, split along H
-//                          so that the grid covers the GPU; partial sums to [S][T][E].
+//   router_logits_kernel   fp32 x . W_router^T, tiled 128 tokens x 64 experts, split along
+//                          H so that the grid covers the GPU; partial sums to [S][T][E].
 //   router_select_kernel   one warp per token: sums the S partials in a fixed order, then
 //                          selects (router_select.cuh).
 #include <float.h>
@@ -30,63 +30,90 @@ namespace moe {
 
 namespace {
 
-constexpr int kBT = 64;   // tokens per tile
+constexpr int kBT = 128;  // tokens per tile
 constexpr int kBE = 64;   // experts per tile
-constexpr int kBK = 32;   // floats of H per stage
+constexpr int kBK = 16;   // floats of H per stage
 constexpr int kTargetCtas = 2 * 152;
 
-__global__ void __launch_bounds__(256) router_logits_kernel(const float *__restrict__ x,
-                                                            const float *__restrict__ wr, int T,
-                                                            int H, int E, int S,
-                                                            float *__restrict__ part)
+// fp32 x . W_router^T on one 128-token x 64-expert tile over the H range of split s.  Each
+// thread sums 8 x 4 outputs: tokens {4ty .. 4ty+3, 64+4ty .. 64+4ty+3} x experts 4tx ..
+// 4tx+3, so a warp's shared-memory reads are 16-byte lanes at a 16-byte stride.  The next
+// stage's x and W are loaded into registers while the current one is multiplied, then
+// stored into the other shared-memory buffer.  Two CTAs fit an SM.
+__global__ void __launch_bounds__(256, 2) router_logits_kernel(const float *__restrict__ x,
+                                                               const float *__restrict__ wr, int T,
+                                                               int H, int E, int S,
+                                                               float *__restrict__ part)
 {
-    __shared__ float xs[kBK][kBT + 4];
-    __shared__ float ws[kBK][kBE + 4];
+    __shared__ __align__(16) float xs[2][kBK][kBT + 4];
+    __shared__ __align__(16) float ws[2][kBK][kBE + 4];
     pdl_wait();
     pdl_launch_dependents();
     const int t0 = blockIdx.x * kBT, e0 = blockIdx.y * kBE, s = blockIdx.z;
     const int nch = H / kBK;
     const int c0 = (int)((long long)s * nch / S), c1 = (int)((long long)(s + 1) * nch / S);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    float acc[4][4];
+    float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
 
-    for (int c = c0; c < c1; ++c) {
+    // stage loads: 128 rows x 16 floats of x (two float4 per thread), 64 rows of W (one)
+    float4 xv[2], wv;
+    auto load = [&](int c) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int idx = tid + 256 * i, r = idx >> 3, c4 = idx & 7;
-            const int t = t0 + r, e = e0 + r;
-            float4 xv = make_float4(0.f, 0.f, 0.f, 0.f), wv = xv;
-            if (t < T) xv = *reinterpret_cast<const float4 *>(x + (size_t)t * H + c * kBK + c4 * 4);
-            if (e < E) {
-                const uint4 u = ld_stream_v4(wr + (size_t)e * H + c * kBK + c4 * 4);
-                wv = make_float4(__uint_as_float(u.x), __uint_as_float(u.y),
-                                 __uint_as_float(u.z), __uint_as_float(u.w));
-            }
-            xs[c4 * 4 + 0][r] = xv.x; xs[c4 * 4 + 1][r] = xv.y;
-            xs[c4 * 4 + 2][r] = xv.z; xs[c4 * 4 + 3][r] = xv.w;
-            ws[c4 * 4 + 0][r] = wv.x; ws[c4 * 4 + 1][r] = wv.y;
-            ws[c4 * 4 + 2][r] = wv.z; ws[c4 * 4 + 3][r] = wv.w;
+            const int idx = tid + 256 * i, r = idx >> 2, c4 = idx & 3;
+            const int t = t0 + r;
+            xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < T) xv[i] = *reinterpret_cast<const float4 *>(x + (size_t)t * H + c * kBK + c4 * 4);
         }
-        __syncthreads();
-#pragma unroll 8
-        for (int k = 0; k < kBK; ++k) {
-            const float4 a = *reinterpret_cast<const float4 *>(&xs[k][ty * 4]);
-            const float4 b = *reinterpret_cast<const float4 *>(&ws[k][tx * 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+        const int r = tid >> 2, c4 = tid & 3, e = e0 + r;
+        wv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < E) {
+            const uint4 u = ld_stream_v4(wr + (size_t)e * H + c * kBK + c4 * 4);
+            wv = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                             __uint_as_float(u.w));
+        }
+    };
+    auto store = [&](int b) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + 256 * i, r = idx >> 2, c4 = idx & 3;
+            xs[b][c4 * 4 + 0][r] = xv[i].x; xs[b][c4 * 4 + 1][r] = xv[i].y;
+            xs[b][c4 * 4 + 2][r] = xv[i].z; xs[b][c4 * 4 + 3][r] = xv[i].w;
+        }
+        const int r = tid >> 2, c4 = tid & 3;
+        ws[b][c4 * 4 + 0][r] = wv.x; ws[b][c4 * 4 + 1][r] = wv.y;
+        ws[b][c4 * 4 + 2][r] = wv.z; ws[b][c4 * 4 + 3][r] = wv.w;
+    };
+    if (c0 < c1) {
+        load(c0);
+        store(0);
+    }
+    __syncthreads();
+    for (int c = c0; c < c1; ++c) {
+        const int b = (c - c0) & 1;
+        if (c + 1 < c1) load(c + 1);
+#pragma unroll
+        for (int k = 0; k < kBK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&xs[b][k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&xs[b][k][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&ws[b][k][tx * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[4] = {b0.x, b0.y, b0.z, b0.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
+        if (c + 1 < c1) store(b ^ 1);
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
         if (t >= T) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -272,8 +299,11 @@ int router_splits(const moe_config &c, int T)
     const int nch = c.hidden / kBK;
     const long long base = (long long)((T + kBT - 1) / kBT) * ((c.n_experts + kBE - 1) / kBE);
     long long s = (kTargetCtas + base - 1) / (base > 0 ? base : 1);
-    if (s < 1) s = 1;
     if (s > nch) s = nch;
+    // partial logits within kRouteScratchFloats whenever one split fits
+    const long long cap = (long long)kRouteScratchFloats / ((long long)(T > 0 ? T : 1) * c.n_experts);
+    if (s > cap) s = cap;
+    if (s < 1) s = 1;
     return (int)s;
 }
 
