@@ -60,6 +60,19 @@ __device__ void select_token(const SelectParams &p, LogitFn logit, int t,
     const int lane = threadIdx.x & 31;
     const int E = p.E, K = p.K;
 
+    // every logit and bias of this lane is loaded before any of them is used, so the loads
+    // overlap instead of queueing behind each other's arithmetic
+    float lv[kPerLane], bv[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int e = lane + 32 * j;
+        lv[j] = 0.0f;
+        bv[j] = 0.0f;
+        if (e < E) {
+            lv[j] = logit(e);
+            bv[j] = p.bias[e];
+        }
+    }
     float sig[kPerLane];
     uint32_t key[kPerLane];
 #pragma unroll
@@ -68,9 +81,8 @@ __device__ void select_token(const SelectParams &p, LogitFn logit, int t,
         sig[j] = 0.0f;
         key[j] = 0u;
         if (e < E) {
-            const float l = logit(e);
-            sig[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-            key[j] = order_key(__fadd_rn(sig[j], p.bias[e]));
+            sig[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lv[j])));
+            key[j] = order_key(__fadd_rn(sig[j], bv[j]));
         }
     }
 
