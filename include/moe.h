@@ -163,6 +163,15 @@ int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t 
 int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, float *scales,
                            void *stream);
 
+/* Diagnostic of the error path of the kernels' bounded device-side waits:
+ * one CTA polls, `polls` times (1 .. 2^24), an mbarrier that nothing arrives
+ * at, gives up and records the timeout in the workspace's error word exactly
+ * as the tcgen05 pipeline's waits do.  Nothing faults or hangs; the next
+ * moe_check_errors on the workspace returns MOE_ERR_TIMEOUT and clears the
+ * word.  workspace: any workspace of the library (>= 256 bytes, 256-byte
+ * aligned).  Asynchronous on stream. */
+int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls, void *stream);
+
 /* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
  * device work): 1 = the tcgen05 tensor-core grouped GEMM (batches beyond the
  * decode route, T > 64, with hidden, d_ff and d_ff_shared multiples of 512),

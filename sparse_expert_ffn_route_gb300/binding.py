@@ -34,7 +34,7 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
-           "moe_topk_hits", "moe_quantize_int4_gs64")
+           "moe_topk_hits", "moe_quantize_int4_gs64", "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -98,6 +98,7 @@ def load_library():
     L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
     L.moe_quantize_int4_gs64.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.moe_selftest_wait_timeout.argtypes = [vp, sz, i32, vp]
     L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -182,6 +183,13 @@ def moe_quantize_int4_gs64(w, packed, scales, stream=None):
     rows = w.numel() // K if K else 0
     _check(load_library().moe_quantize_int4_gs64(_ptr(w), rows, K, _ptr(packed), _ptr(scales),
                                                   _stream(stream)), "moe_quantize_int4_gs64")
+
+
+def moe_selftest_wait_timeout(workspace, polls: int = 4096, stream=None):
+    """Make one bounded device wait run out on purpose; moe_check_errors then reports
+    MOE_ERR_TIMEOUT (the error path of the kernels' waits, with no fault or hang)."""
+    _check(load_library().moe_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(polls),
+                                                     _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def moe_route_noalloc(cfg, x, w_router, bias, ids, w, keff, stream=None):

@@ -454,6 +454,19 @@ int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, flo
     return ok();
 }
 
+int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls, void *stream)
+{
+    if (!workspace) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_ALIGN, "workspace is not 256-byte aligned");
+    if (workspace_bytes < 256) return fail(MOE_ERR_WORKSPACE, "workspace is smaller than 256 bytes");
+    if (polls < 1 || polls > (1 << 24)) return fail(MOE_ERR_ARG, "polls must be in [1, 2^24] (got %d)", polls);
+    int rc;
+    if ((rc = check_device())) return rc;
+    const cudaError_t e = launch_selftest_wait(static_cast<int32_t *>(workspace), polls, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return ok();
+}
+
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
 {
     if (check_config(cfg) != MOE_OK || T < 0) return -1;
@@ -619,6 +632,7 @@ int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream)
     if (e != cudaSuccess) return cuda_fail(e, "error check");
     if (flag & kErrBadExpertId) return fail(MOE_ERR_DEVICE, "an expert id outside [0, n_experts) was skipped");
     if (flag & kErrBadKeff) return fail(MOE_ERR_DEVICE, "a keff outside [0, top_k] was clamped");
+    if (flag & kErrTimeout) return fail(MOE_ERR_TIMEOUT, "a bounded device-side wait gave up; the kernel stopped early and its outputs are incomplete");
     if (flag) return fail(MOE_ERR_DEVICE, "device error word 0x%x", flag);
     return ok();
 }

@@ -183,6 +183,9 @@ cudaError_t launch_topk_hits(const int32_t *ids_pred, const int32_t *keff_pred,
 cudaError_t launch_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales,
                                  cudaStream_t st);
 
+// diagnostic: one bounded wait on an mbarrier nothing arrives at (selftest.cu)
+cudaError_t launch_selftest_wait(int32_t *err, int polls, cudaStream_t st);
+
 // host helpers shared with the entry points outside moe_api.cu
 int set_error(int code, const char *fmt, ...);   // records the thread's last error message
 int require_device();                            // MOE_OK on a compute capability 10.3 device

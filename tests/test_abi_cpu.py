@@ -73,6 +73,15 @@ def test_lookahead_validation(lib):
         == moe.MOE_ERR_SHAPE
 
 
+def test_selftest_validation(lib):
+    st = lib.moe_selftest_wait_timeout
+    assert st(None, 1 << 20, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert st(FAKE + 16, 1 << 20, 16, None) == moe.MOE_ERR_ALIGN
+    assert st(FAKE, 128, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert st(FAKE, 1 << 20, 0, None) == moe.MOE_ERR_ARG
+    assert st(FAKE, 1 << 20, (1 << 24) + 1, None) == moe.MOE_ERR_ARG
+
+
 def test_quantize_validation(lib):
     q = lib.moe_quantize_int4_gs64
     assert q(FAKE, -1, 64, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE

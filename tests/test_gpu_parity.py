@@ -529,3 +529,24 @@ def test_layer_forward_tensor_path_wider_shared_expert(moe):
     assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
     assert np.isfinite(y).all()
     tokens_within(y[clear], ref["y"][clear], TOL)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(moe):
+    """A device wait that runs out (a flag nothing sets) ends the kernel with an error status
+    that moe_check_errors returns as MOE_ERR_TIMEOUT; the context stays usable."""
+    wl = synth.WORKLOADS["tiny"]
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, 16)
+    moe.moe_check_errors(ws)                      # clean to begin with
+    moe.moe_selftest_wait_timeout(ws, polls=4096)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_check_errors(ws)
+    assert ei.value.code == moe.MOE_ERR_TIMEOUT
+    moe.moe_check_errors(ws)                      # the record is cleared
+    # the same context still runs a layer correctly
+    x, wr, bias = _inputs(wl, 16)
+    y, rt = _layer_gpu(moe, wl, x, wr, bias)
+    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
+                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
+    assert np.array_equal(rt["ids"], ref["ids"])
+    tokens_within(y, ref["y"], TOL)
