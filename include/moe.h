@@ -173,9 +173,12 @@ int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, flo
 int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls, void *stream);
 
 /* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
- * device work): 1 = the tcgen05 tensor-core grouped GEMM (batches beyond the
- * decode route, T > 64, with hidden, d_ff and d_ff_shared multiples of 512),
- * 0 = the GEMV-shaped kernels.  Returns -1 for an invalid config or T < 0.
+ * device work): 1 = the tcgen05 tensor-core grouped GEMM, 0 = the GEMV-shaped
+ * kernels.  The tensor path takes batches beyond the decode route (T > 64)
+ * whose matrices have hidden, d_ff and d_ff_shared in multiples of 512, when
+ * the expected tokens per routed expert T*K/U (U = E*(1-(1-K/E)^T), the
+ * distinct experts of uniform routing) is at least 5, or at once when hidden
+ * or d_ff is under 1024.  Returns -1 for an invalid config or T < 0.
  * ["MoE 路由与专家流式加载" §1.3: the expert FFN turns from a weight-streaming
  * GEMV into a dense contraction once tokens per expert grow.] */
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);

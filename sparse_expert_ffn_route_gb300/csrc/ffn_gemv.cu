@@ -65,12 +65,26 @@ int pick_tc(int nc, int T, int K, int E, bool shared)
 
 }  // namespace
 
+bool ffn_use_tensor_cores(const FfnArgs &a)
+{
+    if (a.T <= kRouteClusterMaxT || !ffn_tc_supported(a)) return false;
+    // Measured on GB300: a tensor-core tile pays about the same per 64-input group whatever its
+    // width, while the GEMV kernels stream an expert's weights once per 4 of its tokens.  On
+    // wide matrices the GEMV kernels are faster below about 5 tokens per routed expert (GLM
+    // T=128: 2.40 vs 2.76 ms; wide layer T=128: 3.05 vs 3.87 ms) and slower above (GLM T=256:
+    // 4.80 vs 3.11 ms).  On narrow ones (hidden or d_ff under 1024) their tasks are too short
+    // and the tensor path wins from the first batch past the decode route.
+    if (a.H < 1024 || a.F < 1024) return true;
+    const double U = a.E * (1.0 - pow(1.0 - (double)a.K / a.E, (double)a.T));
+    return U > 0.0 && (double)a.T * a.K / U >= 5.0;
+}
+
 void ffn_configure(FfnArgs &a)
 {
     const bool sh = a.n_shared != 0;
     const bool small = a.T <= kRouteClusterMaxT;
     // batches beyond the decode route: the tensor-core grouped GEMM (ffn_tc.cu)
-    a.tensor = (!small && ffn_tc_supported(a)) ? 1 : 0;
+    a.tensor = (!small && ffn_use_tensor_cores(a)) ? 1 : 0;
     if (a.tensor) {
         a.slice_gu = 0;
         a.slice_dn = 0;

@@ -476,7 +476,10 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
     a.F = cfg->d_ff;
     a.n_shared = cfg->n_shared;
     a.Fs = cfg->n_shared ? cfg->d_ff_shared : cfg->d_ff;
-    return (T > kRouteClusterMaxT && ffn_tc_supported(a)) ? 1 : 0;
+    a.E = cfg->n_experts;
+    a.K = cfg->top_k;
+    a.T = T;
+    return ffn_use_tensor_cores(a) ? 1 : 0;
 }
 
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,

@@ -160,6 +160,9 @@ void ffn_configure(FfnArgs &a);
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st);
 // tensor-core path (ffn_tc.cu): whole 128-row tiles of every matrix of the call
 bool ffn_tc_supported(const FfnArgs &a);
+// the tcgen05 path takes an FFN call when its batch is beyond the decode route, its matrices
+// are supported, and it has enough tokens per routed expert (ffn_gemv.cu)
+bool ffn_use_tensor_cores(const FfnArgs &a);
 cudaError_t launch_ffn_tc(bool gate_up, const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 // pair_of (nullable) gives each (t, i) its list position directly; without it the position

@@ -284,6 +284,7 @@ def test_layer_forward(moe, name, T):
 
 
 @pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 32, [0, 13, 31]),
+                                           ("glm_decode", 128, [0, 77, 127]),
                                            ("wide", 64, [0, 40]), ("prefill", 4096, [0, 2047, 4095])])
 def test_layer_forward_full_size_sampled(moe, name, T, sample):
     """Full-size layer through moe_layer_forward (the call the benchmark times); routing of
