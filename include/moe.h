@@ -266,6 +266,19 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
 /* Synchronises `stream`, then returns MOE_ERR_DEVICE if a kernel that used
  * this workspace since the last check found invalid data (see moe_permute),
  * and clears the record; MOE_OK otherwise.  Not for use inside stream capture. */
+/* moe_layer_forward on host buffers: x_host [T][H] and y_host [T][H] fp32 in
+ * host memory (pinned, e.g. cudaHostAlloc, for the copies to run
+ * asynchronously; pageable memory works but the copies then hold the host).
+ * On the stream: x is copied into the workspace, the layer runs there, y is
+ * copied back.  Every other argument, error and flag as moe_layer_forward;
+ * the workspace (moe_workspace_size) holds both device copies.  Returns with
+ * the work enqueued: y_host is complete once the stream has reached it. */
+int moe_layer_forward_host(const moe_config *cfg, const float *x_host, int T,
+                           const float *w_router, const float *bias,
+                           const moe_expert_weights *routed, const moe_expert_weights *shared,
+                           float *y_host, const moe_routing *routing, void *workspace,
+                           size_t workspace_bytes, int flags, void *stream);
+
 int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream);
 
 /* Per-stage device time of the moe_layer_forward calls made on this thread

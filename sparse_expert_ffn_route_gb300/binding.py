@@ -34,7 +34,8 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
-           "moe_topk_hits", "moe_quantize_int4_gs64", "moe_selftest_wait_timeout")
+           "moe_topk_hits", "moe_quantize_int4_gs64", "moe_selftest_wait_timeout",
+           "moe_layer_forward_host")
 
 
 class MoeError(RuntimeError):
@@ -103,6 +104,7 @@ def load_library():
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_combine.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, i32, vp]
+    L.moe_layer_forward_host.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, i32, vp]
     L.moe_check_errors.argtypes = [vp, sz, vp]
     L.moe_stage_times.argtypes = [vp, vp, i32]
     L.moe_route_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp]
@@ -249,6 +251,26 @@ def moe_layer_forward(cfg, x, w_router, bias, routed, shared, y, workspace, rout
                                              ctypes.byref(ro) if ro else None, _ptr(workspace),
                                              workspace.numel(), flags, _stream(stream)),
            "moe_layer_forward")
+
+
+def moe_layer_forward_host(cfg, x_host, w_router, bias, routed, shared, y_host, workspace,
+                           routing=None, flags: int = 0, stream=None):
+    """moe_layer_forward on host tensors x_host / y_host (CPU, pinned for asynchronous
+    copies): the library copies x in, runs the layer and copies y out on the stream."""
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("moe_layer_forward_host takes CPU tensors for x and y")
+    T = x_host.shape[0]
+    rw = ExpertWeights.of(routed)
+    sw = ExpertWeights.of(shared) if shared is not None else None
+    ro = None
+    if routing is not None:
+        ro = Routing(_ptr(routing.get("ids")), _ptr(routing.get("w")), _ptr(routing.get("keff")))
+    _check(load_library().moe_layer_forward_host(ctypes.byref(cfg), _ptr(x_host), T, _ptr(w_router),
+                                                  _ptr(bias), ctypes.byref(rw),
+                                                  ctypes.byref(sw) if sw else None, _ptr(y_host),
+                                                  ctypes.byref(ro) if ro else None, _ptr(workspace),
+                                                  workspace.numel(), flags, _stream(stream)),
+           "moe_layer_forward_host")
 
 
 def moe_check_errors(workspace, stream=None):

@@ -380,6 +380,8 @@ WsLayout ws_layout(const moe_config &c, int T)
     L.hcsum = take(rows * (fm / 32) * 4);
     L.y = take((rows > s_dn * rows_s ? rows : s_dn * rows_s) * H * 4);
     L.xn = take((size_t)T * H * 4);
+    L.xs = take((size_t)T * H * 4);
+    L.ys = take((size_t)T * H * 4);
     L.total = off;
     return L;
 }
@@ -743,6 +745,32 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     }
     if (e != cudaSuccess) return cuda_fail(e, "layer launch");
     if (flags & MOE_FLAG_SYNC_CHECK) return moe_check_errors(workspace, workspace_bytes, stream);
+    return ok();
+}
+
+int moe_layer_forward_host(const moe_config *cfg, const float *x_host, int T,
+                           const float *w_router, const float *bias,
+                           const moe_expert_weights *routed, const moe_expert_weights *shared,
+                           float *y_host, const moe_routing *routing, void *workspace,
+                           size_t workspace_bytes, int flags, void *stream)
+{
+    int rc;
+    if ((rc = check_config(cfg)) || (rc = check_tokens(T))) return rc;
+    if (T == 0) return ok();
+    if (!x_host) return fail(MOE_ERR_ARG, "x_host is NULL");
+    if (!y_host) return fail(MOE_ERR_ARG, "y_host is NULL");
+    WsLayout L;
+    if ((rc = check_ws(*cfg, T, workspace, workspace_bytes, &L)) || (rc = check_device())) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *xd = at<float>(workspace, L.xs), *yd = at<float>(workspace, L.ys);
+    const size_t bytes = (size_t)T * cfg->hidden * sizeof(float);
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of x to the device");
+    if ((rc = moe_layer_forward(cfg, xd, T, w_router, bias, routed, shared, yd, routing, workspace,
+                                workspace_bytes, flags, stream)))
+        return rc;
+    e = cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of y to the host");
     return ok();
 }
 

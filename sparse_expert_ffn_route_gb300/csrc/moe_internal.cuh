@@ -108,6 +108,7 @@ struct WsLayout {
     size_t hp, hp_plane_floats;       // partial gate planes then partial up planes
     size_t xbf, hbf;                  // bf16 codes of x and h (tensor path)
     size_t xn;                        // [T][H] fp32 RMSNorm output (router look-ahead)
+    size_t xs, ys;                    // [T][H] fp32 device copies of host x and y (host call)
     size_t hq, hscale, hcsum;         // quantised h
     size_t y;                         // [rows][H] fp32 (shared rows, then routed pairs)
     size_t plan;                      // FfnPlan

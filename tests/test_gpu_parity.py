@@ -551,3 +551,21 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
                                synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
     assert np.array_equal(rt["ids"], ref["ids"])
     tokens_within(y, ref["y"], TOL)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("glm_decode", 8), ("a3b_decode", 128)])
+def test_layer_forward_host_buffers(moe, name, T):
+    """moe_layer_forward_host (host x in, host y out) gives the device call's output bit for bit."""
+    wl = synth.WORKLOADS[name]
+    x, wr, bias = _inputs(wl, T)
+    cfg = moe_cfg(wl)
+    ws = moe.alloc_workspace(cfg, T)
+    routed = device_experts(wl)
+    shared = device_experts(wl, shared=True) if wl.n_shared else None
+    y_dev = torch.empty(T, wl.hidden, device="cuda")
+    moe.moe_layer_forward(cfg, x.cuda(), wr.cuda(), bias.cuda(), routed, shared, y_dev, ws)
+    x_host = x.pin_memory()
+    y_host = torch.full((T, wl.hidden), float("nan")).pin_memory()
+    moe.moe_layer_forward_host(cfg, x_host, wr.cuda(), bias.cuda(), routed, shared, y_host, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
