@@ -95,6 +95,18 @@ void ffn_configure(FfnArgs &a)
         a.geo_dn[1] = make_tc_geo(a.Fs, a.H, 1);
         return;
     }
+    // the rest: the row GEMV where its shapes allow, else the warp GEMV below
+    a.rows = ffn_rows_supported(a) ? 1 : 0;
+    if (a.rows) {
+        a.slice_gu = 0;
+        a.slice_dn = 0;
+        a.tc_gu = a.tc_dn = kRowTok;
+        a.geo_gu[0] = make_rows_geo(a.H, a.F);
+        a.geo_gu[1] = make_rows_geo(a.H, a.Fs);
+        a.geo_dn[0] = make_rows_geo(a.F, a.H);
+        a.geo_dn[1] = make_rows_geo(a.Fs, a.H);
+        return;
+    }
     const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;
     const bool sgu = small && a.slice_gu && a.H > 32 * kSliceChunks;
     const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks &&
@@ -119,12 +131,14 @@ void ffn_configure(FfnArgs &a)
 cudaError_t launch_ffn_gate_up(const FfnArgs &a, cudaStream_t st)
 {
     if (a.tensor) return launch_ffn_tc(true, a, st);
+    if (a.rows) return launch_ffn_rows(true, a, st);
     return launch(choose(true, max_nc(a.geo_gu, a.n_shared != 0), a.tc_gu, probes_gu(a)), a, st);
 }
 
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st)
 {
     if (a.tensor) return launch_ffn_tc(false, a, st);
+    if (a.rows) return launch_ffn_rows(false, a, st);
     return launch(choose(false, max_nc(a.geo_dn, a.n_shared != 0), a.tc_dn, probes_dn(a)), a, st);
 }
 

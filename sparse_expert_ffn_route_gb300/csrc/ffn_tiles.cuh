@@ -73,6 +73,28 @@ __host__ __device__ inline Geo make_tc_geo(int kdim, int nrows, int matrices)
     return g;
 }
 
+// Geometry of the row-per-lane-group GEMV (ffn_rows.cu): blocks of kRowBlock rows over the
+// whole reduction, every token of a chunk against one pass over the block's weights.
+constexpr int kRowBlock = 64;
+constexpr int kRowTok = 8;    // tokens per task at most
+
+__host__ __device__ inline Geo make_rows_geo(int kdim, int nrows)
+{
+    Geo g;
+    g.kdim = kdim;
+    g.nrows = nrows;
+    g.S = 1;
+    g.sch = kdim / 32;
+    g.lpr = 4;
+    g.rpw = 8;
+    g.nc = 1;
+    g.ru = kRowBlock;
+    g.rb = kRowBlock;
+    g.rowbytes = kdim / 2;
+    g.G = kdim / 64;
+    return g;
+}
+
 // Tasks of a slot: (token chunk of at most tc tokens, slice, row block), in that order of
 // significance.
 __host__ __device__ __forceinline__ int tasks_of(const Geo &g, int ntok, int tc)
@@ -81,18 +103,18 @@ __host__ __device__ __forceinline__ int tasks_of(const Geo &g, int ntok, int tc)
     return ((g.nrows + g.rb - 1) / g.rb) * g.S * ((ntok + tc - 1) / tc);
 }
 
-// Tokens a kernel built for chunks of tc computes for a chunk of nt (its code path) ...
+// Tokens a kernel built for chunks of tc computes for a chunk of nt (its code path: the
+// smallest power of two that holds nt, at most tc) ...
 __host__ __device__ __forceinline__ int chunk_width(int nt, int tc)
 {
-    if (nt <= 1 || tc == 1) return 1;
-    if (nt == 2 || tc == 2) return 2;
-    if (nt <= 4 || tc == 4) return 4;
-    return tc;
+    int w = 1;
+    while (w < nt && w < tc) w *= 2;
+    return w;
 }
 
 // ... and the relative cost of one of its tasks: the per-token work plus about three
-// tokens' worth of per-task work (copies, unpacking, reduction, stores).  Warps take equal
-// shares of the summed cost, not of the task count.
+// tokens' worth of per-task work (copies, unpacking, reduction, stores).  Warps of the warp
+// GEMV take equal shares of the summed cost, not of the task count.
 __host__ __device__ __forceinline__ int task_weight(int nt, int tc) { return chunk_width(nt, tc) + 3; }
 
 __host__ __device__ __forceinline__ long long slot_cost(const Geo &g, int ntok, int tc)

@@ -43,6 +43,9 @@ struct FfnPlan {
     int32_t n_slots;
     int32_t gu_tiles;                 // total gate/up tasks
     int32_t dn_tiles;                 // total down tasks
+    // task counters of the kernels that hand out tasks on demand (ffn_rows.cu): the next
+    // task and the CTAs finished, [0] gate/up, [1] down; zero between launches
+    int32_t next[2], done[2];
     int32_t pad;
     int32_t expert[kMaxSlots];        // expert id, -1 for the shared expert
     int32_t ntok[kMaxSlots];          // tokens routed to the slot
@@ -88,6 +91,7 @@ struct FfnArgs {
     int plane_rows;                   // output rows of the call (shared rows + routed pairs)
     int slice_gu, slice_dn;           // rows cut into 1024-input slices
     int tensor;                       // the tcgen05 path (ffn_tc.cu) runs gate/up and down
+    int rows;                         // the row GEMV (ffn_rows.cu) runs gate/up and down
     __nv_bfloat16 *x_bf16;            // [rows][H] the codes of x per output row as bf16 (tensor path)
     __nv_bfloat16 *h_bf16;            // [rows][hstride] the codes of h as bf16 (tensor path)
     int tc_gu, tc_dn;                 // token chunk per task
@@ -165,6 +169,10 @@ bool ffn_tc_supported(const FfnArgs &a);
 // are supported, and it has enough tokens per routed expert (ffn_gemv.cu)
 bool ffn_use_tensor_cores(const FfnArgs &a);
 cudaError_t launch_ffn_tc(bool gate_up, const FfnArgs &a, cudaStream_t st);
+// row GEMV (ffn_rows.cu): reductions that are multiples of 256 inputs, 16-byte aligned
+// operands; one pass over each 64-row weight block per chunk of up to 16 tokens
+bool ffn_rows_supported(const FfnArgs &a);
+cudaError_t launch_ffn_rows(bool gate_up, const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 // pair_of (nullable) gives each (t, i) its list position directly; without it the position
 // is found by binary search in the expert's token list.  S_r / S_s slice planes (plane

@@ -122,6 +122,8 @@ __device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const i
         plan->dn_cost[nslots] = cbase_dn;
         plan->gu_tiles = base_gu;
         plan->dn_tiles = base_dn;
+        plan->next[0] = plan->next[1] = 0;
+        plan->done[0] = plan->done[1] = 0;
     }
 }
 
