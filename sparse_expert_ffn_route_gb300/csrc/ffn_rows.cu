@@ -7,9 +7,9 @@
 // kRowBlock rows, chunk of at most kRwTok tokens) over the whole reduction (geometry
 // make_rows_geo).  The copy warp takes tasks one at a time from a counter in the plan, so a CTA
 // that drew long tasks (the shared expert's 8-token chunks) takes fewer, and streams each
-// through a ring of stages in shared memory with TMA, 512 inputs per stage: per matrix a
-// [64 rows][2 lines][128 B] box of nibbles (128-byte swizzle) and the [64][8] group scales,
-// plus one [2][256 B] box of int8 codes per token (the row picked by token id for gate/up, by
+// through a ring of stages in shared memory with TMA, 1024 inputs per stage: per matrix a
+// [64 rows][4 lines][128 B] box of nibbles (128-byte swizzle) and the [64][16] group scales,
+// plus one [4][256 B] box of int8 codes per token (the row picked by token id for gate/up, by
 // output row for down).  One TMA instruction per stage issues all of them, a box per lane.
 //
 // Compute warp w owns rows 4w .. 4w+3 of the block; lane l takes row 4w + l/8 and chunk
@@ -46,7 +46,7 @@ constexpr int kRwWarps = 16;                           // compute warps
 constexpr int kRwRowsPerWarp = 4;
 constexpr int kRwThreads = (kRwWarps + 1) * 32;        // + the copy warp
 constexpr int kRwTok = kRowTok;                        // tokens per task at most
-constexpr int kRwLines = 2;                            // 128-byte lines per row and stage
+constexpr int kRwLines = 4;                            // 128-byte lines per row and stage
 constexpr int kRwInputs = kRwLines * 256;              // inputs per stage
 constexpr int kRwWBytes = kRowBlock * kRwLines * 128;  // nibbles of one matrix per stage
 constexpr int kRwSBytes = kRowBlock * kRwLines * 4 * 4;   // its group scales
@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
 
     if (warp == kRwWarps) {
         // ------------------------------- copy warp ------------------------------------
-        // Tasks are taken one at a time from the shared counter.  While task i is issued, the
-        // index of task i+1 (taken one task earlier) is decoded and its code rows are loaded.
+        // Tasks are taken one at a time from the shared counter, two ahead: the counter's
+        // answer (slow while HBM is saturated) has two tasks' time to arrive.  While task i is
+        // issued, task i+1 is decoded and its code rows are loaded.
         // Lane L of the stage's one TMA instruction copies: L < NM nibbles of matrix L;
         // NM <= L < 2 NM scales of matrix L - NM; 2 NM <= L < 2 NM + nt the codes of token
         // L - 2 NM.
@@ -349,33 +350,38 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         };
         int task = lane == 0 ? atomicAdd(next, 1) : 0;
         task = __shfl_sync(0xffffffffu, task, 0);
-        int grabbed = lane == 0 && task < total ? atomicAdd(next, 1) : total;
+        // counter requests in flight (lane 0): the answers for tasks i+1 and, with at least
+        // four tasks per CTA, i+2 (with fewer, the CTAs that start first would take them all)
+        const bool deep = total >= 4 * (int)gridDim.x;
+        int g1 = lane == 0 && task < total ? atomicAdd(next, 1) : total;
+        int g2 = lane == 0 && task < total && deep ? atomicAdd(next, 1) : total;
         Task t{};
         int arow = 0;
         decode(task, t, arow);
-        bool ok = true;
-        while (ok) {
+        // Issues task `task`; g holds the answer of a request made one or two tasks ago and
+        // gets a new request.  The deep loop alternates g1 and g2, so no register waits on a
+        // request made in the same step.  False once the stop stage is issued or on a timeout.
+        auto step = [&](int &g) -> bool {
             if (task >= total) {
                 // no more tasks: a stage without copies tells the compute warps to stop
                 const int slot = (int)(k % D);
-                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err)) break;
+                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err)) return false;
                 if (lane == 0) {
                     sh->hdr[slot].task = -1;
                     mbar_arrive(&sh->full[slot]);
                 }
                 ++k;
-                break;
+                return false;
             }
-            // the next task: its index (taken earlier), a new one taken, its rows loaded
-            const int ntask = __shfl_sync(0xffffffffu, grabbed, 0);
-            if (lane == 0 && ntask < total) grabbed = atomicAdd(next, 1);
+            const int ntask = __shfl_sync(0xffffffffu, g, 0);
+            if (lane == 0 && ntask < total) g = atomicAdd(next, 1);
             Task tn{};
             int narow = 0;
             decode(ntask, tn, narow);
 
-            const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
-            const int nst = (g.kdim + kRwInputs - 1) / kRwInputs;
-            const int wrow = (t.sh ? 0 : t.e * g.nrows) + t.r0;
+            const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+            const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
+            const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
             const uint32_t bytes = NM * (kRwWBytes + kRwSBytes) + t.nt * kRwTokBytes;
             // this lane's box: map, shared-memory offset, coordinates (the line or group
             // coordinate advances with the stage)
@@ -399,10 +405,8 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             }
             for (int s = 0; s < nst; ++s, ++k) {
                 const int slot = (int)(k % D);
-                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err)) {
-                    ok = false;
-                    break;
-                }
+                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
+                    return false;
                 const uint32_t fb = smem_u32(&sh->full[slot]);
                 if (lane == 0) {
                     if (s == 0) {
@@ -424,6 +428,14 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             task = ntask;
             t = tn;
             arow = narow;
+            return true;
+        };
+        if (deep) {
+            while (step(g1) && step(g2)) {
+            }
+        } else {
+            while (step(g1)) {
+            }
         }
         // before the CTA exits, every copy it issued has landed (the compute warps have seen
         // all of them unless the CTA stopped early)
@@ -502,7 +514,7 @@ cudaError_t encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// nibbles of `rows` rows of kdim inputs: {128 B, kdim/256 lines, rows}, boxes {128, 2, 64},
+// nibbles of `rows` rows of kdim inputs: {128 B, kdim/256 lines, rows}, boxes {128, 4, 64},
 // 128-byte swizzle, reads past the end filled with zeros
 cudaError_t nibble_map(CUtensorMap *m, const uint8_t *base, int kdim, long long rows)
 {
@@ -511,7 +523,7 @@ cudaError_t nibble_map(CUtensorMap *m, const uint8_t *base, int kdim, long long 
                      {128, kRwLines, kRowBlock}, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-// group scales [rows][kdim/64] fp32: {groups, rows, 1}, boxes of 8 groups x 64 rows
+// group scales [rows][kdim/64] fp32: {groups, rows, 1}, boxes of 16 groups x 64 rows
 cudaError_t scale_map(CUtensorMap *m, const float *base, int kdim, long long rows)
 {
     const cuuint64_t ld = (cuuint64_t)(kdim / 64) * 4;
@@ -520,7 +532,7 @@ cudaError_t scale_map(CUtensorMap *m, const float *base, int kdim, long long row
                      CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
-// int8 codes [rows][ld], `cols` of them read: {256, cols/256, rows}, boxes {256, 2, 1}
+// int8 codes [rows][ld], `cols` of them read: {256, cols/256, rows}, boxes {256, 4, 1}
 cudaError_t code_map(CUtensorMap *m, const int8_t *base, int cols, int ld, int rows)
 {
     return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base,
