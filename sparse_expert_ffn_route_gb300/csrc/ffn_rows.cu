@@ -70,10 +70,16 @@ static_assert(rw_stage_bytes<true>() % 1024 == 0 && rw_stage_bytes<false>() % 10
 static_assert(rw_stages<false>() >= rw_stages<true>(), "RwShared holds the deeper ring");
 
 // Written by the copy warp into the slot of a task's first stage, before the stage's arrival:
-// the task, decoded.  task -1: no more tasks.
+// the task, decoded, and the code row of each of its tokens.  task -1: no more tasks.
 struct RwHdr {
     int task, e, r0, j0, nt, rowbase, tokbase, pad;
+    int arow[kRwTok];
 };
+
+// The activation scales of the call (x by token, or h by output row), copied into shared
+// memory once per CTA when there are at most this many: a global load issued at a task's start
+// would not return before its end while the ring keeps HBM saturated.
+constexpr int kRwScaleTable = 4096;
 
 struct RwShared {
     uint64_t full[rw_stages<false>()];    // stage landed (TMA transaction bytes)
@@ -93,7 +99,7 @@ template <bool GU>
 constexpr size_t rw_smem_bytes()
 {
     return 1024 /* alignment */ + (size_t)rw_stages<GU>() * rw_stage_bytes<GU>() + sizeof(RwShared) +
-           sizeof(RwPlan);
+           sizeof(RwPlan) + kRwScaleTable * sizeof(float);
 }
 
 // Tensor maps (all 3-D, so that one instruction issues every box of a stage): nibbles and
@@ -182,19 +188,11 @@ __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int 
 template <bool GU, bool PROBE, int N>
 __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const Geo &g, int nst,
                                           const uint8_t *ring, RwShared *sh, uint32_t &k, int rin,
-                                          int c, int lane)
+                                          int c, int lane, const float (&sx)[kRwTok / 8])
 {
     constexpr int NM = rw_nm<GU>();
     constexpr int D = rw_stages<GU>();
     constexpr int SB = rw_stage_bytes<GU>();
-    constexpr int NS = kRwTok / 8;
-    // the activation scales of this lane's tokens (c, c+8), loaded now, used by the epilogue
-    float sx[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-        const int j = c + 8 * i;
-        sx[i] = j < t.nt ? (GU ? a.xq.scale[act_row<GU>(a, t, j)] : a.hq.scale[t.rowbase + j]) : 0.0f;
-    }
     float acc[NM][N];
 #pragma unroll
     for (int m = 0; m < NM; ++m)
@@ -303,6 +301,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     uint8_t *ring = reinterpret_cast<uint8_t *>(((uintptr_t)rw_smem_raw + 1023) & ~(uintptr_t)1023);
     RwShared *sh = reinterpret_cast<RwShared *>(ring + (size_t)D * SB);
     RwPlan *ps = reinterpret_cast<RwPlan *>(sh + 1);
+    float *stab = reinterpret_cast<float *>(ps + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < D; ++i) {
@@ -328,6 +327,11 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         }
     }
     if (threadIdx.x == 0) ps->n_slots = ns;
+    const float *gscale = GU ? a.xq.scale : a.hq.scale;
+    const int nscale = GU ? a.T : a.plane_rows;
+    const bool table = nscale <= kRwScaleTable;
+    if (table)
+        for (int i = threadIdx.x; i < nscale; i += blockDim.x) stab[i] = gscale[i];
     __syncthreads();
     const int total = GU ? plan->gu_tiles : plan->dn_tiles;
     int32_t *next = &plan->next[GU ? 0 : 1];
@@ -408,9 +412,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
                     return false;
                 const uint32_t fb = smem_u32(&sh->full[slot]);
-                if (lane == 0) {
-                    if (s == 0) {
-                        RwHdr &h = sh->hdr[slot];
+                if (s == 0) {
+                    RwHdr &h = sh->hdr[slot];
+                    if (lane == 0) {
                         h.task = task;
                         h.e = t.e;
                         h.r0 = t.r0;
@@ -419,8 +423,10 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                         h.rowbase = t.rowbase;
                         h.tokbase = t.tokbase;
                     }
-                    mbar_arrive_expect_tx(&sh->full[slot], bytes);
+                    if (lane >= 2 * NM && lane < 2 * NM + kRwTok) h.arow[lane - 2 * NM] = arow;
+                    __syncwarp();
                 }
+                if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], bytes);
                 __syncwarp();
                 if (active)
                     tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb);
@@ -458,15 +464,23 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             t.nt = h.nt;
             t.rowbase = h.rowbase;
             t.tokbase = h.tokbase;
+            // the activation scales of this lane's tokens (c, c+8, ...), for the epilogue
+            float sx[kRwTok / 8];
+#pragma unroll
+            for (int i = 0; i < kRwTok / 8; ++i) {
+                const int j = c + 8 * i;
+                const int r = j < t.nt ? h.arow[j] : 0;
+                sx[i] = j < t.nt ? (table ? stab[r] : gscale[r]) : 0.0f;
+            }
             const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (g.kdim + kRwInputs - 1) / kRwInputs;
             bool ok;
             switch (chunk_width(t.nt, kRwTok)) {
-            case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane); break;
-            case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane); break;
-            case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane); break;
-            case 8: ok = rows_task<GU, PROBE, 8>(a, t, g, nst, ring, sh, k, rin, c, lane); break;
-            default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane); break;
+            case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 8: ok = rows_task<GU, PROBE, 8>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
             }
             if (!ok) break;
         }
