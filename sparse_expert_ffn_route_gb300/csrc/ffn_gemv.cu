@@ -101,10 +101,10 @@ void ffn_configure(FfnArgs &a)
         a.slice_gu = 0;
         a.slice_dn = 0;
         a.tc_gu = a.tc_dn = kRowTok;
-        a.geo_gu[0] = make_rows_geo(a.H, a.F);
-        a.geo_gu[1] = make_rows_geo(a.H, a.Fs);
-        a.geo_dn[0] = make_rows_geo(a.F, a.H);
-        a.geo_dn[1] = make_rows_geo(a.Fs, a.H);
+        a.geo_gu[0] = make_rows_geo(a.H, a.F, kRowTaskGateUp);
+        a.geo_gu[1] = make_rows_geo(a.H, a.Fs, kRowTaskGateUp);
+        a.geo_dn[0] = make_rows_geo(a.F, a.H, kRowTaskDown);
+        a.geo_dn[1] = make_rows_geo(a.Fs, a.H, kRowTaskDown);
         return;
     }
     const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;

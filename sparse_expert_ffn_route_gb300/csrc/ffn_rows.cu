@@ -3,9 +3,9 @@
 // on the integer-dot path; "colibri 开发演进实录" §2.2 K1 / K1b: int4-gs64 weights against int8
 // activations, an integer dot per 64-group, then the group scale].
 //
-// A CTA is kRwWarps compute warps and one copy warp, one CTA per SM.  A task is (slot, block of
-// kRowBlock rows, chunk of at most kRwTok tokens) over the whole reduction (geometry
-// make_rows_geo).  The copy warp takes tasks one at a time from a counter in the plan, so a CTA
+// A CTA is kRwWarps compute warps and one copy warp, one CTA per SM.  A task is (slot, rows,
+// chunk of at most kRwTok tokens) over the whole reduction (geometry make_rows_geo): one block
+// of kRowBlock rows for gate/up, two for down, done block by block.  The copy warp takes tasks one at a time from a counter in the plan, so a CTA
 // that drew long tasks (the shared expert's 8-token chunks) takes fewer, and streams each
 // through a ring of stages in shared memory with TMA, 1024 inputs per stage: per matrix a
 // [64 rows][4 lines][128 B] box of nibbles (128-byte swizzle) and the [64][16] group scales,
@@ -156,7 +156,13 @@ __device__ __forceinline__ int act_row(const FfnArgs &a, const Task &t, int j)
     return t.rowbase + j;
 }
 
-// task -> (slot, row block, token chunk): tasks run (chunk, block) within a slot, block first
+// 64-row blocks of a task starting at row r0
+__device__ __forceinline__ int rw_blocks(const Geo &g, int r0)
+{
+    return (min(g.rb, g.nrows - r0) + kRowBlock - 1) / kRowBlock;
+}
+
+// task -> (slot, rows, token chunk): tasks run (chunk, rows) within a slot, rows first
 template <bool GU>
 __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int task)
 {
@@ -171,12 +177,12 @@ __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int 
     t.e = ps.expert[lo];
     t.sh = t.e < 0 ? 1 : 0;
     const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
-    const int nblk = (g.nrows + kRowBlock - 1) / kRowBlock;
+    const int nblk = (g.nrows + g.rb - 1) / g.rb;
     const int local = task - ps.prefix[lo];
     const int ch = local / nblk, blk = local - ch * nblk;
     t.j0 = ch * kRwTok;
     t.nt = min(kRwTok, ps.ntok[lo] - t.j0);
-    t.r0 = blk * kRowBlock;
+    t.r0 = blk * g.rb;
     t.tokbase = ps.tokbase[lo];
     t.rowbase = ps.rowbase[lo] + t.j0;
     t.s = 0;
@@ -385,34 +391,37 @@ __global__ void __launch_bounds__(kRwThreads, 1)
 
             const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
+            const int nq = rw_blocks(geo, t.r0) * nst;   // stages of the task, block by block
             const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
             const uint32_t bytes = NM * (kRwWBytes + kRwSBytes) + t.nt * kRwTokBytes;
             // this lane's box: map, shared-memory offset, coordinates (the line or group
             // coordinate advances with the stage)
             const CUtensorMap *map = &maps.act;
-            int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
+            int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0, by = 0, bz = 0;
             const bool active = lane < 2 * NM + t.nt;
             if (lane < NM) {
                 map = &maps.w[t.sh][lane];
                 off = lane * kRwWBytes;
                 z = wrow;
                 dy = kRwLines;
+                bz = kRowBlock;
             } else if (lane < 2 * NM) {
                 map = &maps.s[t.sh][lane - NM];
                 off = NM * kRwWBytes + (lane - NM) * kRwSBytes;
                 y = wrow;
                 dx = kRwLines * 4;
+                by = kRowBlock;
             } else {
                 off = NM * (kRwWBytes + kRwSBytes) + (lane - 2 * NM) * kRwTokBytes;
                 z = arow;
                 dy = kRwLines;
             }
-            for (int s = 0; s < nst; ++s, ++k) {
+            for (int q = 0, b = 0, s = 0; q < nq; ++q, ++k) {
                 const int slot = (int)(k % D);
                 if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
                     return false;
                 const uint32_t fb = smem_u32(&sh->full[slot]);
-                if (s == 0) {
+                if (q == 0) {
                     RwHdr &h = sh->hdr[slot];
                     if (lane == 0) {
                         h.task = task;
@@ -429,7 +438,12 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], bytes);
                 __syncwarp();
                 if (active)
-                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb);
+                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy + b * by,
+                           z + b * bz, fb);
+                if (++s == nst) {
+                    s = 0;
+                    ++b;
+                }
             }
             task = ntask;
             t = tn;
@@ -474,13 +488,16 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             }
             const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (g.kdim + kRwInputs - 1) / kRwInputs;
-            bool ok;
-            switch (chunk_width(t.nt, kRwTok)) {
-            case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-            case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-            case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-            case 8: ok = rows_task<GU, PROBE, 8>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-            default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            const int nb = rw_blocks(g, t.r0);
+            const int width = chunk_width(t.nt, kRwTok);
+            bool ok = true;
+            for (int b = 0; b < nb && ok; ++b, t.r0 += kRowBlock) {
+                switch (width) {
+                case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                }
             }
             if (!ok) break;
         }

@@ -73,12 +73,15 @@ __host__ __device__ inline Geo make_tc_geo(int kdim, int nrows, int matrices)
     return g;
 }
 
-// Geometry of the row-per-lane-group GEMV (ffn_rows.cu): blocks of kRowBlock rows over the
-// whole reduction, every token of a chunk against one pass over the block's weights.
+// Geometry of the row-per-lane-group GEMV (ffn_rows.cu): tasks of `rows` rows (blocks of
+// kRowBlock, done one after the other) over the whole reduction, every token of a chunk
+// against one pass over the weights.  Down tasks take two blocks: their rows are a third as
+// long as gate/up rows, and a task has costs of its own.
 constexpr int kRowBlock = 64;
 constexpr int kRowTok = 8;    // tokens per task at most
+constexpr int kRowTaskGateUp = kRowBlock, kRowTaskDown = 2 * kRowBlock;
 
-__host__ __device__ inline Geo make_rows_geo(int kdim, int nrows)
+__host__ __device__ inline Geo make_rows_geo(int kdim, int nrows, int rows)
 {
     Geo g;
     g.kdim = kdim;
@@ -88,8 +91,8 @@ __host__ __device__ inline Geo make_rows_geo(int kdim, int nrows)
     g.lpr = 4;
     g.rpw = 8;
     g.nc = 1;
-    g.ru = kRowBlock;
-    g.rb = kRowBlock;
+    g.ru = rows;
+    g.rb = rows;
     g.rowbytes = kdim / 2;
     g.G = kdim / 64;
     return g;
