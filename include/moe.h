@@ -177,7 +177,7 @@ int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls
  * kernels.  The tensor path takes batches beyond the decode route (T > 64)
  * whose matrices have hidden, d_ff and d_ff_shared in multiples of 512, when
  * the expected tokens per routed expert T*K/U (U = E*(1-(1-K/E)^T), the
- * distinct experts of uniform routing) is at least 5, or at once when hidden
+ * distinct experts of uniform routing) is at least 10, or at once when hidden
  * or d_ff is under 1024.  Returns -1 for an invalid config or T < 0.
  * ["MoE 路由与专家流式加载" §1.3: the expert FFN turns from a weight-streaming
  * GEMV into a dense contraction once tokens per expert grow.] */

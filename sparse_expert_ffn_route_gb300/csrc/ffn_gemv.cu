@@ -68,15 +68,16 @@ int pick_tc(int nc, int T, int K, int E, bool shared)
 bool ffn_use_tensor_cores(const FfnArgs &a)
 {
     if (a.T <= kRouteClusterMaxT || !ffn_tc_supported(a)) return false;
-    // Measured on GB300: a tensor-core tile pays about the same per 64-input group whatever its
-    // width, while the GEMV kernels stream an expert's weights once per 4 of its tokens.  On
-    // wide matrices the GEMV kernels are faster below about 5 tokens per routed expert (GLM
-    // T=128: 2.40 vs 2.76 ms; wide layer T=128: 3.05 vs 3.87 ms) and slower above (GLM T=256:
-    // 4.80 vs 3.11 ms).  On narrow ones (hidden or d_ff under 1024) their tasks are too short
-    // and the tensor path wins from the first batch past the decode route.
+    // Measured on GB300 (gate/up + down): a tensor-core tile pays about the same per 64-input
+    // group whatever its width, while the row GEMV streams an expert's weights once per 8 of
+    // its tokens.  On wide matrices the row GEMV is faster below about 10 tokens per routed
+    // expert (GLM T=256, 8 per expert: 2.35 vs 3.11 ms; wide layer T=256: 2.78 vs 4.46 ms),
+    // level near 10 (wide layer T=512: 5.18 vs 5.08 ms) and slower above (GLM T=512: 4.39 vs
+    // 3.46 ms).  On narrow ones (hidden or d_ff under 1024) its tasks are too short and the
+    // tensor path wins from the first batch past the decode route (A3B T=128: 0.092 vs 0.143 ms).
     if (a.H < 1024 || a.F < 1024) return true;
     const double U = a.E * (1.0 - pow(1.0 - (double)a.K / a.E, (double)a.T));
-    return U > 0.0 && (double)a.T * a.K / U >= 5.0;
+    return U > 0.0 && (double)a.T * a.K / U >= 10.0;
 }
 
 void ffn_configure(FfnArgs &a)

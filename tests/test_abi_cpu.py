@@ -50,11 +50,12 @@ def test_workspace_size(lib):
 def test_ffn_path_query(lib):
     # the tensor-core grouped GEMM takes batches beyond the 64-token decode route when every
     # matrix of the layer has dimensions in multiples of 512
-    # ... and, on wide matrices, at least 5 expected tokens per routed expert (GLM: T = 65 and
-    # 128 give 2.3 and 4.1, T = 256 gives 8.0); narrow ones (d_ff 512) take it at once
+    # ... and, on wide matrices, at least 10 expected tokens per routed expert (GLM: T = 65,
+    # 128 and 256 give 2.3, 4.1 and 8.0, T = 512 gives 16.0); narrow ones (d_ff 512) take it
+    # at once
     glm = _cfg(hidden=6144, n_experts=256, top_k=8, d_ff=2048, d_ff_shared=2048)
-    assert [moe.moe_ffn_uses_tensor_cores(glm, t) for t in (0, 1, 64, 65, 128, 256, 4096)] == \
-        [0, 0, 0, 0, 0, 1, 1]
+    assert [moe.moe_ffn_uses_tensor_cores(glm, t) for t in (0, 1, 64, 65, 128, 256, 512, 4096)] == \
+        [0, 0, 0, 0, 0, 0, 1, 1]
     a3b = _cfg(hidden=2048, n_experts=256, top_k=8, d_ff=512, d_ff_shared=512)
     assert [moe.moe_ffn_uses_tensor_cores(a3b, t) for t in (64, 65, 128)] == [0, 1, 1]
     tiny = _cfg()   # d_ff = 128: GEMV kernels at every batch size

@@ -196,6 +196,21 @@ def test_expert_ffn_exact_accumulators(moe, name, T):
     _check_ffn(g, ref)
 
 
+@pytest.mark.parametrize("T", [24, 64])
+def test_expert_ffn_exact_accumulators_row_gemv(moe, T):
+    """Row GEMV (decode-sized batch, reductions in multiples of 256) on a mid-sized shape:
+    gate/up rows of 2048 inputs take two 1024-input stages, down rows of 768 inputs one stage
+    whose last line lies past the row (zero-filled), down tasks take two 64-row blocks, and
+    routed experts with more than 8 tokens run in several token chunks."""
+    from dataclasses import replace
+    wl = replace(synth.WORKLOADS["a3b_decode"], name="rows_mid", hidden=2048, d_ff=768,
+                 d_ff_shared=768, n_experts=16, top_k=4)
+    assert moe.moe_ffn_uses_tensor_cores(moe_cfg(wl), T) == 0
+    g, ref, perm = _ffn_both(moe, wl, T)
+    assert np.diff(perm["offsets"]).max() > 8
+    _check_ffn(g, ref)
+
+
 def test_expert_ffn_tensor_tile_edges(moe):
     """Tensor-core path (a3b shape, T = 300) on a constructed routing: experts with 129 tokens
     (a full 128-token tile plus a one-token tile), exactly 128, 127, 1 and 0 tokens."""
