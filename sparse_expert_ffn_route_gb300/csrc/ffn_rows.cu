@@ -16,8 +16,8 @@
 // c = l % 8 (16 bytes, 32 weights) of every 128-byte line, so the eight lanes of a row split
 // its reduction.  Shared-memory reads run at the minimum number of wavefronts: the swizzle
 // spreads a warp's nibble chunks over all banks, the codes are broadcast to the rows' lanes,
-// and lanes c >= 4 read the two halves of their 32 codes in the other order (with the weight
-// words swapped to match), so the eight chunks of a read fall on distinct banks.
+// and lanes c >= 4 read the two halves of their 32 codes (and of their 32 weights) in the
+// other order, so the eight chunks of a read fall on distinct banks.
 //
 // Per chunk of 32 weights and token (integer, exact): with
 //     lo = ((w << 4) & 0xF0F0F0F0) ^ 0x80808080,   hi = (w & 0xF0F0F0F0) ^ 0x80808080
@@ -221,14 +221,10 @@ __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const
             float sc[NM];
 #pragma unroll
             for (int m = 0; m < NM; ++m) {
-                uint4 wq = *reinterpret_cast<const uint4 *>(stg + m * kRwWBytes + woff);
-                if (sw) {
-                    const uint32_t x = wq.x, y = wq.y;
-                    wq.x = wq.z;
-                    wq.y = wq.w;
-                    wq.z = x;
-                    wq.w = y;
-                }
+                // the chunk as two 8-byte halves, in the order this lane reads its codes
+                const uint2 *wp = reinterpret_cast<const uint2 *>(stg + m * kRwWBytes + woff);
+                const uint2 w0 = wp[sw], w1 = wp[sw ^ 1];
+                const uint4 wq = make_uint4(w0.x, w0.y, w1.x, w1.y);
                 signed_nibbles(wq.x, lo[m][0], hi[m][0]);
                 signed_nibbles(wq.y, lo[m][1], hi[m][1]);
                 signed_nibbles(wq.z, lo[m][2], hi[m][2]);
@@ -489,13 +485,17 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (g.kdim + kRwInputs - 1) / kRwInputs;
             const int nb = rw_blocks(g, t.r0);
-            const int width = chunk_width(t.nt, kRwTok);
+            // code paths for 1-6 and 8 tokens: the dot-product work follows the chunk's
+            // token count (7 rounds up to 8)
             bool ok = true;
             for (int b = 0; b < nb && ok; ++b, t.r0 += kRowBlock) {
-                switch (width) {
+                switch (t.nt) {
                 case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
                 case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                case 3: ok = rows_task<GU, PROBE, 3>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
                 case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                case 5: ok = rows_task<GU, PROBE, 5>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+                case 6: ok = rows_task<GU, PROBE, 6>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
                 default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
                 }
             }
