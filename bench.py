@@ -458,6 +458,8 @@ def run_ours(args, world, rank, local):
                    "routed_scaling_factor": wl.routed_scaling_factor, "top_p": wl.top_p,
                    "unique_experts_mean": round(float(np.mean([s[0] for s in stats])), 1),
                    "batches_rotated": N_BATCHES,
+                   "ffn_kernel": {moe.MOE_FFN_WARP_GEMV: "warp GEMV", moe.MOE_FFN_TENSOR: "tcgen05 grouped GEMM",
+                                  moe.MOE_FFN_ROW_GEMV: "row GEMV"}.get(moe.moe_ffn_path(cfg, T), "?"),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights"
                          % (np.mean([algorithmic_bytes(wl, T, *s)["layer"] for s in stats]) / 1e9),
                    "parallelism": "dp%d (replicas, no collective)" % world},

@@ -28,6 +28,9 @@ MOE_ERR_WORKSPACE = -7
 MOE_ERR_DEVICE = -8
 MOE_FLAG_SYNC_CHECK = 1
 MOE_FLAG_STAGE_EVENTS = 2
+MOE_FFN_WARP_GEMV = 0
+MOE_FFN_TENSOR = 1
+MOE_FFN_ROW_GEMV = 2
 STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", "down", "combine")
 
 # every symbol include/moe.h declares
@@ -35,7 +38,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
            "moe_topk_hits", "moe_quantize_int4_gs64", "moe_selftest_wait_timeout",
-           "moe_layer_forward_host")
+           "moe_layer_forward_host", "moe_ffn_path")
 
 
 class MoeError(RuntimeError):
@@ -95,6 +98,8 @@ def load_library():
     L.moe_workspace_size.restype = sz
     L.moe_ffn_uses_tensor_cores.argtypes = [vp, i32]
     L.moe_ffn_uses_tensor_cores.restype = i32
+    L.moe_ffn_path.argtypes = [vp, i32]
+    L.moe_ffn_path.restype = i32
     L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
@@ -143,6 +148,12 @@ def moe_ffn_uses_tensor_cores(cfg: MoeConfig, T: int) -> int:
     """1 if a call with T tokens runs the tensor-core grouped GEMM, 0 for the GEMV kernels,
     -1 for an invalid config or T."""
     return int(load_library().moe_ffn_uses_tensor_cores(ctypes.byref(cfg), T))
+
+
+def moe_ffn_path(cfg: MoeConfig, T: int) -> int:
+    """The grouped expert-FFN kernel a call with T tokens runs: MOE_FFN_WARP_GEMV,
+    MOE_FFN_TENSOR or MOE_FFN_ROW_GEMV; -1 for an invalid config or T."""
+    return int(load_library().moe_ffn_path(ctypes.byref(cfg), T))
 
 
 def alloc_workspace(cfg: MoeConfig, max_tokens: int, device="cuda") -> torch.Tensor:
@@ -270,7 +281,7 @@ def moe_layer_forward_host(cfg, x_host, w_router, bias, routed, shared, y_host, 
                                                   ctypes.byref(sw) if sw else None, _ptr(y_host),
                                                   ctypes.byref(ro) if ro else None, _ptr(workspace),
                                                   workspace.numel(), flags, _stream(stream)),
-           "moe_layer_forward_host")
+           "moe_layer_forward_host", "moe_ffn_path")
 
 
 def moe_check_errors(workspace, stream=None):

@@ -484,6 +484,24 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
     return ffn_use_tensor_cores(a) ? 1 : 0;
 }
 
+int moe_ffn_path(const moe_config *cfg, int T)
+{
+    const int tc = moe_ffn_uses_tensor_cores(cfg, T);
+    if (tc != 0) return tc;
+    // the row GEMV's shape conditions; the operands' 16-byte alignment holds for every call
+    // that passes validation (weights are checked, the workspace regions are aligned)
+    FfnArgs a;
+    memset(&a, 0, sizeof a);
+    a.H = cfg->hidden;
+    a.F = cfg->d_ff;
+    a.n_shared = cfg->n_shared;
+    a.Fs = cfg->n_shared ? cfg->d_ff_shared : cfg->d_ff;
+    a.hstride = fmax_of(*cfg);
+    a.xq.q_ld = cfg->hidden;
+    a.hq.q_ld = a.hstride;
+    return ffn_rows_supported(a) ? MOE_FFN_ROW_GEMV : MOE_FFN_WARP_GEMV;
+}
+
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
               int T, int32_t *ids, float *w, int32_t *keff, void *workspace,
               size_t workspace_bytes, void *stream)

@@ -63,6 +63,15 @@ def test_ffn_path_query(lib):
     assert moe.moe_ffn_uses_tensor_cores(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 100) == 0
     assert moe.moe_ffn_uses_tensor_cores(glm, -1) == -1
     assert moe.moe_ffn_uses_tensor_cores(_cfg(top_k=9), 16) == -1
+    # the kernel below the tensor path: the row GEMV when every reduction is a multiple of
+    # 256 inputs, the warp GEMV otherwise
+    R, W, TC = moe.MOE_FFN_ROW_GEMV, moe.MOE_FFN_WARP_GEMV, moe.MOE_FFN_TENSOR
+    assert [moe.moe_ffn_path(glm, t) for t in (1, 32, 256, 512)] == [R, R, R, TC]
+    assert [moe.moe_ffn_path(a3b, t) for t in (64, 65)] == [R, TC]
+    assert [moe.moe_ffn_path(tiny, t) for t in (1, 16, 65)] == [W, W, W]
+    assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 32) == W
+    assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=768), 32) == R
+    assert moe.moe_ffn_path(glm, -1) == -1 and moe.moe_ffn_path(_cfg(top_k=9), 16) == -1
 
 
 def test_lookahead_validation(lib):

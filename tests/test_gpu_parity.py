@@ -205,7 +205,7 @@ def test_expert_ffn_exact_accumulators_row_gemv(moe, T):
     from dataclasses import replace
     wl = replace(synth.WORKLOADS["a3b_decode"], name="rows_mid", hidden=2048, d_ff=768,
                  d_ff_shared=768, n_experts=16, top_k=4)
-    assert moe.moe_ffn_uses_tensor_cores(moe_cfg(wl), T) == 0
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_ROW_GEMV
     g, ref, perm = _ffn_both(moe, wl, T)
     assert np.diff(perm["offsets"]).max() > 8
     _check_ffn(g, ref)
