@@ -281,7 +281,7 @@ def moe_layer_forward_host(cfg, x_host, w_router, bias, routed, shared, y_host, 
                                                   ctypes.byref(sw) if sw else None, _ptr(y_host),
                                                   ctypes.byref(ro) if ro else None, _ptr(workspace),
                                                   workspace.numel(), flags, _stream(stream)),
-           "moe_layer_forward_host", "moe_ffn_path")
+           "moe_layer_forward_host")
 
 
 def moe_check_errors(workspace, stream=None):

@@ -5,12 +5,13 @@
 //
 // A CTA is kRwWarps compute warps and one copy warp, one CTA per SM.  A task is (slot, rows,
 // chunk of at most kRwTok tokens) over the whole reduction (geometry make_rows_geo): one block
-// of kRowBlock rows for gate/up, two for down, done block by block.  The copy warp takes tasks one at a time from a counter in the plan, so a CTA
-// that drew long tasks (the shared expert's 8-token chunks) takes fewer, and streams each
-// through a ring of stages in shared memory with TMA, 1024 inputs per stage: per matrix a
-// [64 rows][4 lines][128 B] box of nibbles (128-byte swizzle) and the [64][16] group scales,
-// plus one [4][256 B] box of int8 codes per token (the row picked by token id for gate/up, by
-// output row for down).  One TMA instruction per stage issues all of them, a box per lane.
+// of kRowBlock rows for gate/up, two for down, done block by block.  The copy warp takes tasks
+// one at a time from a counter in the plan, so a CTA that drew long tasks (the shared
+// expert's 8-token chunks) takes fewer, and streams each through a ring of stages in shared
+// memory with TMA, 1024 inputs per stage: per matrix a [64 rows][4 lines][128 B] box of
+// nibbles (128-byte swizzle) and the [64][16] group scales, plus one [4][256 B] box of int8
+// codes per token (the row picked by token id for gate/up, by output row for down).  One TMA
+// instruction per stage issues all of them, a box per lane.
 //
 // Compute warp w owns rows 4w .. 4w+3 of the block; lane l takes row 4w + l/8 and chunk
 // c = l % 8 (16 bytes, 32 weights) of every 128-byte line, so the eight lanes of a row split
@@ -189,8 +190,9 @@ __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int 
     return t;
 }
 
-// The compute warps' share of one task of width N (N >= the task's token count): every stage
-// of the reduction, then the epilogue.  k counts the stages of the CTA.
+// The compute warps' share of one 64-row block of a task (rows t.r0 ..), computed for N tokens
+// (N >= the task's token count): every stage of the reduction, then the epilogue.  k counts
+// the stages of the CTA.
 template <bool GU, bool PROBE, int N>
 __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const Geo &g, int nst,
                                           const uint8_t *ring, RwShared *sh, uint32_t &k, int rin,
