@@ -186,7 +186,8 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
 /* Which grouped expert-FFN kernel a call with T tokens runs (host-side, no
  * device work): MOE_FFN_TENSOR when moe_ffn_uses_tensor_cores says so;
  * otherwise MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when
- * hidden, d_ff and d_ff_shared are multiples of 256, else MOE_FFN_WARP_GEMV.
+ * hidden, d_ff and d_ff_shared are multiples of 256 and T >= 8, else
+ * MOE_FFN_WARP_GEMV.
  * Returns -1 for an invalid config or T < 0.
  * ["colibri 开发演进实录" §2.2 K1/K1b: the integer dot both GEMV kernels run.] */
 #define MOE_FFN_WARP_GEMV 0

@@ -96,8 +96,9 @@ void ffn_configure(FfnArgs &a)
         a.geo_dn[1] = make_tc_geo(a.Fs, a.H, 1);
         return;
     }
-    // the rest: the row GEMV where its shapes allow, else the warp GEMV below
-    a.rows = ffn_rows_supported(a) ? 1 : 0;
+    // the rest: the row GEMV where its shapes allow and the batch has kRowGemvMinT tokens or
+    // more, else the warp GEMV below
+    a.rows = (a.T >= kRowGemvMinT && ffn_rows_supported(a)) ? 1 : 0;
     if (a.rows) {
         a.slice_gu = 0;
         a.slice_dn = 0;

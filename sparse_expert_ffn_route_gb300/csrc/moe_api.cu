@@ -499,7 +499,7 @@ int moe_ffn_path(const moe_config *cfg, int T)
     a.hstride = fmax_of(*cfg);
     a.xq.q_ld = cfg->hidden;
     a.hq.q_ld = a.hstride;
-    return ffn_rows_supported(a) ? MOE_FFN_ROW_GEMV : MOE_FFN_WARP_GEMV;
+    return T >= kRowGemvMinT && ffn_rows_supported(a) ? MOE_FFN_ROW_GEMV : MOE_FFN_WARP_GEMV;
 }
 
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
