@@ -1,5 +1,6 @@
-// ffn_gemv.cu -- host side of the grouped expert FFN: chooses the kernel variant (chunks
-// per lane, tokens per chunk, rows in flight) and the task geometry, and launches.
+// ffn_gemv.cu -- host side of the grouped expert FFN: chooses the kernel (tcgen05 grouped
+// GEMM, row GEMV or warp GEMV), the warp GEMV's variant (chunks per lane, tokens per chunk,
+// rows in flight) and the task geometry, and launches.
 #include "ffn_kernels.cuh"
 #include "launch.cuh"
 
