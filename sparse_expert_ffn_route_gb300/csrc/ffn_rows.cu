@@ -5,7 +5,7 @@
 //
 // A CTA is kRwWarps compute warps and one copy warp, one CTA per SM.  A task is (slot, rows,
 // chunk of at most kRwTok tokens) over the whole reduction (geometry make_rows_geo): one block
-// of kRowBlock rows for gate/up, two for down, done block by block.  The copy warp takes tasks
+// of kRowBlock rows for gate/up, two for down.  The copy warp takes tasks
 // one at a time from a counter in the plan, so a CTA that drew long tasks (the shared
 // expert's 8-token chunks) takes fewer, and streams each through a ring of stages in shared
 // memory with TMA, 1024 inputs per stage: per matrix a [64 rows][4 lines][128 B] box of
@@ -57,8 +57,10 @@ constexpr int kRwABytes = kRwTok * kRwTokBytes;
 static_assert(kRowBlock == kRwWarps * kRwRowsPerWarp, "the compute warps cover the row block");
 static_assert(kRwTok % 8 == 0 && kRwTok <= 16, "a lane stores tokens c, c+8, ...; lanes issue the code boxes");
 
+// operand blocks per stage, each with its own nibble and scale boxes: gate and up of the same
+// 64 rows, or the two 64-row blocks of a down task.  Both share every code read.
 template <bool GU>
-constexpr int rw_nm() { return GU ? 2 : 1; }
+constexpr int rw_nm() { return 2; }
 template <bool GU>
 constexpr int rw_stage_bytes() { return rw_nm<GU>() * (kRwWBytes + kRwSBytes) + kRwABytes; }
 // as many stages as fit the budget (beside the plan copy, within 227 KB)
@@ -157,12 +159,6 @@ __device__ __forceinline__ int act_row(const FfnArgs &a, const Task &t, int j)
     return t.rowbase + j;
 }
 
-// 64-row blocks of a task starting at row r0
-__device__ __forceinline__ int rw_blocks(const Geo &g, int r0)
-{
-    return (min(g.rb, g.nrows - r0) + kRowBlock - 1) / kRowBlock;
-}
-
 // task -> (slot, rows, token chunk): tasks run (chunk, rows) within a slot, rows first
 template <bool GU>
 __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int task)
@@ -190,9 +186,10 @@ __device__ __forceinline__ Task rw_task(const FfnArgs &a, const RwPlan &ps, int 
     return t;
 }
 
-// The compute warps' share of one 64-row block of a task (rows t.r0 ..), computed for N tokens
-// (N >= the task's token count): every stage of the reduction, then the epilogue.  k counts
-// the stages of the CTA.
+// The compute warps' share of one task, computed for N tokens (N >= the task's token count):
+// every stage of the reduction, then the epilogue.  Operand block m is gate (m = 0) and up
+// (m = 1) of rows t.r0 .. t.r0+63 for gate/up, rows t.r0 + 64 m .. for down.  k counts the
+// stages of the CTA.
 template <bool GU, bool PROBE, int N>
 __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const Geo &g, int nst,
                                           const uint8_t *ring, RwShared *sh, uint32_t &k, int rin,
@@ -254,9 +251,10 @@ __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const
                         // lane l ^ 1
                         const int other = __shfl_xor_sync(0xffffffffu, d, 1);
                         const int grp = s * (kRwInputs / 64) + gl;
-                        if (t.sh == 0 && j < t.nt && (c & 1) == 0 && grp < g.G) {
+                        const int prow = t.r0 + (GU ? 0 : m * kRowBlock) + rin;
+                        if (t.sh == 0 && j < t.nt && (c & 1) == 0 && grp < g.G && prow < g.nrows) {
                             const size_t pr = (size_t)(t.rowbase + j - a.routed_rowbase);
-                            const size_t o = (pr * g.nrows + t.r0 + rin) * g.G + grp;
+                            const size_t o = (pr * g.nrows + prow) * g.G + grp;
                             int32_t *dst = GU ? (m == 0 ? a.probe.acc_gate : a.probe.acc_up)
                                               : a.probe.acc_down;
                             if (dst) dst[o] = (d + other) >> 4;
@@ -285,10 +283,12 @@ __device__ __forceinline__ bool rows_task(const FfnArgs &a, const Task &t, const
         const size_t orow = (size_t)(t.rowbase + j);
         const float s = sx[j >> 3] * 0.0625f;
         if (GU) {
-            const float gate = s * acc[0][j], up = s * acc[NM - 1][j];
+            const float gate = s * acc[0][j], up = s * acc[1][j];
             a.h[orow * a.hstride + row] = gate / (1.0f + expf(-gate)) * up;
         } else {
-            a.y[orow * a.H + row] = s * acc[0][j];
+#pragma unroll
+            for (int m = 0; m < NM; ++m)
+                if (row + m * kRowBlock < g.nrows) a.y[orow * a.H + row + m * kRowBlock] = s * acc[m][j];
         }
     }
     return true;
@@ -389,37 +389,35 @@ __global__ void __launch_bounds__(kRwThreads, 1)
 
             const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
-            const int nq = rw_blocks(geo, t.r0) * nst;   // stages of the task, block by block
             const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
             const uint32_t bytes = NM * (kRwWBytes + kRwSBytes) + t.nt * kRwTokBytes;
             // this lane's box: map, shared-memory offset, coordinates (the line or group
             // coordinate advances with the stage)
             const CUtensorMap *map = &maps.act;
-            int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0, by = 0, bz = 0;
+            // (gate/up: matrix m; down: the m-th 64-row block of the one matrix)
+            int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
             const bool active = lane < 2 * NM + t.nt;
             if (lane < NM) {
-                map = &maps.w[t.sh][lane];
+                map = &maps.w[t.sh][GU ? lane : 0];
                 off = lane * kRwWBytes;
-                z = wrow;
+                z = wrow + (GU ? 0 : lane * kRowBlock);
                 dy = kRwLines;
-                bz = kRowBlock;
             } else if (lane < 2 * NM) {
-                map = &maps.s[t.sh][lane - NM];
+                map = &maps.s[t.sh][GU ? lane - NM : 0];
                 off = NM * kRwWBytes + (lane - NM) * kRwSBytes;
-                y = wrow;
+                y = wrow + (GU ? 0 : (lane - NM) * kRowBlock);
                 dx = kRwLines * 4;
-                by = kRowBlock;
             } else {
                 off = NM * (kRwWBytes + kRwSBytes) + (lane - 2 * NM) * kRwTokBytes;
                 z = arow;
                 dy = kRwLines;
             }
-            for (int q = 0, b = 0, s = 0; q < nq; ++q, ++k) {
+            for (int s = 0; s < nst; ++s, ++k) {
                 const int slot = (int)(k % D);
                 if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
                     return false;
                 const uint32_t fb = smem_u32(&sh->full[slot]);
-                if (q == 0) {
+                if (s == 0) {
                     RwHdr &h = sh->hdr[slot];
                     if (lane == 0) {
                         h.task = task;
@@ -436,12 +434,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], bytes);
                 __syncwarp();
                 if (active)
-                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy + b * by,
-                           z + b * bz, fb);
-                if (++s == nst) {
-                    s = 0;
-                    ++b;
-                }
+                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb);
             }
             task = ntask;
             t = tn;
@@ -486,20 +479,17 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             }
             const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (g.kdim + kRwInputs - 1) / kRwInputs;
-            const int nb = rw_blocks(g, t.r0);
             // code paths for 1-6 and 8 tokens: the dot-product work follows the chunk's
             // token count (7 rounds up to 8)
-            bool ok = true;
-            for (int b = 0; b < nb && ok; ++b, t.r0 += kRowBlock) {
-                switch (t.nt) {
-                case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                case 3: ok = rows_task<GU, PROBE, 3>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                case 5: ok = rows_task<GU, PROBE, 5>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                case 6: ok = rows_task<GU, PROBE, 6>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
-                }
+            bool ok;
+            switch (t.nt) {
+            case 1: ok = rows_task<GU, PROBE, 1>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 2: ok = rows_task<GU, PROBE, 2>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 3: ok = rows_task<GU, PROBE, 3>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 4: ok = rows_task<GU, PROBE, 4>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 5: ok = rows_task<GU, PROBE, 5>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            case 6: ok = rows_task<GU, PROBE, 6>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
+            default: ok = rows_task<GU, PROBE, kRwTok>(a, t, g, nst, ring, sh, k, rin, c, lane, sx); break;
             }
             if (!ok) break;
         }
