@@ -280,6 +280,24 @@ struct StageScope {
     StageRec rec_;
 };
 
+// the shape fields of an FFN call, as the path queries see them (no buffers)
+FfnArgs query_args(const moe_config &c, int T)
+{
+    FfnArgs a;
+    memset(&a, 0, sizeof a);
+    a.H = c.hidden;
+    a.F = c.d_ff;
+    a.n_shared = c.n_shared;
+    a.Fs = c.n_shared ? c.d_ff_shared : c.d_ff;
+    a.E = c.n_experts;
+    a.K = c.top_k;
+    a.T = T;
+    a.hstride = fmax_of(c);
+    a.xq.q_ld = c.hidden;
+    a.hq.q_ld = a.hstride;
+    return a;
+}
+
 }  // namespace
 
 int set_error(int code, const char *fmt, ...)
@@ -472,16 +490,7 @@ int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
 {
     if (check_config(cfg) != MOE_OK || T < 0) return -1;
-    FfnArgs a;
-    memset(&a, 0, sizeof a);
-    a.H = cfg->hidden;
-    a.F = cfg->d_ff;
-    a.n_shared = cfg->n_shared;
-    a.Fs = cfg->n_shared ? cfg->d_ff_shared : cfg->d_ff;
-    a.E = cfg->n_experts;
-    a.K = cfg->top_k;
-    a.T = T;
-    return ffn_use_tensor_cores(a) ? 1 : 0;
+    return ffn_use_tensor_cores(query_args(*cfg, T)) ? 1 : 0;
 }
 
 int moe_ffn_path(const moe_config *cfg, int T)
@@ -490,16 +499,8 @@ int moe_ffn_path(const moe_config *cfg, int T)
     if (tc != 0) return tc;
     // the row GEMV's shape conditions; the operands' 16-byte alignment holds for every call
     // that passes validation (weights are checked, the workspace regions are aligned)
-    FfnArgs a;
-    memset(&a, 0, sizeof a);
-    a.H = cfg->hidden;
-    a.F = cfg->d_ff;
-    a.n_shared = cfg->n_shared;
-    a.Fs = cfg->n_shared ? cfg->d_ff_shared : cfg->d_ff;
-    a.hstride = fmax_of(*cfg);
-    a.xq.q_ld = cfg->hidden;
-    a.hq.q_ld = a.hstride;
-    return T >= kRowGemvMinT && ffn_rows_supported(a) ? MOE_FFN_ROW_GEMV : MOE_FFN_WARP_GEMV;
+    return T >= kRowGemvMinT && ffn_rows_supported(query_args(*cfg, T)) ? MOE_FFN_ROW_GEMV
+                                                                         : MOE_FFN_WARP_GEMV;
 }
 
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
