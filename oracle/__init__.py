@@ -59,9 +59,11 @@ def lib():
         L.moe_ref_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_ref_quant_row.argtypes = [vp, i32, vp, vp]
         L.moe_ref_quant_row.restype = None
+        L.moe_ref_quant_row_pre.argtypes = [vp, i32, vp, vp, vp]
+        L.moe_ref_quant_row_pre.restype = None
         L.moe_ref_group_dot.argtypes = [vp, vp, i32]
-        L.moe_ref_expert_apply.argtypes = [i32, i32] + [vp] * 6 + [vp, ctypes.c_float] + [vp] * 8
-        L.moe_ref_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp] + [vp] * 7
+        L.moe_ref_expert_apply.argtypes = [i32, i32] + [vp] * 6 + [vp, ctypes.c_float] + [vp] * 9
+        L.moe_ref_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp] + [vp] * 8
         L.moe_ref_shared_ffn.argtypes = [vp, vp, i32, vp, vp]
         L.moe_ref_combine.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp]
         L.moe_ref_layer_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -206,6 +208,15 @@ def quant_row(v):
     return q, float(s[0])
 
 
+def quant_row_pre(v):
+    """quant_row plus the fp32 value each code rounds (v * 127 / amax)."""
+    v = _np(v, np.float32)
+    q = np.zeros(v.shape[-1], np.int8); s = np.zeros(1, np.float32)
+    pre = np.zeros(v.shape[-1], np.float32)
+    lib().moe_ref_quant_row_pre(_p(v), v.shape[-1], _p(q), _p(s), _p(pre))
+    return q, float(s[0]), pre
+
+
 def quant_rows(m):
     m = _np(m, np.float32)
     q = np.zeros(m.shape, np.int8); s = np.zeros(m.shape[0], np.float32)
@@ -225,18 +236,19 @@ def expert_apply(H, F, expert: Dict, xq, sx: float, probes: bool = False, hq_in=
     wt, keep = _weights(expert)
     xq = _np(xq, np.int8)
     y = np.zeros(H, np.float64)
-    ag = au = ad = hq = hs = None
+    ag = au = ad = hq = hs = hp = None
     if probes:
         ag = np.zeros((F, H // 64), np.int32); au = np.zeros((F, H // 64), np.int32)
         ad = np.zeros((H, F // 64), np.int32); hq = np.zeros(F, np.int8); hs = np.zeros(1, np.float32)
+        hp = np.zeros(F, np.float32)
     hqi = _np(hq_in, np.int8)
     hsi = None if hs_in is None else np.array([hs_in], np.float32)
     _check(lib().moe_ref_expert_apply(H, F, wt.w_gate, wt.s_gate, wt.w_up, wt.s_up, wt.w_down,
                                       wt.s_down, _p(xq), sx, _p(y), _p(ag), _p(au), _p(ad),
-                                      _p(hq), _p(hs), _p(hqi), _p(hsi)), "moe_ref_expert_apply")
+                                      _p(hq), _p(hs), _p(hqi), _p(hsi), _p(hp)), "moe_ref_expert_apply")
     out = {"y": y}
     if probes:
-        out.update(acc_gate=ag, acc_up=au, acc_down=ad, hq=hq, hs=float(hs[0]))
+        out.update(acc_gate=ag, acc_up=au, acc_down=ad, hq=hq, hs=float(hs[0]), h_pre=hp)
     return out
 
 
@@ -247,19 +259,19 @@ def expert_ffn(cfg: Config, x, routed: Dict, offsets, tok, probes: bool = False,
     T, H, F = x.shape[0], cfg.hidden, cfg.d_ff
     P = int(offsets[cfg.n_experts])
     y = np.zeros((max(P, 1), H), np.float64)
-    ag = au = ad = hq = hs = None
+    ag = au = ad = hq = hs = hp = None
     if probes:
         ag = np.zeros((P, F, H // 64), np.int32); au = np.zeros((P, F, H // 64), np.int32)
         ad = np.zeros((P, H, F // 64), np.int32); hq = np.zeros((P, F), np.int8)
-        hs = np.zeros(P, np.float32)
+        hs = np.zeros(P, np.float32); hp = np.zeros((P, F), np.float32)
     hqi = _np(hq_in, np.int8); hsi = _np(hs_in, np.float32)
     tokp = tok if tok.size else np.zeros(1, np.int32)
     _check(lib().moe_ref_expert_ffn(ctypes.byref(cfg), _p(x), T, ctypes.byref(wt), _p(offsets),
                                     _p(tokp), _p(y), _p(ag), _p(au), _p(ad), _p(hq), _p(hs),
-                                    _p(hqi), _p(hsi)), "moe_ref_expert_ffn")
+                                    _p(hqi), _p(hsi), _p(hp)), "moe_ref_expert_ffn")
     out = {"y_pairs": y[:P]}
     if probes:
-        out.update(acc_gate=ag, acc_up=au, acc_down=ad, hq=hq, hs=hs)
+        out.update(acc_gate=ag, acc_up=au, acc_down=ad, hq=hq, hs=hs, h_pre=hp)
     return out
 
 

@@ -214,19 +214,29 @@ int moe_ref_permute(const moe_ref_config *c, const int32_t *ids, const int32_t *
  * ------------------------------------------------------------------------ */
 void moe_ref_quant_row(const float *v, int n, int8_t *q, float *scale)
 {
+    moe_ref_quant_row_pre(v, n, q, scale, NULL);
+}
+
+void moe_ref_quant_row_pre(const float *v, int n, int8_t *q, float *scale, float *pre)
+{
     float amax = 0.0f;
     for (int i = 0; i < n; ++i) {
         float a = fabsf(v[i]);
         if (a > amax) amax = a;
     }
     if (amax == 0.0f) {
-        for (int i = 0; i < n; ++i) q[i] = 0;
+        for (int i = 0; i < n; ++i) {
+            q[i] = 0;
+            if (pre) pre[i] = 0.0f;
+        }
         *scale = 0.0f;
         return;
     }
     const float inv = 127.0f / amax;
     for (int i = 0; i < n; ++i) {
-        float r = rintf(v[i] * inv);
+        const float p = v[i] * inv;   /* the value the code rounds */
+        if (pre) pre[i] = p;
+        float r = rintf(p);
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
         q[i] = (int8_t)r;
@@ -279,7 +289,7 @@ int moe_ref_expert_apply(int H, int F, const uint8_t *w_gate, const float *s_gat
                          const float *s_down, const int8_t *xq, float sx, double *y,
                          int32_t *acc_gate, int32_t *acc_up, int32_t *acc_down,
                          int8_t *hq_out, float *hs_out, const int8_t *hq_in,
-                         const float *hs_in)
+                         const float *hs_in, float *hpre_out)
 {
     if (H <= 0 || F <= 0 || H % GS || F % GS) return -2;
     const int GH = H / GS, GF = F / GS;
@@ -300,8 +310,9 @@ int moe_ref_expert_apply(int H, int F, const uint8_t *w_gate, const float *s_gat
     if (hq_in) {
         memcpy(hq, hq_in, (size_t)F);
         hs = *hs_in;
+        if (hpre_out) memset(hpre_out, 0, sizeof(float) * (size_t)F);
     } else {
-        moe_ref_quant_row(h32, F, hq, &hs);
+        moe_ref_quant_row_pre(h32, F, hq, &hs, hpre_out);
     }
     if (hq_out) memcpy(hq_out, hq, (size_t)F);
     if (hs_out) *hs_out = hs;
@@ -327,7 +338,7 @@ int moe_ref_expert_ffn(const moe_ref_config *c, const float *x, int T,
                        const moe_ref_weights *rw, const int32_t *offsets,
                        const int32_t *tok, double *y_pairs, int32_t *acc_gate,
                        int32_t *acc_up, int32_t *acc_down, int8_t *hq_out, float *hs_out,
-                       const int8_t *hq_in, const float *hs_in)
+                       const int8_t *hq_in, const float *hs_in, float *hpre_out)
 {
     int rc = check_config(c);
     if (rc) return rc;
@@ -357,7 +368,8 @@ int moe_ref_expert_ffn(const moe_ref_config *c, const float *x, int T,
             acc_up ? acc_up + (size_t)p * F * GH : NULL,
             acc_down ? acc_down + (size_t)p * H * GF : NULL,
             hq_out ? hq_out + (size_t)p * F : NULL, hs_out ? hs_out + p : NULL,
-            hq_in ? hq_in + (size_t)p * F : NULL, hs_in ? hs_in + p : NULL) != 0;
+            hq_in ? hq_in + (size_t)p * F : NULL, hs_in ? hs_in + p : NULL,
+            hpre_out ? hpre_out + (size_t)p * F : NULL) != 0;
     }
     free(pe); free(xq); free(sx);
     return err ? -3 : 0;
@@ -378,7 +390,7 @@ int moe_ref_shared_ffn(const moe_ref_config *c, const float *x, int T,
     for (int t = 0; t < T; ++t)
         err |= moe_ref_expert_apply(H, F, sw->w_gate, sw->s_gate, sw->w_up, sw->s_up, sw->w_down,
                                     sw->s_down, xq + (size_t)t * H, sx[t], ys + (size_t)t * H,
-                                    NULL, NULL, NULL, NULL, NULL, NULL, NULL) != 0;
+                                    NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL) != 0;
     free(xq); free(sx);
     return err ? -3 : 0;
 }
@@ -438,7 +450,7 @@ int moe_ref_layer_forward(const moe_ref_config *c, const float *x, int T,
     if ((rc = moe_ref_route(c, x, w_router, bias, T, ids, w, keff, NULL))) goto done;
     if ((rc = moe_ref_permute(c, ids, keff, T, counts, offsets, tok, slot, uniq, &n_uniq))) goto done;
     if ((rc = moe_ref_expert_ffn(c, x, T, routed, offsets, tok, y_pairs, NULL, NULL, NULL, NULL,
-                                 NULL, NULL, NULL)))
+                                 NULL, NULL, NULL, NULL)))
         goto done;
     if (ys && (rc = moe_ref_shared_ffn(c, x, T, shared, ys))) goto done;
     rc = moe_ref_combine(c, y_pairs, slot, offsets, w, keff, T, ys, y);

@@ -84,6 +84,9 @@ int moe_ref_permute(const moe_ref_config *c, const int32_t *ids, const int32_t *
 
 /* Per-row symmetric int8 quantisation of n fp32 values: q [n], *scale. */
 void moe_ref_quant_row(const float *v, int n, int8_t *q, float *scale);
+/* The same, also writing pre [n] (nullable): the fp32 value v * (127 / amax) that each
+ * code rounds, so a test can tell how close a code lies to a rounding boundary. */
+void moe_ref_quant_row_pre(const float *v, int n, int8_t *q, float *scale, float *pre);
 
 /* int32 dot of one 64-group: sum_k (u_k - 8) * q_k for elements 64g..64g+63
  * of a packed row. */
@@ -95,24 +98,26 @@ int32_t moe_ref_group_dot(const uint8_t *row, const int8_t *q, int g);
  * Optional (nullable) probes: acc_gate/acc_up [F][H/64], acc_down [H][F/64]
  * int32 group accumulators; hq_out [F], hs_out: the quantised h.
  * hq_in/hs_in (nullable): run the down projection on this quantised h
- * instead of the one computed here. */
+ * instead of the one computed here.  hpre_out [F] (nullable): the pre-rounding
+ * value of each h code (see moe_ref_quant_row_pre; zeros when hq_in is given). */
 int moe_ref_expert_apply(int H, int F, const uint8_t *w_gate, const float *s_gate,
                          const uint8_t *w_up, const float *s_up, const uint8_t *w_down,
                          const float *s_down, const int8_t *xq, float sx, double *y,
                          int32_t *acc_gate, int32_t *acc_up, int32_t *acc_down,
                          int8_t *hq_out, float *hs_out, const int8_t *hq_in,
-                         const float *hs_in);
+                         const float *hs_in, float *hpre_out);
 
 /* Routed expert FFN over a permutation: pair p (permuted order) is token
  * tok[p] through expert e with offsets[e] <= p < offsets[e+1].
  * y_pairs [P][H] fp64.  Probes as in moe_ref_expert_apply, indexed by pair:
  * acc_gate/acc_up [P][F][H/64], acc_down [P][H][F/64], hq_out [P][F],
- * hs_out [P], hq_in [P][F], hs_in [P].  Parallel over pairs (OpenMP). */
+ * hs_out [P], hq_in [P][F], hs_in [P], hpre_out [P][F].  Parallel over pairs
+ * (OpenMP). */
 int moe_ref_expert_ffn(const moe_ref_config *c, const float *x, int T,
                        const moe_ref_weights *routed, const int32_t *offsets,
                        const int32_t *tok, double *y_pairs, int32_t *acc_gate,
                        int32_t *acc_up, int32_t *acc_down, int8_t *hq_out, float *hs_out,
-                       const int8_t *hq_in, const float *hs_in);
+                       const int8_t *hq_in, const float *hs_in, float *hpre_out);
 
 /* Shared expert over every token: ys [T][H] fp64 (weight 1). */
 int moe_ref_shared_ffn(const moe_ref_config *c, const float *x, int T,
