@@ -2,23 +2,27 @@
 
 Bars: selected expert ids, keff, per-expert token lists, unique lists and int32
 per-group accumulators exact; fp32 outputs within max-abs 1e-3 x RMS of the
-oracle's output.  The router's fp32 logits are summed in a different order on
-the two sides, so tokens whose routing decision sits within 1e-5 of a tie are
-counted and excluded from the exact checks (the tiny workload must have none).
-Downstream calls are fed the oracle's routing, never the other way round.
+oracle's output.  Where floating point decides an integer, ``parity`` compares
+what is unique and proves the rest valid: a token whose routing decision sits
+within 1e-5 of a tie must still be a valid routing under that margin (the tiny
+workload must have none), and an int8 code of h that differs from the oracle's
+must sit at a rounding boundary within a proven error bound, with its effect on
+the down accumulators and on the output accounted for exactly.  Downstream
+calls are fed the oracle's routing, never the other way round.
 """
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from helpers import tokens_within, device_experts, moe_cfg, oracle_tokens, rel_err, routing_margins
+import parity
+from helpers import device_experts, host_experts, moe_cfg, oracle_tokens, rel_err
+from parity import TIE, TOL, routing_margins
 
 pytestmark = pytest.mark.gpu
-
-TOL = 1e-3        # max-abs error relative to the oracle output's RMS
-TIE = 1e-5        # routing margin below which a token is a near tie
 
 
 @pytest.fixture(scope="module")
@@ -51,18 +55,11 @@ def _route_both(moe, wl, T, batch=0):
     return x, wr, bias, (ids.cpu().numpy(), w.cpu().numpy(), keff.cpu().numpy()), ref, margin
 
 
-def _check_routing(wl, gpu, ref, margin):
-    ids, w, keff = gpu
-    clear = margin > TIE
-    assert np.array_equal(ids[clear], ref["ids"][clear])
-    assert np.array_equal(keff[clear], ref["keff"][clear])
-    np.testing.assert_allclose(w[clear], ref["w"][clear], rtol=2e-5, atol=1e-7)
-    # near-tie tokens: the GPU's choice must still be a valid routing
-    for t in np.nonzero(~clear)[0]:
-        k = keff[t]
-        assert 1 <= k <= wl.top_k and len(set(ids[t, :k].tolist())) == k
-        assert np.all(ids[t, k:] == -1) and np.all(w[t, k:] == 0)
-    return int((~clear).sum())
+def _check_routing(wl, gpu, ref, bias):
+    """Exact routing away from ties, a valid routing under the tie margin at them."""
+    return parity.check_routing(gpu, ref["ids"], ref["w"], ref["keff"], ref["logits"],
+                                np.asarray(bias), wl.top_k, wl.top_p, wl.norm_topk_prob,
+                                wl.routed_scaling_factor)
 
 
 ROUTE_CASES = [("tiny", 16), ("tiny", 1), ("a3b_decode", 64), ("glm_decode", 1),
@@ -72,8 +69,9 @@ ROUTE_CASES = [("tiny", 16), ("tiny", 1), ("a3b_decode", 64), ("glm_decode", 1),
 @pytest.mark.parametrize("name,T", ROUTE_CASES)
 def test_route(moe, name, T):
     wl = synth.WORKLOADS[name]
-    _, _, _, gpu, ref, margin = _route_both(moe, wl, T)
-    near = _check_routing(wl, gpu, ref, margin)
+    _, _, bias, gpu, ref, margin = _route_both(moe, wl, T)
+    near = _check_routing(wl, gpu, ref, bias)
+    print("%s T=%d: %d near-tie token(s), each a valid routing" % (name, T, near))
     if name == "tiny":
         assert near == 0
     assert near <= max(1, T // 50)
@@ -86,8 +84,8 @@ def test_route_top_p_variants(moe):
                                   (0.3, 1, 1.0, 1)):
         wl = replace(base, top_p=top_p, norm_topk_prob=norm, routed_scaling_factor=scale,
                      top_k=K)
-        _, _, _, gpu, ref, margin = _route_both(moe, wl, 200)
-        assert _check_routing(wl, gpu, ref, margin) <= 4
+        _, _, bias, gpu, ref, margin = _route_both(moe, wl, 200)
+        assert _check_routing(wl, gpu, ref, bias) <= 4
 
 
 def _permute_gpu(moe, wl, ids, keff):
@@ -158,7 +156,8 @@ def test_permute_skewed_and_invalid(moe):
 
 
 def _ffn_both(moe, wl, T, batch=0, probes=True, routing=None):
-    """GPU moe_expert_ffn on the oracle's routing (or a given (ids, keff)) vs the oracle."""
+    """GPU moe_expert_ffn on the oracle's routing (or a given (ids, keff)) vs the oracle.
+    The oracle's result also carries what the h-code checks need (x, its codes, weights)."""
     x, wr, bias = _inputs(wl, T, batch)
     cfg_r = oracle.config_of(wl)
     r = oracle.route(cfg_r, x, wr, bias) if routing is None else {"ids": routing[0], "keff": routing[1]}
@@ -181,8 +180,11 @@ def _ffn_both(moe, wl, T, batch=0, probes=True, routing=None):
                        torch.tensor([perm["n_uniq"]], dtype=torch.int32, device="cuda"), y, ws,
                        probe=probe)
     torch.cuda.synchronize()
-    R_host = {k: v.numpy() for k, v in synth.gen_experts(wl).items()}
+    R_host = host_experts(wl)
     ref = oracle.expert_ffn(cfg_r, x, R_host, perm["offsets"], perm["tok"], probes=probes)
+    ref["x"] = x.numpy()
+    ref["xq"], ref["sx"] = oracle.quant_rows(x)
+    ref["experts"] = R_host
     g = {k: v.cpu().numpy() for k, v in (probe or {}).items()}
     g["y"] = y[:P].cpu().numpy()
     return g, ref, perm
@@ -193,7 +195,7 @@ def _ffn_both(moe, wl, T, batch=0, probes=True, routing=None):
 def test_expert_ffn_exact_accumulators(moe, name, T):
     wl = synth.WORKLOADS[name]
     g, ref, perm = _ffn_both(moe, wl, T)
-    _check_ffn(g, ref)
+    _check_ffn(g, ref, perm)
 
 
 @pytest.mark.parametrize("T", [24, 64])
@@ -208,7 +210,7 @@ def test_expert_ffn_exact_accumulators_row_gemv(moe, T):
     assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_ROW_GEMV
     g, ref, perm = _ffn_both(moe, wl, T)
     assert np.diff(perm["offsets"]).max() > 8
-    _check_ffn(g, ref)
+    _check_ffn(g, ref, perm)
 
 
 def test_expert_ffn_tensor_tile_edges(moe):
@@ -236,37 +238,59 @@ def test_expert_ffn_tensor_tile_edges(moe):
     g, ref, perm = _ffn_both(moe, wl, T, routing=(ids, keff))
     cnt = np.diff(perm["offsets"])
     assert cnt[0] == 129 and cnt[1] == 128 and cnt[2] >= 127 and cnt[3] >= 1 and (cnt[4:8] == 0).all()
-    _check_ffn(g, ref)
+    _check_ffn(g, ref, perm)
 
 
-def _check_ffn(g, ref):
-    assert np.array_equal(g["acc_gate"], ref["acc_gate"])
-    assert np.array_equal(g["acc_up"], ref["acc_up"])
-    # h is fp32 on both sides but summed in a different order: a code may move by one step
-    # at a rounding boundary.  Rows with identical codes must give identical down accumulators.
-    same = np.all(g["hq"] == ref["hq"], axis=1)
-    diff = np.abs(g["hq"].astype(np.int32) - ref["hq"].astype(np.int32))
-    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
-    assert same.mean() > 0.9
-    assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
-    np.testing.assert_allclose(g["h_scale"], ref["hs"], rtol=1e-5)
-    # identical codes: the outputs differ only by fp32 rounding of the scale arithmetic
-    assert rel_err(g["y"][same], ref["y_pairs"][same]) <= TOL
-    # a code one step away (h at a rounding boundary) moves the row by about one code's
-    # share, hs * |w| of a few elements out of F
-    assert rel_err(g["y"], ref["y_pairs"]) <= 20 * TOL
+def _check_ffn(g, ref, perm):
+    """Exact gate/up accumulators; every differing h code justified; down accumulators exact
+    (oracle's on matching rows, int64 brute force on the GPU's codes elsewhere); outputs within
+    1e-3 x RMS of the oracle's, moved by exactly the justified flips."""
+    return parity.check_ffn_pairs(g, ref, ref["x"], ref["experts"], perm["offsets"], perm["tok"],
+                                  ref["xq"], ref["sx"])
 
 
 def test_expert_ffn_glm_full_width(moe):
-    """Full GLM-decode widths (H=6144, F=2048) at T=4: exact gate/up accumulators."""
+    """Full GLM-decode widths (H=6144, F=2048) at T=4 (the warp GEMV)."""
     wl = synth.WORKLOADS["glm_decode"]
-    g, ref, _ = _ffn_both(moe, wl, 4)
-    assert np.array_equal(g["acc_gate"], ref["acc_gate"])
-    assert np.array_equal(g["acc_up"], ref["acc_up"])
-    same = np.all(g["hq"] == ref["hq"], axis=1)
-    assert np.array_equal(g["acc_down"][same], ref["acc_down"][same])
-    assert rel_err(g["y"][same], ref["y_pairs"][same]) <= TOL
-    assert rel_err(g["y"], ref["y_pairs"]) <= 20 * TOL
+    g, ref, perm = _ffn_both(moe, replace(wl, n_experts=48), 4)
+    _check_ffn(g, ref, perm)
+
+
+def test_expert_ffn_exact_accumulators_glm_row_gemv(moe):
+    """The benchmarked decode kernel at the shape it runs at: the row GEMV on GLM widths
+    (H=6144, F=2048) with T=32 tokens over 32 experts, so experts receive more than 8 tokens
+    and run in several token chunks ["colibri 开发演进实录" §2.2 K1b, per-group int32 dot]."""
+    wl = replace(synth.WORKLOADS["glm_decode"], n_experts=32)
+    T = 32
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_ROW_GEMV
+    g, ref, perm = _ffn_both(moe, wl, T)
+    assert np.diff(perm["offsets"]).max() > 8
+    _check_ffn(g, ref, perm)
+
+
+def test_expert_ffn_exact_accumulators_glm_tensor(moe):
+    """The tcgen05 grouped GEMM at prefill widths (H=6144, F=2048): 32 experts, 320 tokens,
+    top-2, a skewed routing in which expert 0 takes 300 tokens (two full 128-token tiles and a
+    44-token tile), expert 1 takes 257 (two full tiles and a one-token tile), and the rest
+    follow a Zipf(1.1) popularity, some with no token at all."""
+    wl = replace(synth.WORKLOADS["prefill"], n_experts=32, top_k=2)
+    T, K, E = 320, 2, 32
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_TENSOR
+    rng = np.random.default_rng(7)
+    p = 1.0 / np.arange(1, E - 1, dtype=np.float64) ** 1.1
+    p /= p.sum()
+    ids = np.empty((T, K), np.int32)
+    for t in range(T):
+        a = 0 if t < 300 else 2 + int(rng.choice(E - 2, p=p))
+        b = 1 if 20 <= t < 277 else 2 + int(rng.choice(E - 2, p=p))
+        while b == a:
+            b = 2 + int(rng.choice(E - 2, p=p))
+        ids[t] = (a, b)
+    keff = np.full(T, K, np.int32)
+    g, ref, perm = _ffn_both(moe, wl, T, routing=(ids, keff))
+    cnt = np.diff(perm["offsets"])
+    assert cnt[0] == 300 and cnt[1] == 257 and (cnt == 0).any()
+    _check_ffn(g, ref, perm)
 
 
 def _layer_gpu(moe, wl, x, wr, bias, routing=True):
@@ -283,19 +307,35 @@ def _layer_gpu(moe, wl, x, wr, bias, routing=True):
     return y.cpu().numpy(), {k: v.cpu().numpy() for k, v in rt.items()}
 
 
+def _check_layer(wl, x, wr, bias, y, rt, routed=None, shared=None, what="layer"):
+    """A layer call's routing against the oracle's (exact away from ties, valid at them) and
+    its outputs on every token away from a tie: within 1e-3 x RMS of the oracle's, or
+    explained exactly by justified h-code flips.  routed / shared: host weights (default:
+    the workload's generated experts)."""
+    cfg = oracle.config_of(wl)
+    r = oracle.route(cfg, x, wr, bias, with_logits=True)
+    near = _check_routing(wl, (rt["ids"], rt["w"], rt["keff"]), r, bias)
+    assert np.isfinite(y).all()
+    clear = routing_margins(r["logits"], bias.numpy(), wl.top_k, wl.top_p) > TIE
+    R = host_experts(wl) if routed is None else {k: np.asarray(v) for k, v in routed.items()}
+    S = None
+    if wl.n_shared:
+        S = host_experts(wl, shared=True) if shared is None else {k: np.asarray(v) for k, v in shared.items()}
+    L = parity.layer_reference(oracle, cfg, x, r["ids"], r["w"], r["keff"], R, S)
+    toks = np.nonzero(clear)[0]
+    out = parity.explain_tokens(y, L, toks, ref_rms=parity.rms(L["y"][toks]), what=what)
+    return near, out
+
+
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("a3b_decode", 64),
                                     ("a3b_decode", 128)])
 def test_layer_forward(moe, name, T):
     wl = synth.WORKLOADS[name]
     x, wr, bias = _inputs(wl, T)
     y, rt = _layer_gpu(moe, wl, x, wr, bias)
-    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
-                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
-    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
-    clear = routing_margins(logits, bias.numpy(), wl.top_k, wl.top_p) > TIE
-    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
-    assert np.isfinite(y).all()
-    tokens_within(y[clear], ref["y"][clear], TOL)
+    near, _ = _check_layer(wl, x, wr, bias, y, rt, what="%s T=%d" % (name, T))
+    if name == "tiny":
+        assert near == 0
 
 
 @pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 32, [0, 13, 31]),
@@ -311,11 +351,11 @@ def test_layer_forward_full_size_sampled(moe, name, T, sample):
     assert np.isfinite(y).all()
     ref = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)
     margin = routing_margins(ref["logits"], bias.numpy(), wl.top_k, wl.top_p)
-    _check_routing(wl, (rt["ids"], rt["w"], rt["keff"]), ref, margin)
+    _check_routing(wl, (rt["ids"], rt["w"], rt["keff"]), ref, bias)
     rows = [t for t in sample if margin[t] > TIE]
     assert rows
-    yref = oracle_tokens(wl, x.numpy()[rows], ref["ids"][rows], ref["w"][rows], ref["keff"][rows])
-    tokens_within(y[rows], yref, TOL)
+    L = oracle_tokens(wl, x.numpy()[rows], ref["ids"][rows], ref["w"][rows], ref["keff"][rows])
+    parity.explain_tokens(y[rows], L, range(len(rows)), what="%s T=%d sampled" % (name, T))
 
 
 def test_combine_with_shared(moe):
@@ -363,15 +403,9 @@ def test_edge_cases(moe, case):
     wl = synth.Workload(name, H, E, K, F, ns, Fs, (T,), norm, scale, top_p, 0.3)
     x, wr, bias = _inputs(wl, T)
     y, rt = _layer_gpu(moe, wl, x, wr, bias)
-    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias, synth.gen_experts(wl),
-                               synth.gen_experts(wl, shared=True) if ns else None)
-    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
-    clear = routing_margins(logits, bias.numpy(), K, top_p) > TIE
-    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
-    tokens_within(y[clear], ref["y"][clear], TOL)
-    g, refp, _ = _ffn_both(moe, wl, T)
-    assert np.array_equal(g["acc_gate"], refp["acc_gate"])
-    assert np.array_equal(g["acc_up"], refp["acc_up"])
+    _check_layer(wl, x, wr, bias, y, rt, what=name)
+    g, refp, perm = _ffn_both(moe, wl, T)
+    _check_ffn(g, refp, perm)
 
 
 def test_zero_tokens_and_deterministic(moe):
@@ -419,8 +453,7 @@ def test_route_lookahead(moe, name, T):
     moe.moe_route_lookahead(cfg, h.cuda(), g.cuda(), eps, wr.cuda(), bias.cuda(), ids, w, keff, ws)
     torch.cuda.synchronize()
     ref = oracle.route_lookahead(oracle.config_of(wl), h, g, eps, wr, bias, with_logits=True)
-    margin = routing_margins(ref["logits"], bias.numpy(), K, wl.top_p)
-    near = _check_routing(wl, (ids.cpu().numpy(), w.cpu().numpy(), keff.cpu().numpy()), ref, margin)
+    near = _check_routing(wl, (ids.cpu().numpy(), w.cpu().numpy(), keff.cpu().numpy()), ref, bias)
     if name == "tiny":
         assert near == 0
     assert near <= max(1, T // 50)
@@ -499,7 +532,6 @@ def test_quantize_int4_exact(moe, rows, K):
 
 def test_quantize_int4_feeds_the_layer(moe):
     # weights quantised on the GPU run through the layer exactly like the oracle's own codes
-    from dataclasses import replace
     wl = synth.WORKLOADS["tiny"]
     H, F, E = wl.hidden, wl.d_ff, wl.n_experts
     def quantised(shared):
@@ -519,14 +551,17 @@ def test_quantize_int4_feeds_the_layer(moe):
     cfg = moe_cfg(wl)
     ws = moe.alloc_workspace(cfg, T)
     y = torch.empty(T, H, device="cuda")
+    K = wl.top_k
+    rt = dict(ids=torch.empty(T, K, dtype=torch.int32, device="cuda"),
+              w=torch.empty(T, K, dtype=torch.float32, device="cuda"),
+              keff=torch.empty(T, dtype=torch.int32, device="cuda"))
     moe.moe_layer_forward(cfg, x.cuda(), wr.cuda(), bias.cuda(),
                           {k: v.cuda() for k, v in routed.items()},
-                          {k: v.cuda() for k, v in shared.items()}, y, ws)
+                          {k: v.cuda() for k, v in shared.items()}, y, ws, routing=rt)
     torch.cuda.synchronize()
-    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias, routed, shared)
-    yg = y.cpu().numpy()
-    assert np.isfinite(yg).all()
-    tokens_within(yg, ref["y"], TOL)
+    _check_layer(wl, x, wr, bias, y.cpu().numpy(), {k: v.cpu().numpy() for k, v in rt.items()},
+                 routed={k: v.numpy() for k, v in routed.items()},
+                 shared={k: v.numpy() for k, v in shared.items()}, what="quantised weights")
 
 
 def test_layer_forward_tensor_path_wider_shared_expert(moe):
@@ -538,13 +573,7 @@ def test_layer_forward_tensor_path_wider_shared_expert(moe):
     assert moe.moe_ffn_uses_tensor_cores(moe_cfg(wl), T) == 1
     x, wr, bias = _inputs(wl, T)
     y, rt = _layer_gpu(moe, wl, x, wr, bias)
-    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
-                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
-    logits = oracle.route(oracle.config_of(wl), x, wr, bias, with_logits=True)["logits"]
-    clear = routing_margins(logits, bias.numpy(), wl.top_k, wl.top_p) > TIE
-    assert np.array_equal(rt["ids"][clear], ref["ids"][clear])
-    assert np.isfinite(y).all()
-    tokens_within(y[clear], ref["y"][clear], TOL)
+    _check_layer(wl, x, wr, bias, y, rt, what="a3b, wider shared expert")
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(moe):
@@ -562,10 +591,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(moe):
     # the same context still runs a layer correctly
     x, wr, bias = _inputs(wl, 16)
     y, rt = _layer_gpu(moe, wl, x, wr, bias)
-    ref = oracle.layer_forward(oracle.config_of(wl), x, wr, bias,
-                               synth.gen_experts(wl), synth.gen_experts(wl, shared=True))
-    assert np.array_equal(rt["ids"], ref["ids"])
-    tokens_within(y, ref["y"], TOL)
+    near, _ = _check_layer(wl, x, wr, bias, y, rt, what="after a timeout")
+    assert near == 0
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("glm_decode", 8), ("a3b_decode", 128)])
