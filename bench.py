@@ -6,11 +6,13 @@ Default workload: the decode-shaped GLM-style layer (hidden 6144, 256 routed exp
 d_ff 2048, one shared expert d_ff 2048, routed_scaling_factor 2.5) at a batch of 32 tokens.
 A step is one moe_layer_forward call (router, batch-union, routed + shared expert FFN,
 combine) on a batch of synthetic tokens; the batches rotate over 5 seeded inputs so that
-the set of experts read changes from step to step.  Every step reads ~3.5 GB of expert
-weights, far above the 126 MB L2, so nothing is served from L2 across steps.
+the set of experts read changes from step to step.  Every step reads about 2 GB of expert
+weights (95 unique experts and the shared one at 21 MB each), far above the 129 MB L2, so
+nothing is served from L2 across steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--tokens T] [--no-sweep] [--no-cpu-baseline]
+                    [--workload NAME] [--tokens T] [--no-sweep] [--no-configs]
+                    [--no-cpu-baseline]
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU and its own
 batches (weak scaling, no collective on the data path); rank 0 prints the JSON line with
@@ -29,6 +31,7 @@ import sys
 import tempfile
 import threading
 import time
+from dataclasses import replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -446,6 +449,10 @@ def run_ours(args, world, rank, local):
                                  "stage_us": {k: round(v[0] / steps_b * 1e3, 1) for k, v in stb.items()}}
             del wsb, xdb, yb
 
+    configs = None
+    if not args.no_configs and rank == 0 and world == 1 and wl.name == "glm_decode":
+        configs = measure_other_configs(moe, args, dev, peak, wl, routed, shared)
+
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -469,10 +476,154 @@ def run_ours(args, world, rank, local):
     }
     if sweep:
         out["sweep"] = sweep
+    if configs:
+        out["configs"] = configs
     if lookahead:
         out["router_lookahead"] = lookahead
     if quantiser:
         out["weight_quantiser"] = quantiser
+    return out
+
+
+# --------------------------------------------------------------------------- other configs
+
+# The other layer shapes the metric is reported on, each measured in the default run:
+# (workload, batch sizes, top_p override or None).  The A3B-style layer is also routed with
+# top-p off, for the count of experts top-p saves ("MoE 路由与专家流式加载" §1.2).
+OTHER_CONFIGS = (("a3b_decode", (64,), None), ("a3b_decode", (64,), 0.0), ("prefill", (4096,), None),
+                 ("wide", (1, 8, 64, 512, 8192), None))
+L2_BYTES = 129 * 2 ** 20
+
+
+def same_experts(a: synth.Workload, b: synth.Workload) -> bool:
+    """Do two workloads draw identical expert tensors (same shapes, seed and scale range)?"""
+    return (a.hidden, a.n_experts, a.d_ff, a.d_ff_shared, a.seed, a.scale_lo, a.scale_hi) == \
+        (b.hidden, b.n_experts, b.d_ff, b.d_ff_shared, b.seed, b.scale_lo, b.scale_hi)
+
+
+def measure_layer(moe, wl, T, routed, shared, dev, steps, warmup, peak, rank=0):
+    """One layer configuration: tokens/s over `steps` timed calls (CUDA events on the launch
+    stream), the stages' device time from a second pass with stage events, the routing
+    statistics (unique experts, kept experts per token, tokens per routed expert) and the
+    roofline of the dominant FFN stage.  When one call reads less than four times the L2
+    size, L2 is flushed (a 256 MB write) before every call and each call is timed alone."""
+    cfg = moe.MoeConfig.make(wl.hidden, wl.n_experts, wl.top_k, wl.d_ff, wl.n_shared,
+                             wl.d_ff_shared, wl.norm_topk_prob, wl.routed_scaling_factor, wl.top_p)
+    wr, bias = synth.gen_router(wl)
+    wr, bias = wr.to(dev), bias.to(dev)
+    xd = [synth.gen_x(wl, T, batch=rank * N_BATCHES + b).to(dev) for b in range(N_BATCHES)]
+    ws = moe.alloc_workspace(cfg, T, device=dev)
+    y = torch.empty(T, wl.hidden, device=dev)
+    K, E = wl.top_k, wl.n_experts
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, dtype=torch.float32, device=dev)
+    keff = torch.empty(T, dtype=torch.int32, device=dev)
+    bufs = [torch.empty(n, dtype=torch.int32, device=dev) for n in (E, E + 1, T * K, T * K, E, 1)]
+    stats, keffs, tpe_max, tpe_mean = [], [], [], []
+    for x in xd:
+        moe.moe_route(cfg, x, wr, bias, ids, w, keff, ws)
+        moe.moe_permute(cfg, ids, keff, *bufs, ws)
+        cnt = bufs[0].cpu().numpy()
+        stats.append((int(bufs[5].item()), int(bufs[1][-1].item())))
+        keffs.append(float(keff.float().mean().item()))
+        tpe_max.append(int(cnt.max()))
+        tpe_mean.append(float(cnt[cnt > 0].mean()))
+    layer_bytes = float(np.mean([algorithmic_bytes(wl, T, *s)["layer"] for s in stats]))
+    flush = layer_bytes < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+
+    def run(n, flags=0):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n if flush else 1)]
+        torch.cuda.synchronize()
+        if not flush:
+            evs[0][0].record(stream)
+        for k in range(n):
+            if flush:
+                scratch.zero_()
+                evs[k][0].record(stream)
+            moe.moe_layer_forward(cfg, xd[k % N_BATCHES], wr, bias, routed, shared, y, ws, flags=flags)
+            if flush:
+                evs[k][1].record(stream)
+        if not flush:
+            evs[0][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    run(warmup)
+    ms = run(steps)
+    moe.moe_stage_times(reset=True)
+    run(steps, flags=moe.MOE_FLAG_STAGE_EVENTS)
+    st = moe.moe_stage_times(reset=True)
+    tot = {"gate_up": 0.0, "down": 0.0, "layer": 0.0}
+    fl = {"gate_up": 0.0, "down": 0.0}
+    for k in range(steps):
+        U, P = stats[k % N_BATCHES]
+        for key, v in algorithmic_bytes(wl, T, U, P).items():
+            tot[key] += v
+        for key, v in algorithmic_flops(wl, T, P).items():
+            fl[key] += v
+    dom = max(("gate_up", "down"), key=lambda s_: st[s_][0])
+    gbs = tot[dom] / (st[dom][0] / 1e3) / 1e9
+    path = {moe.MOE_FFN_WARP_GEMV: "warp GEMV", moe.MOE_FFN_TENSOR: "tcgen05 grouped GEMM",
+            moe.MOE_FFN_ROW_GEMV: "row GEMV"}.get(moe.moe_ffn_path(cfg, T), "?")
+    if moe.moe_ffn_uses_tensor_cores(cfg, T) == 1:
+        tpeak, tkind = tensor_peak()
+        tf = fl[dom] / (st[dom][0] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "ffn_" + dom, "achieved": round(tf, 1), "peak": tpeak,
+                "peak_kind": tkind, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+                "algorithmic_flops_per_launch": round(fl[dom] / steps),
+                "launch_ms": round(st[dom][0] / steps, 4), "hbm_achieved_gbs": round(gbs, 1),
+                "int8_tensor": "none on sm_103a (ptxas: tcgen05.mma .kind::i8 not supported); "
+                               "the contraction runs exactly on kind::f16"}
+    else:
+        roof = {"bound": "hbm", "kernel": "ffn_" + dom, "achieved": round(gbs, 1), "peak": peak,
+                "peak_kind": "measured", "unit": "GB/s", "frac": round(gbs / peak, 4),
+                "algorithmic_bytes_per_launch": round(tot[dom] / steps),
+                "launch_ms": round(st[dom][0] / steps, 4)}
+    return {"tokens": T, "ffn_kernel": path, "tokens_per_s": round(T * steps / (ms / 1e3), 1),
+            "us_per_layer": round(ms / steps * 1e3, 2),
+            "layer_hbm_frac": round(tot["layer"] / (ms / 1e3) / 1e9 / peak, 4),
+            "roofline": roof,
+            "stage_us": {k: round(v[0] / steps * 1e3, 1) for k, v in st.items()},
+            "unique_experts_mean": round(float(np.mean([s_[0] for s_ in stats])), 1),
+            "keff_mean": round(float(np.mean(keffs)), 3),
+            "tokens_per_routed_expert": {"mean": round(float(np.mean(tpe_mean)), 1),
+                                         "max": int(max(tpe_max))},
+            "timed_steps": steps,
+            "l2": ("flushed (256 MB write) before each call; calls timed one by one" if flush else
+                   "inputs larger than L2 (%.2f GB of expert weights per call)" % (layer_bytes / 1e9))}
+
+
+def measure_other_configs(moe, args, dev, peak, base_wl, base_routed, base_shared):
+    """Every other layer configuration of the metric, on this GPU, one after the other."""
+    out = {}
+    cache = {}
+    for name, tokens, top_p in OTHER_CONFIGS:
+        wl = synth.WORKLOADS[name]
+        if top_p is not None:
+            wl = replace(wl, top_p=top_p)
+        if same_experts(wl, base_wl):
+            routed, shared = base_routed, base_shared
+        else:
+            key = name
+            if key not in cache:
+                cache.clear()
+                torch.cuda.empty_cache()
+                cache[key] = (synth.gen_experts(wl, device=dev),
+                              synth.gen_experts(wl, shared=True, device=dev) if wl.n_shared else None)
+            routed, shared = cache[key]
+        for T in tokens:
+            steps = max(5, min(args.steps, 50 if T <= 512 else 20))
+            r = measure_layer(moe, wl, T, routed, shared, dev, steps, 3, peak)
+            if top_p is not None:
+                r["top_p"] = top_p
+                r["parity"] = "parity unpinned: the pages' fewer experts under top-p rest on trained routers"
+            label = "%s_T%d%s" % (name, T, "" if top_p is None else "_top_p_off")
+            out[label] = r
+    cache.clear()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -562,6 +713,8 @@ def main(argv=None):
     ap.add_argument("--n-experts", type=int, default=0,
                     help="override the routed expert count (for small profiling captures)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other layer configurations (A3B, prefill, wide)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -218,7 +218,9 @@ int moe_route(const moe_config *cfg, const float *x, const float *w_router, cons
  *   every batch up to T = 4096 fits; larger ones use moe_route with a workspace).
  *   The call allocates nothing.  Its first call on each device looks up the
  *   array's device address (cudaGetSymbolAddress) with that device current:
- *   make that first call before any stream capture.
+ *   make that first call before any stream capture.  The address is looked up
+ *   again when the device's current context changes (after cudaDeviceReset, for
+ *   instance); make the first call after such a reset outside stream capture too.
  *   All calls share the one array and it keeps the last call's contents; the
  *   router overwrites every scratch entry before reading it, so nothing needs
  *   clearing.  Calls that overlap on the GPU (other streams or host threads)
@@ -275,9 +277,6 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
                       const moe_expert_weights *shared, float *y, const moe_routing *routing,
                       void *workspace, size_t workspace_bytes, int flags, void *stream);
 
-/* Synchronises `stream`, then returns MOE_ERR_DEVICE if a kernel that used
- * this workspace since the last check found invalid data (see moe_permute),
- * and clears the record; MOE_OK otherwise.  Not for use inside stream capture. */
 /* moe_layer_forward on host buffers: x_host [T][H] and y_host [T][H] fp32 in
  * host memory (pinned, e.g. cudaHostAlloc, for the copies to run
  * asynchronously; pageable memory works but the copies then hold the host).
@@ -291,6 +290,10 @@ int moe_layer_forward_host(const moe_config *cfg, const float *x_host, int T,
                            float *y_host, const moe_routing *routing, void *workspace,
                            size_t workspace_bytes, int flags, void *stream);
 
+/* Synchronises `stream`, then returns MOE_ERR_DEVICE if a kernel that used
+ * this workspace since the last check found invalid data (see moe_permute),
+ * MOE_ERR_TIMEOUT if a bounded device-side wait gave up, and clears the record;
+ * MOE_OK otherwise.  Not for use inside stream capture. */
 int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream);
 
 /* Per-stage device time of the moe_layer_forward calls made on this thread

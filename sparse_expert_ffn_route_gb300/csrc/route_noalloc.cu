@@ -21,7 +21,32 @@ namespace {
 static __device__ __align__(256) float g_route_scratch[kRouteScratchFloats];
 
 std::mutex g_setup_mu;
-float *g_scratch_dev[64];   // device address of g_route_scratch, per device; null until set up
+// device address of g_route_scratch per device, and the context it was looked up in (a
+// device reset or a primary-context teardown reloads the module, so the address is looked up
+// again whenever the current context differs from the one recorded)
+float *g_scratch_dev[64];
+void *g_scratch_ctx[64];
+
+// the current driver context, through the runtime's driver entry point (no libcuda link)
+void *current_context()
+{
+    using GetCtx = int (*)(void **);
+    static std::once_flag once;
+    static GetCtx fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCtx>(p);
+        else
+            cudaGetLastError();
+    });
+    void *ctx = nullptr;
+    if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
 
 }  // namespace
 
@@ -49,15 +74,21 @@ extern "C" int moe_route_noalloc(const moe_config *cfg, const float *x, const fl
     }
     float *scratch = nullptr;
     {
-        // first call on this device: look up the array's device address with the device current
+        // first call on this device (or in a new context of it): look up the array's device
+        // address with the device current
+        void *ctx = current_context();
         std::lock_guard<std::mutex> lock(g_setup_mu);
-        if (!g_scratch_dev[dev]) {
+        if (!g_scratch_dev[dev] || g_scratch_ctx[dev] != ctx) {
             void *p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
-            if (e != cudaSuccess || p == nullptr)
+            if (e != cudaSuccess || p == nullptr) {
+                cudaGetLastError();   // leave no sticky error behind for unrelated callers
+                g_scratch_dev[dev] = nullptr;
                 return set_error(MOE_ERR_CUDA, "moe_route_noalloc: cudaGetSymbolAddress failed: %s",
                                  cudaGetErrorString(e));
+            }
             g_scratch_dev[dev] = static_cast<float *>(p);
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_dev[dev];
     }

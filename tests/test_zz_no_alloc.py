@@ -32,7 +32,10 @@ def _outputs(T, K):
             torch.full((T,), -9, dtype=torch.int32, device="cuda"))
 
 
-@pytest.mark.parametrize("name,T", [("glm_decode", 32), ("a3b_decode", 64)])
+# T <= 64 takes the cluster router (final logits [T][E] in the array); larger batches split
+# the reduction over H ([S][T][E] partial logits), up to T = 4096 at E = 256
+@pytest.mark.parametrize("name,T", [("glm_decode", 32), ("a3b_decode", 64), ("glm_decode", 512),
+                                    ("prefill", 4096)])
 def test_route_noalloc_matches_route_on_two_calls(moe, name, T):
     wl = synth.WORKLOADS[name]
     cfg = moe_cfg(wl)
