@@ -72,6 +72,8 @@ def lib():
         L.moe_ref_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp]
         L.moe_ref_topk_hits.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.moe_ref_quantize_int4.argtypes = [vp, i32, i32, vp, vp]
+        L.moe_ref_quantize_int3.argtypes = [vp, i32, i32, vp, vp]
+        L.moe_ref_dequant_int3.argtypes = [vp, vp, i32, i32, vp]
         _lib = L
     return _lib
 
@@ -147,6 +149,25 @@ def quantize_int4(w):
     scales = np.zeros((rows, K // 64), np.float32)
     _check(lib().moe_ref_quantize_int4(_p(w), rows, K, _p(packed), _p(scales)), "moe_ref_quantize_int4")
     return packed, scales
+
+
+def quantize_int3(w):
+    """fp32 weights [rows][K] -> (packed int3-g64 [rows][3K/8] u8, scales [rows][K/64] fp32)."""
+    w = _np(w, np.float32)
+    rows, K = w.shape
+    packed = np.zeros((rows, 3 * K // 8), np.uint8)
+    scales = np.zeros((rows, K // 64), np.float32)
+    _check(lib().moe_ref_quantize_int3(_p(w), rows, K, _p(packed), _p(scales)), "moe_ref_quantize_int3")
+    return packed, scales
+
+
+def dequant_int3(packed, scales):
+    """The fp32 values [rows][K] an int3-g64 matrix stands for."""
+    packed = _np(packed, np.uint8); scales = _np(scales, np.float32)
+    rows, G = scales.shape
+    out = np.zeros((rows, 64 * G), np.float32)
+    _check(lib().moe_ref_dequant_int3(_p(packed), _p(scales), rows, 64 * G, _p(out)), "moe_ref_dequant_int3")
+    return out
 
 
 def rmsnorm(x, g, eps: float):

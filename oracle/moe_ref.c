@@ -581,3 +581,83 @@ int moe_ref_quantize_int4(const float *w, int rows, int K, uint8_t *packed, floa
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Offline fp32 -> int3-g64 weight quantiser (fmt=5 of "colibri 开发演进实录"
+ * §8.3: 3-bit weights with one scale per 64-weight group).  The pages give the
+ * container, not the rule or the bit packing; the readings taken follow the
+ * int4-gs64 quantiser above with three bits:
+ *   amax  = max |w|   over the group
+ *   scale = amax / 3                  (fp32)
+ *   u     = clamp(rint(w * (3 / amax)), -3, 3) + 4   (round half to even, fp32)
+ * so value = scale * (u - 4) and u = 0 is unused; an all-zero group gets scale 0
+ * and codes 4.  Packing: a group is 24 bytes holding a 192-bit little-endian bit
+ * string, weight k of the group in bits 3k .. 3k+2 (bit b in byte b / 8, bit
+ * b % 8 of that byte, least significant first).
+ *   w [rows][K] fp32, K a multiple of 64 -> packed [rows][3K/8] u8,
+ *   scales [rows][K/64] fp32.
+ * ------------------------------------------------------------------------ */
+#define I3_GROUP_BYTES 24 /* 64 weights x 3 bits */
+
+static void put_bits3(uint8_t *grp, int k, int u)
+{
+    for (int j = 0; j < 3; ++j) {
+        const int b = 3 * k + j;
+        if ((u >> j) & 1) grp[b >> 3] |= (uint8_t)(1u << (b & 7));
+    }
+}
+
+static int get_bits3(const uint8_t *grp, int k)
+{
+    int u = 0;
+    for (int j = 0; j < 3; ++j) {
+        const int b = 3 * k + j;
+        u |= ((grp[b >> 3] >> (b & 7)) & 1) << j;
+    }
+    return u;
+}
+
+int moe_ref_quantize_int3(const float *w, int rows, int K, uint8_t *packed, float *scales)
+{
+    if (rows < 0 || K <= 0 || K % GS) return -2;
+    if (rows > 0 && (!w || !packed || !scales)) return -1;
+    const int G = K / GS;
+    for (int r = 0; r < rows; ++r) {
+        for (int g = 0; g < G; ++g) {
+            const float *v = w + (size_t)r * K + (size_t)g * GS;
+            float amax = 0.0f;
+            for (int k = 0; k < GS; ++k) {
+                const float a = fabsf(v[k]);
+                if (a > amax) amax = a;
+            }
+            const float inv = amax > 0.0f ? 3.0f / amax : 0.0f;
+            scales[(size_t)r * G + g] = amax / 3.0f;
+            uint8_t *grp = packed + ((size_t)r * G + g) * I3_GROUP_BYTES;
+            memset(grp, 0, I3_GROUP_BYTES);
+            for (int k = 0; k < GS; ++k) {
+                const float p = v[k] * inv;
+                float q = rintf(p);
+                if (q > 3.0f) q = 3.0f;
+                if (q < -3.0f) q = -3.0f;
+                put_bits3(grp, k, (int)q + 4);
+            }
+        }
+    }
+    return 0;
+}
+
+/* The values an int3-g64 matrix stands for: out[r][k] = scale(r, k/64) * (u - 4). */
+int moe_ref_dequant_int3(const uint8_t *packed, const float *scales, int rows, int K, float *out)
+{
+    if (rows < 0 || K <= 0 || K % GS) return -2;
+    if (rows > 0 && (!packed || !scales || !out)) return -1;
+    const int G = K / GS;
+    for (int r = 0; r < rows; ++r)
+        for (int g = 0; g < G; ++g) {
+            const uint8_t *grp = packed + ((size_t)r * G + g) * I3_GROUP_BYTES;
+            const float s = scales[(size_t)r * G + g];
+            for (int k = 0; k < GS; ++k)
+                out[(size_t)r * K + (size_t)g * GS + k] = s * (float)(get_bits3(grp, k) - 4);
+        }
+    return 0;
+}

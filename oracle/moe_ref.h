@@ -23,7 +23,8 @@
  *   shared    always-on shared expert added to the output
  *             ["MoE 路由与专家流式加载" §1.4]
  *   quantise  offline fp32 -> int4-gs64 weights, symmetric absmax per group
- *             ["colibri 开发演进实录" §2.1]
+ *             ["colibri 开发演进实录" §2.1], and the int3-g64 variant (fmt=5,
+ *             ibid. §8.3)
  *   lookahead RMSNorm then the router, predicting a later layer's top-K from
  *             a residual state, and the recall of such a prediction
  *             ["MoE 路由与专家流式加载" §5]
@@ -156,6 +157,15 @@ int moe_ref_topk_hits(int T, int K, const int32_t *ids_pred, const int32_t *keff
  * + 8 (fp32, round half to even); w [rows][K] -> packed [rows][K/2] (element
  * 2j low nibble) and scales [rows][K/64].  Returns -2 unless K % 64 == 0. */
 int moe_ref_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales);
+
+/* Offline fp32 -> int3-g64 weight quantiser (fmt=5, "colibri 开发演进实录" §8.3):
+ * per 64-weight group, scale = amax / 3 and u = clamp(rint(w * 3 / amax), -3, 3) + 4
+ * (fp32, round half to even); each group packs into 24 bytes, weight k in bits
+ * 3k .. 3k+2 of the group's little-endian bit string.  w [rows][K] -> packed
+ * [rows][3K/8], scales [rows][K/64].  moe_ref_dequant_int3 writes the values the
+ * codes stand for, scale * (u - 4).  Both return -2 unless K % 64 == 0. */
+int moe_ref_quantize_int3(const float *w, int rows, int K, uint8_t *packed, float *scales);
+int moe_ref_dequant_int3(const uint8_t *packed, const float *scales, int rows, int K, float *out);
 
 #ifdef __cplusplus
 }
