@@ -163,6 +163,21 @@ int moe_topk_hits(const moe_config *cfg, const int32_t *ids_pred, const int32_t 
 int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, float *scales,
                            void *stream);
 
+/* Offline weight quantiser to the 3-bit variant int3-g64 (fmt=5,
+ * "colibri 开发演进实录" §8.3: 3-bit weights with a scale per 64 weights).  The
+ * layer calls above read int4-gs64 only; this converts checkpoints to the
+ * smaller container.
+ *   w [rows][K] fp32 (device, 16-byte aligned), K a multiple of 64.
+ *   packed [rows][3K/8] u8 and scales [rows][K/64] fp32 (device, scales 4-byte
+ *   aligned), written in full: per 64-weight group, scale = amax / 3 and
+ *   u = clamp(rint(w * (3 / amax)), -3, 3) + 4 (fp32, round half to even), the
+ *   value standing for scale * (u - 4); the group's 64 codes fill 24 bytes, code k
+ *   in bits 3k .. 3k+2 of the group's little-endian bit string (bit b in byte
+ *   b / 8 at bit b % 8); an all-zero group gets scale 0 and codes 4.
+ * MOE_ERR_SHAPE for rows < 0 or a bad K.  Asynchronous on stream. */
+int moe_quantize_int3_g64(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                          void *stream);
+
 /* Diagnostic of the error path of the kernels' bounded device-side waits:
  * one CTA polls, `polls` times (1 .. 2^24), an mbarrier that nothing arrives
  * at, gives up and records the timeout in the workspace's error word exactly
@@ -174,11 +189,12 @@ int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls
 
 /* Which grouped expert-FFN kernels a call with T tokens runs (host-side, no
  * device work): 1 = the tcgen05 tensor-core grouped GEMM, 0 = the GEMV-shaped
- * kernels.  The tensor path takes batches beyond the decode route (T > 64)
- * whose matrices have hidden, d_ff and d_ff_shared in multiples of 512, when
- * the expected tokens per routed expert T*K/U (U = E*(1-(1-K/E)^T), the
- * distinct experts of uniform routing) is at least 10, or at once when hidden
- * or d_ff is under 1024.  Returns -1 for an invalid config or T < 0.
+ * kernels.  The tensor path takes layers whose matrices have hidden, d_ff and
+ * d_ff_shared in multiples of 512: on narrow ones (hidden or d_ff under 1024)
+ * every batch of 32 tokens or more, otherwise batches beyond the decode route
+ * (T > 64) whose expected tokens per routed expert T*K/U (U = E*(1-(1-K/E)^T),
+ * the distinct experts of uniform routing) is at least 10.  Returns -1 for an
+ * invalid config or T < 0.
  * ["MoE 路由与专家流式加载" §1.3: the expert FFN turns from a weight-streaming
  * GEMV into a dense contraction once tokens per expert grow.] */
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);

@@ -37,7 +37,8 @@ STAGES = ("router", "select", "permute", "plan", "quant", "gate_up", "quant_h", 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_check_errors", "moe_stage_times", "moe_last_error_string",
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
-           "moe_topk_hits", "moe_quantize_int4_gs64", "moe_selftest_wait_timeout",
+           "moe_topk_hits", "moe_quantize_int4_gs64", "moe_quantize_int3_g64",
+           "moe_selftest_wait_timeout",
            "moe_layer_forward_host", "moe_ffn_path")
 
 
@@ -104,6 +105,7 @@ def load_library():
     L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
     L.moe_quantize_int4_gs64.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.moe_quantize_int3_g64.argtypes = [vp, i32, i32, vp, vp, vp]
     L.moe_selftest_wait_timeout.argtypes = [vp, sz, i32, vp]
     L.moe_permute.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -187,6 +189,15 @@ def moe_topk_hits(cfg, ids_pred, keff_pred, ids_true, keff_true, hits, stream=No
     _check(load_library().moe_topk_hits(ctypes.byref(cfg), _ptr(ids_pred), _ptr(keff_pred),
                                          _ptr(ids_true), _ptr(keff_true), T, _ptr(hits),
                                          _stream(stream)), "moe_topk_hits")
+
+
+def moe_quantize_int3_g64(w, packed, scales, stream=None):
+    """fp32 weights w [rows][K] (K a multiple of 64) -> int3-g64: packed [rows][3K/8] uint8
+    and scales [rows][K/64] float32 (every leading dimension flattened into rows)."""
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    _check(load_library().moe_quantize_int3_g64(_ptr(w), rows, K, _ptr(packed), _ptr(scales),
+                                                 _stream(stream)), "moe_quantize_int3_g64")
 
 
 def moe_quantize_int4_gs64(w, packed, scales, stream=None):

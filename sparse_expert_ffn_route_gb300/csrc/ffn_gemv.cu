@@ -68,7 +68,13 @@ int pick_tc(int nc, int T, int K, int E, bool shared)
 
 bool ffn_use_tensor_cores(const FfnArgs &a)
 {
-    if (a.T <= kRouteClusterMaxT || !ffn_tc_supported(a)) return false;
+    if (!ffn_tc_supported(a)) return false;
+    // On narrow matrices the row GEMV's tasks are one or two stages long and its dp4a work
+    // grows with every token, so decode-route batches of kTensorMinTNarrow tokens or more
+    // take the tensor path too (A3B-style layer, T = 64, top-p 0.7: 27 unique experts of
+    // about 12 tokens each).
+    const bool narrow = a.H < 1024 || a.F < 1024;
+    if (a.T <= kRouteClusterMaxT) return narrow && a.T >= kTensorMinTNarrow;
     // Measured on GB300 (gate/up + down): a tensor-core tile pays about the same per 64-input
     // group whatever its width, while the row GEMV streams an expert's weights once per 8 of
     // its tokens.  On wide matrices the row GEMV is faster below about 10 tokens per routed
@@ -76,7 +82,7 @@ bool ffn_use_tensor_cores(const FfnArgs &a)
     // level near 10 (wide layer T=512: 5.18 vs 5.08 ms) and slower above (GLM T=512: 4.39 vs
     // 3.46 ms).  On narrow ones (hidden or d_ff under 1024) its tasks are too short and the
     // tensor path wins from the first batch past the decode route (A3B T=128: 0.092 vs 0.143 ms).
-    if (a.H < 1024 || a.F < 1024) return true;
+    if (narrow) return true;
     const double U = a.E * (1.0 - pow(1.0 - (double)a.K / a.E, (double)a.T));
     return U > 0.0 && (double)a.T * a.K / U >= 10.0;
 }
@@ -85,8 +91,8 @@ void ffn_configure(FfnArgs &a)
 {
     const bool sh = a.n_shared != 0;
     const bool small = a.T <= kRouteClusterMaxT;
-    // batches beyond the decode route: the tensor-core grouped GEMM (ffn_tc.cu)
-    a.tensor = (!small && ffn_use_tensor_cores(a)) ? 1 : 0;
+    // the tensor-core grouped GEMM (ffn_tc.cu) where ffn_use_tensor_cores takes it
+    a.tensor = ffn_use_tensor_cores(a) ? 1 : 0;
     if (a.tensor) {
         a.slice_gu = 0;
         a.slice_dn = 0;

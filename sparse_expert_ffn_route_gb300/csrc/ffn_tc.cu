@@ -10,20 +10,25 @@
 // acc += s[row][g] * A.  The token's activation scale multiplies at the end.
 //
 // Tile: 128 weight rows (one matrix of one expert) x up to 128 tokens of the expert's list;
-// one task per tile, all K groups.  Warp roles in a CTA of 14 warps:
-//   warps 0-3  one weight row each per thread: load the row's nibbles of the next groups
-//              from HBM (16-byte non-allocating loads, kNibAhead groups ahead in registers),
-//              convert them to bf16 (u - 8) and store them into the group's A buffer in TMEM.
+// one task per tile, all K groups.  Warp roles in a CTA of 16 warps:
+//   warps 0-3  one weight row each per thread: take the row's nibbles of a group from the
+//              nibble stages in shared memory, convert them to bf16 (u - 8) and store them
+//              into the group's A buffer in TMEM.
 //   warp 4     allocates TMEM; one thread issues the 4 MMAs of each group (A from TMEM, B
 //              from shared memory) and commits them to the rings' mbarriers.
 //   warp 5     loads the B tiles: the tile's activation rows (bf16 codes, laid out in
 //              output-row order, 128 bytes per row per group) by 2-D TMA with the 128-byte
 //              swizzle, one box per power-of-two part of the tile's height (a TMA instruction
-//              costs the issuing warp about a hundred cycles, so boxes are as large as the
-//              tile allows), into a ring of kBStages shared-memory stages.
+//              costs the issuing warp hundreds of cycles, so boxes are as large as the tile
+//              allows), into a ring of kBStages shared-memory stages.
 //   warps 6-13 the epilogue, two warps per 32 TMEM lanes (32 rows), 64 token columns each:
 //              per group the accumulator is loaded 16 columns at a time (the next load in
 //              flight) and added into registers with the group scale (packed fp32x2 FMAs).
+//   warp 14    loads the weight nibbles by 2-D TMA, 4 groups of the tile's 128 rows per box
+//              (16 KB, 128-byte swizzle), into a ring of kNStages stages, so the converters
+//              never wait on a global load (held in registers, as an earlier version did,
+//              a few groups ahead did not cover the memory latency under load).
+//   warp 15    idle (the block stays whole warpgroups at 128 registers a thread).
 // Groups rotate through kAStages A buffers, kBStages B stages and kDBuf accumulators, each
 // ring with a full and an empty mbarrier; warps arrive once each.  Within every run of 8
 // inputs the contraction runs in the order e0 e4 e1 e5 e2 e6 e3 e7 on both operands (the
@@ -33,6 +38,7 @@
 #include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "device_util.cuh"
@@ -49,17 +55,22 @@ constexpr int kM = 128;             // weight rows per tile (MMA M)
 constexpr int kN = 128;             // tokens per tile, at most (MMA N)
 constexpr int kGK = 64;             // inputs per group (one scale; 4 MMAs of K = 16)
 constexpr int kAStages = 4;         // A buffers in TMEM
-constexpr int kBStages = 10;        // B stages in shared memory
+constexpr int kBStages = 8;         // B stages in shared memory
 constexpr int kDBuf = 3;            // accumulators in TMEM
-constexpr int kNibAhead = 6;        // groups of nibbles held in registers ahead of use
+constexpr int kNStages = 3;         // nibble stages in shared memory (TMA-fed)
+constexpr int kNGroups = 4;         // groups per nibble stage: [128 rows][128 B], 16 KB
 constexpr int kBoxMaps = 4;         // B tensor maps with boxes of 16, 32, 64 and 128 rows
-constexpr int kWarpMma = 4, kWarpTma = 5, kWarpEpi0 = 6;
+constexpr int kWarpMma = 4, kWarpTma = 5, kWarpEpi0 = 6, kWarpNib = 14;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter, 64 token columns each
-constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;
+// warps 0-3 converters, 4 MMA, 5 B loads, 6-13 epilogue, 14 nibble loads, 15 idle (whole
+// warpgroups keep the launch at 128 registers a thread)
+constexpr int kThreads = 16 * 32;
+static_assert(kWarpNib == kWarpEpi0 + kEpiWarps, "warp layout");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;                  // kDBuf accumulators of kN columns
 constexpr uint32_t kColA = kDBuf * kN;         // kAStages A buffers of 32 columns (64 bf16)
 constexpr int kBStageBytes = kN * 128;         // 16 KB, 1024-byte aligned
+constexpr int kNStageBytes = kM * 128;         // 16 KB: 4 groups of 128 rows' nibbles
 constexpr int kSclFloats = kEpiWarps * 32 * 16;   // the epilogue's scale slots
 
 static_assert(kColA + kAStages * 32 <= kTmemCols, "TMEM budget");
@@ -126,12 +137,14 @@ struct TcShared {
     uint64_t bempty[kBStages];   // the MMAs that read the B stage are done (commit)
     uint64_t dfull[kDBuf];       // accumulator ready (commit)
     uint64_t dempty[kDBuf];      // accumulator read (one arrival per epilogue warp)
+    uint64_t nfull[kNStages];    // nibble stage landed (TMA transaction bytes)
+    uint64_t nempty[kNStages];   // nibble stage converted (one arrival per converter warp)
     uint64_t mfinal;             // every MMA of the CTA is done (commit before TMEM is freed)
     uint32_t tmem;
     int abort;
 };
 
-constexpr int kSmemBytes = 1024 /* alignment */ + kBStages * kBStageBytes + kSclFloats * 4 +
+constexpr int kSmemBytes = 1024 /* alignment */ + kBStages * kBStageBytes + kNStages * kNStageBytes + kSclFloats * 4 +
                            (int)((sizeof(TcShared) + 15) / 16 * 16) + (int)sizeof(PlanSmem);
 
 __device__ __forceinline__ bool aborted(const TcShared *sh) { return *(volatile const int *)&sh->abort != 0; }
@@ -204,6 +217,9 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, TcS
 // the B operand's tensor maps: map k has boxes of 64 columns x (16 << k) rows
 struct BMaps {
     CUtensorMap m[kBoxMaps];
+    // nibbles of [routed, shared][matrix] as [rows][row bytes] u8, boxes of 128 B x 128 rows
+    // (128-byte swizzle); matrix 0 / 1 = gate / up for gate/up, 0 = down for down
+    CUtensorMap nib[2][2];
 };
 
 template <bool GU, bool PROBE>
@@ -213,10 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     pdl_wait();
     pdl_launch_dependents();
-    // B stages on a 1024-byte boundary (128-byte swizzle atoms), the epilogue's scale slots,
-    // the control block, the plan
+    // B stages and nibble stages on 1024-byte boundaries (128-byte swizzle atoms), the
+    // epilogue's scale slots, the control block, the plan
     uint8_t *bstage = reinterpret_cast<uint8_t *>(((uintptr_t)tc_smem_raw + 1023) & ~(uintptr_t)1023);
-    float *escl = reinterpret_cast<float *>(bstage + kBStages * kBStageBytes);
+    uint8_t *nstage = bstage + kBStages * kBStageBytes;
+    float *escl = reinterpret_cast<float *>(nstage + kNStages * kNStageBytes);
     TcShared *sh = reinterpret_cast<TcShared *>(escl + kSclFloats);
     PlanSmem *ps = reinterpret_cast<PlanSmem *>(reinterpret_cast<uint8_t *>(sh) +
                                                 (sizeof(TcShared) + 15) / 16 * 16);
@@ -251,6 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh->dfull[i], 1);
             mbar_init(&sh->dempty[i], kEpiWarps);
         }
+        for (int i = 0; i < kNStages; ++i) {
+            mbar_init(&sh->nfull[i], 1);
+            mbar_init(&sh->nempty[i], 4);
+        }
         mbar_init(&sh->mfinal, 1);
         sh->abort = 0;
         fence_mbar_init();
@@ -265,65 +286,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sh->tmem;
 
     if (warp < 4) {
-        // ---------------- converters: thread i owns weight row r0 + i ---------------------
+        // ---------------- converters: thread i owns weight row r0 + i; the nibbles come from
+        // the nibble stages (4 groups each, 128-byte swizzle: 16-byte chunk c of row i sits at
+        // chunk c ^ (i & 7) of its 128-byte line) ----------------------------------------------
         const int i = tid;
-        // nibble cursor: the next group to load into registers, kNibAhead ahead of the
-        // conversion cursor, across task boundaries
-        int ntask = blockIdx.x, ng = 0, nng = 0;
-        const uint8_t *nw = nullptr;
-        auto enter_n = [&]() {
-            if (ntask < total) {
-                const TcTask t = tc_task<GU>(a, *ps, ntask);
-                nw = t.w + (size_t)i * t.rowbytes;
-                nng = t.ngroups;
-            }
-        };
-        auto next_n = [&](uint4 (&slot)[2]) {
-            if (ntask >= total) return;
-            slot[0] = ld_stream_v4(nw + ng * 32);
-            slot[1] = ld_stream_v4(nw + ng * 32 + 16);
-            if (++ng == nng) {
-                ng = 0;
-                ntask += gridDim.x;
-                enter_n();
-            }
-        };
-        enter_n();
-        uint4 nib[kNibAhead][2];
-#pragma unroll
-        for (int q = 0; q < kNibAhead; ++q) next_n(nib[q]);
-        // conversion cursor
-        int ctask = blockIdx.x, cg = 0, cng = ctask < total ? tc_task<GU>(a, *ps, ctask).ngroups : 0;
-        uint32_t it = 0;
-        while (ctask < total && !aborted(sh)) {
-#pragma unroll
-            for (int q = 0; q < kNibAhead; ++q) {
-                if (ctask >= total || aborted(sh)) break;
+        const uint32_t arow = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t it = 0;   // groups of this CTA so far
+        for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
+            const int ng = tc_task<GU>(a, *ps, task).ngroups;
+            bool ok = true;
+            for (int g = 0; g < ng; ++g, ++it) {
+                const uint32_t n = it / kNGroups, gi = it % kNGroups, ns = n % kNStages;
+                if (gi == 0 && !(ok = tc_wait_warp(&sh->nfull[ns], (n / kNStages) & 1, sh, a.err))) break;
+                const uint8_t *line = nstage + ns * kNStageBytes + i * 128;
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(line + (((2 * gi) ^ (i & 7)) << 4));
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(line + (((2 * gi + 1) ^ (i & 7)) << 4));
+                if (gi == kNGroups - 1) {
+                    // the stage is in registers: hand it back to the nibble loads (the reads
+                    // are ordered before the next TMA write into it, another proxy)
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh->nempty[ns]);
+                }
                 const uint32_t st = it % kAStages;
                 // this A buffer was last read by the MMAs of group it - kAStages
                 if (it >= kAStages) {
-                    if (!tc_wait_warp(&sh->aempty[st], ((it / kAStages) - 1) & 1, sh, a.err)) break;
+                    if (!(ok = tc_wait_warp(&sh->aempty[st], ((it / kAStages) - 1) & 1, sh, a.err))) break;
                     tc::fence_after_sync();
                 }
                 uint32_t av[32];
-                const uint32_t wv[8] = {nib[q][0].x, nib[q][0].y, nib[q][0].z, nib[q][0].w,
-                                        nib[q][1].x, nib[q][1].y, nib[q][1].z, nib[q][1].w};
+                const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                 for (int c = 0; c < 8; ++c) nibbles_to_bf16(wv[c], av + 4 * c);
-                next_n(nib[q]);   // this register slot now takes the group kNibAhead on
-                tc::st32(tmem + ((uint32_t)(warp * 32) << 16) + kColA + st * 32, av);
+                tc::st32(arow + kColA + st * 32, av);
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh->afull[st]);
-                ++it;
-                if (++cg == cng) {
-                    cg = 0;
-                    ctask += gridDim.x;
-                    cng = ctask < total ? tc_task<GU>(a, *ps, ctask).ngroups : 0;
-                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == kWarpNib) {
+        // ---------------- nibble stages by TMA: 4 groups of the tile's 128 rows per box -----
+        const uint32_t ns0 = smem_u32(nstage);
+        uint32_t n = 0;   // stages of this CTA so far
+        bool ok = true;
+        for (int task = blockIdx.x; task < total && ok && !aborted(sh); task += gridDim.x) {
+            const TcTask t = tc_task<GU>(a, *ps, task);
+            const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+            const int y = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
+            const CUtensorMap *map = &bmaps.nib[t.sh][GU ? t.m : 0];
+            for (int j = 0; j < t.ngroups / kNGroups && !aborted(sh); ++j, ++n) {
+                const uint32_t s = n % kNStages;
+                if (n >= kNStages && !(ok = tc_wait_warp(&sh->nempty[s], ((n / kNStages) - 1) & 1, sh, a.err)))
+                    break;
+                const uint32_t full = smem_u32(&sh->nfull[s]);
+                arrive_expect_tx_elect(full, kNStageBytes);
+                tma_load_2d_elect(ns0 + s * kNStageBytes, map, j * kNGroups * 32, y, full);
             }
         }
+        // copies still in flight (after a timeout elsewhere) land before the CTA exits
+        for (uint32_t j = n > (uint32_t)kNStages ? n - kNStages : 0; j < n; ++j)
+            mbar_wait(&sh->nfull[j % kNStages], (j / kNStages) & 1);
+        __syncwarp();
     } else if (warp == kWarpMma) {
         // ---------------- MMA issue: the whole warp runs the loop, one lane issues ----------
         const uint64_t bdesc0 = tc::sdesc_kmajor_sw128(smem_u32(bstage));
@@ -384,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = it > (uint32_t)kBStages ? it - kBStages : 0; j < it; ++j)
             mbar_wait(&sh->bfull[j % kBStages], (j / kBStages) & 1);
         __syncwarp();
-    } else {
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
         // ---------------- epilogue: warp reads TMEM lanes 32q .. 32q+31 (rows), token
         // columns 64h .. 64h+63 ----------------------------------------------------------
         const int q = warp & 3, half = (warp - kWarpEpi0) >> 2;
@@ -550,6 +575,22 @@ cudaError_t bf16_rows_map(CUtensorMap *m, const __nv_bfloat16 *base, int cols, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of packed nibble rows [rows][rowbytes] u8: boxes of 128 bytes (4 groups of 64
+// inputs) x 128 rows, 128-byte swizzle.
+cudaError_t nibble_rows_map(CUtensorMap *m, const uint8_t *base, int rowbytes, long long rows)
+{
+    const auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)rowbytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)rowbytes};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kM};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_tc(bool gu, const FfnArgs &a, cudaStream_t st)
@@ -559,11 +600,27 @@ cudaError_t launch_ffn_tc(bool gu, const FfnArgs &a, cudaStream_t st)
     // B operand rows = output rows of the call: the x codes laid out by launch_gather_x_bf16
     // (gate/up) or the h codes written by the h quantisation (down)
     BMaps bmaps;
+    memset(&bmaps, 0, sizeof bmaps);
     const int rows = a.plane_rows > 0 ? a.plane_rows : 1;
     cudaError_t e = cudaSuccess;
     for (int k = 0; k < kBoxMaps && e == cudaSuccess; ++k)
         e = gu ? bf16_rows_map(&bmaps.m[k], a.x_bf16, a.H, a.H, rows, 16 << k)
                : bf16_rows_map(&bmaps.m[k], a.h_bf16, a.hstride, a.hstride, rows, 16 << k);
+    // nibble maps: routed weights [E * rows][kdim / 2], shared [rows][kdim / 2]
+    for (int sh = 0; sh < 2 && e == cudaSuccess; ++sh) {
+        if (sh == 0 && !a.include_routed) continue;
+        if (sh == 1 && !a.n_shared) continue;
+        const moe_expert_weights &W = sh ? a.shared : a.routed;
+        const long long nexp = sh ? 1 : a.E;
+        if (gu) {
+            const int F = sh ? a.Fs : a.F;
+            e = nibble_rows_map(&bmaps.nib[sh][0], W.w_gate, a.H / 2, nexp * F);
+            if (e == cudaSuccess) e = nibble_rows_map(&bmaps.nib[sh][1], W.w_up, a.H / 2, nexp * F);
+        } else {
+            const int F = sh ? a.Fs : a.F;
+            e = nibble_rows_map(&bmaps.nib[sh][0], W.w_down, F / 2, nexp * a.H);
+        }
+    }
     if (e != cudaSuccess) return e;
     if (gu) {
         const int first = a.n_shared ? a.T : 0;

@@ -386,13 +386,16 @@ WsLayout ws_layout(const moe_config &c, int T)
     const size_t s_dn = (fm + 32 * kSliceChunks - 1) / (32 * kSliceChunks);
     L.h = take(rows * fm * 4);
     // gate/up planes: per-slice planes of the decode route, or one plane per matrix on the
-    // tensor-core path (batches beyond kRouteClusterMaxT)
+    // tensor-core path (batches beyond kRouteClusterMaxT, and decode-route batches of narrow
+    // layers: see ffn_use_tensor_cores)
+    const bool narrow = c.hidden < 1024 || c.d_ff < 1024;
+    const bool tensor_possible = T > kRouteClusterMaxT || (narrow && T >= kTensorMinTNarrow);
     const size_t hp_sliced = s_gu > 1 ? s_gu * rows_s * fm : 0;
-    const size_t hp_tensor = T > kRouteClusterMaxT ? rows * fm : 0;
+    const size_t hp_tensor = tensor_possible ? rows * fm : 0;
     L.hp_plane_floats = hp_sliced > hp_tensor ? hp_sliced : hp_tensor;
     L.hp = take(2 * L.hp_plane_floats * 4);
-    L.xbf = take(T > kRouteClusterMaxT ? rows * H * 2 : 0);
-    L.hbf = take(T > kRouteClusterMaxT ? rows * fm * 2 : 0);
+    L.xbf = take(tensor_possible ? rows * H * 2 : 0);
+    L.hbf = take(tensor_possible ? rows * fm * 2 : 0);
     L.hq = take(rows * fm);
     L.hscale = take(rows * 4);
     L.hcsum = take(rows * (fm / 32) * 4);
@@ -471,6 +474,22 @@ int moe_quantize_int4_gs64(const float *w, int rows, int K, uint8_t *packed, flo
     if ((rc = check_device())) return rc;
     const cudaError_t e = launch_quantize_int4(w, rows, K, packed, scales, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "weight quantiser launch");
+    return ok();
+}
+
+int moe_quantize_int3_g64(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                          void *stream)
+{
+    if (rows < 0) return fail(MOE_ERR_SHAPE, "rows must be >= 0 (got %d)", rows);
+    if (K <= 0 || K % kGroup) return fail(MOE_ERR_SHAPE, "K must be a positive multiple of 64 (got %d)", K);
+    if (rows == 0) return ok();
+    REQUIRE_PTR(w, 16);
+    REQUIRE_PTR(packed, 1);
+    REQUIRE_PTR(scales, 4);
+    int rc;
+    if ((rc = check_device())) return rc;
+    const cudaError_t e = launch_quantize_int3(w, rows, K, packed, scales, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int3 weight quantiser launch");
     return ok();
 }
 

@@ -20,6 +20,8 @@ constexpr int kMaxDim = 8192;
 // batches up to this many tokens take the decode route: cluster router (with the x
 // quantisation) and one CTA for selection, batch-union and FFN plan
 constexpr int kRouteClusterMaxT = 64;
+// decode-route batches of at least this many tokens take the tensor path on narrow matrices
+constexpr int kTensorMinTNarrow = 32;
 // the combine adds up to this many slice planes of y, so down rows are sliced only up to
 // this many 1024-input slices
 constexpr int kMaxCombinePlanes = 2;
@@ -193,6 +195,8 @@ cudaError_t launch_topk_hits(const int32_t *ids_pred, const int32_t *keff_pred,
 
 // offline fp32 -> int4-gs64 weight quantiser (quantize_weights.cu)
 cudaError_t launch_quantize_int4(const float *w, int rows, int K, uint8_t *packed, float *scales,
+                                 cudaStream_t st);
+cudaError_t launch_quantize_int3(const float *w, int rows, int K, uint8_t *packed, float *scales,
                                  cudaStream_t st);
 
 // diagnostic: one bounded wait on an mbarrier nothing arrives at (selftest.cu)

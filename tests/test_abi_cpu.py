@@ -57,7 +57,7 @@ def test_ffn_path_query(lib):
     assert [moe.moe_ffn_uses_tensor_cores(glm, t) for t in (0, 1, 64, 65, 128, 256, 512, 4096)] == \
         [0, 0, 0, 0, 0, 0, 1, 1]
     a3b = _cfg(hidden=2048, n_experts=256, top_k=8, d_ff=512, d_ff_shared=512)
-    assert [moe.moe_ffn_uses_tensor_cores(a3b, t) for t in (64, 65, 128)] == [0, 1, 1]
+    assert [moe.moe_ffn_uses_tensor_cores(a3b, t) for t in (16, 31, 32, 64, 65, 128)] == [0, 0, 1, 1, 1, 1]
     tiny = _cfg()   # d_ff = 128: GEMV kernels at every batch size
     assert [moe.moe_ffn_uses_tensor_cores(tiny, t) for t in (1, 65, 5000)] == [0, 0, 0]
     assert moe.moe_ffn_uses_tensor_cores(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 100) == 0
@@ -67,7 +67,7 @@ def test_ffn_path_query(lib):
     # 256 inputs and the batch has 8 tokens or more, the warp GEMV otherwise
     R, W, TC = moe.MOE_FFN_ROW_GEMV, moe.MOE_FFN_WARP_GEMV, moe.MOE_FFN_TENSOR
     assert [moe.moe_ffn_path(glm, t) for t in (1, 4, 7, 8, 32, 256, 512)] == [W, W, W, R, R, R, TC]
-    assert [moe.moe_ffn_path(a3b, t) for t in (64, 65)] == [R, TC]
+    assert [moe.moe_ffn_path(a3b, t) for t in (16, 64, 65)] == [R, TC, TC]
     assert [moe.moe_ffn_path(tiny, t) for t in (1, 16, 65)] == [W, W, W]
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 32) == W
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=768), 32) == R
@@ -105,6 +105,13 @@ def test_quantize_validation(lib):
     assert q(None, 4, 64, FAKE, FAKE, None) == moe.MOE_ERR_ARG
     assert q(FAKE, 4, 64, FAKE + 8, FAKE, None) == moe.MOE_ERR_ALIGN
     assert q(FAKE, 0, 64, None, None, None) == moe.MOE_OK   # nothing to do
+    q3 = lib.moe_quantize_int3_g64
+    assert q3(FAKE, -1, 64, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE
+    assert q3(FAKE, 4, 96, FAKE, FAKE, None) == moe.MOE_ERR_SHAPE
+    assert q3(None, 4, 64, FAKE, FAKE, None) == moe.MOE_ERR_ARG
+    assert q3(FAKE + 4, 4, 64, FAKE, FAKE, None) == moe.MOE_ERR_ALIGN
+    assert q3(FAKE, 4, 64, FAKE, FAKE + 2, None) == moe.MOE_ERR_ALIGN
+    assert q3(FAKE, 0, 64, None, None, None) == moe.MOE_OK
 
 
 FAKE = 1 << 20   # aligned, never dereferenced: validation fails before any use

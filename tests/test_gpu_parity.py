@@ -530,6 +530,24 @@ def test_quantize_int4_exact(moe, rows, K):
     assert np.array_equal(packed, ref_p)
 
 
+@pytest.mark.parametrize("rows,K", [(1, 64), (37, 320), (2048, 6144)])
+def test_quantize_int3_exact(moe, rows, K):
+    """int3-g64 (fmt=5, "colibri 开发演进实录" §8.3): codes and scales bit for bit."""
+    wl = synth.WORKLOADS["glm_decode"]
+    w = synth.gen_dense_weights(wl, rows, K, matrix=rows + 7)
+    if rows > 1:
+        w[1, 64:128] = 0.0                                         # an empty group
+        w[2, :64] = (torch.arange(64, dtype=torch.float32) % 7 - 3) * 0.5 + 0.25   # ties
+        w[3, :64] = -w[3, :64].abs()
+    packed = torch.full((rows, 3 * K // 8), 0xA5, dtype=torch.uint8, device="cuda")
+    scales = torch.full((rows, K // 64), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_int3_g64(w.cuda(), packed, scales)
+    torch.cuda.synchronize()
+    ref_p, ref_s = oracle.quantize_int3(w)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(packed.cpu().numpy(), ref_p)
+
+
 def test_quantize_int4_feeds_the_layer(moe):
     # weights quantised on the GPU run through the layer exactly like the oracle's own codes
     wl = synth.WORKLOADS["tiny"]
