@@ -174,17 +174,10 @@ __device__ __forceinline__ void nibbles_to_bf16(uint32_t w, uint32_t *out)
     }
 }
 
-// acc0 += s * d0, acc1 += s * d1 as one packed fp32x2 FMA (each lane rounded like fmaf);
-// s2 holds s in both halves
-__device__ __forceinline__ void ffma2(float &acc0, float &acc1, uint64_t s2, uint32_t d0, uint32_t d1)
+// acc += (s, s) * (d0, d1) as one packed fp32x2 FMA (each lane rounded like fmaf)
+__device__ __forceinline__ void ffma2(float2 &acc, float2 s2, uint32_t d0, uint32_t d1)
 {
-    asm("{\n\t.reg .b64 c, b, r;\n\t"
-        "mov.b64 c, {%0, %1};\n\t"
-        "mov.b64 b, {%2, %3};\n\t"
-        "fma.rn.f32x2 r, %4, b, c;\n\t"
-        "mov.b64 {%0, %1}, r;\n\t}"
-        : "+f"(acc0), "+f"(acc1)
-        : "r"(d0), "r"(d1), "l"(s2));
+    acc = __ffma2_rn(s2, make_float2(__uint_as_float(d0), __uint_as_float(d1)), acc);
 }
 
 // 2-D tiled TMA load of one box into shared memory, completing as transaction bytes on bar;
@@ -422,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int task = blockIdx.x; task < total && !aborted(sh); task += gridDim.x) {
             const TcTask t = tc_task<GU>(a, *ps, task);
             cp_async_wait<0>();   // the last task's scale copies (none pending otherwise)
-            float acc[64];
+            float2 acc[32];   // columns 2j, 2j + 1
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.0f, 0.0f);
             // the row's group scales, copied 8 at a time into this thread's two shared slots,
             // one block of 8 ahead (G is a multiple of 8)
             const float *srow = t.s + (size_t)i * t.G;
@@ -457,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cp_async_wait<1>();   // this block's 8 scales have landed
                 }
                 const float scl = myscl[((g >> 3) & 1) * 8 + gi];
-                const uint64_t s2 = ((uint64_t)__float_as_uint(scl) << 32) | __float_as_uint(scl);
+                const float2 s2 = make_float2(scl, scl);
                 const uint32_t buf = it % kDBuf;
                 if (!(ok = tc_wait_warp(&sh->dfull[buf], (it / kDBuf) & 1, sh, a.err))) break;
                 tc::fence_after_sync();
@@ -478,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (cb < ncols) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2) ffma2(acc[cb + j], acc[cb + j + 1], s2, ra[j], ra[j + 1]);
+                        for (int j = 0; j < 16; j += 2) ffma2(acc[(cb + j) >> 1], s2, ra[j], ra[j + 1]);
                     }
                     if (cb + 16 < ncols) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2) ffma2(acc[cb + 16 + j], acc[cb + 17 + j], s2, rb[j], rb[j + 1]);
+                        for (int j = 0; j < 16; j += 2) ffma2(acc[(cb + 16 + j) >> 1], s2, rb[j], rb[j + 1]);
                     }
                     if (PROBE) {
 #pragma unroll
@@ -514,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 64; ++j) {
                 const int jj = c0 + j;
                 const float sx = __shfl_sync(0xffffffffu, tsc[j >> 5], j & 31);
-                if (jj < t.nt) dst[(size_t)(t.rowbase + jj) * ld + t.r0 + i] = sx * acc[j];
+                const float v = (j & 1) ? acc[j >> 1].y : acc[j >> 1].x;
+                if (jj < t.nt) dst[(size_t)(t.rowbase + jj) * ld + t.r0 + i] = sx * v;
             }
         }
         cp_async_wait<0>();
