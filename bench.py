@@ -566,20 +566,21 @@ def measure_layer(moe, wl, T, routed, shared, dev, steps, warmup, peak, rank=0):
             fl[key] += v
     dom = max(("gate_up", "down"), key=lambda s_: st[s_][0])
     gbs = tot[dom] / (st[dom][0] / 1e3) / 1e9
+    traffic = recorded_traffic("ffn_" + dom, "%s_T%d" % (wl.name, T))
     path = {moe.MOE_FFN_WARP_GEMV: "warp GEMV", moe.MOE_FFN_TENSOR: "tcgen05 grouped GEMM",
             moe.MOE_FFN_ROW_GEMV: "row GEMV"}.get(moe.moe_ffn_path(cfg, T), "?")
     if moe.moe_ffn_uses_tensor_cores(cfg, T) == 1:
         tpeak, tkind = tensor_peak()
         tf = fl[dom] / (st[dom][0] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": "ffn_" + dom, "achieved": round(tf, 1), "peak": tpeak,
-                "peak_kind": tkind, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+                "peak_kind": tkind, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4), "traffic": traffic,
                 "algorithmic_flops_per_launch": round(fl[dom] / steps),
                 "launch_ms": round(st[dom][0] / steps, 4), "hbm_achieved_gbs": round(gbs, 1),
                 "int8_tensor": "none on sm_103a (ptxas: tcgen05.mma .kind::i8 not supported); "
                                "the contraction runs exactly on kind::f16"}
     else:
         roof = {"bound": "hbm", "kernel": "ffn_" + dom, "achieved": round(gbs, 1), "peak": peak,
-                "peak_kind": "measured", "unit": "GB/s", "frac": round(gbs / peak, 4),
+                "peak_kind": "measured", "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": round(tot[dom] / steps),
                 "launch_ms": round(st[dom][0] / steps, 4)}
     return {"tokens": T, "ffn_kernel": path, "tokens_per_s": round(T * steps / (ms / 1e3), 1),
