@@ -24,6 +24,12 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work on it and return; they never
  *     synchronise, except moe_layer_forward with MOE_FLAG_SYNC_CHECK.
+ *     Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous work on the stream finishes, and the router
+ *     reads w_router and bias before it waits for that work.  Weights and
+ *     bias are parameters: do not write them with the kernel enqueued just
+ *     before a call on the same stream (an event, a copy or a host sync in
+ *     between orders such a write).
  *   - Arguments are validated on the host before anything is enqueued; a bad
  *     argument returns a negative MOE_ERR_* code and enqueues nothing.
  *     moe_last_error_string() (thread-local) describes the last failure.
@@ -202,7 +208,7 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
 /* Which grouped expert-FFN kernel a call with T tokens runs (host-side, no
  * device work): MOE_FFN_TENSOR when moe_ffn_uses_tensor_cores says so;
  * otherwise MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when
- * hidden, d_ff and d_ff_shared are multiples of 256 and T >= 8, else
+ * hidden, d_ff and d_ff_shared are multiples of 256 and T >= 4, else
  * MOE_FFN_WARP_GEMV.
  * Returns -1 for an invalid config or T < 0.
  * ["colibri 开发演进实录" §2.2 K1/K1b: the integer dot both GEMV kernels run.] */

@@ -6,6 +6,16 @@
 
 namespace moe {
 
+__device__ __forceinline__ uint4 ld_stream_v4_hint(const void *p, uint64_t pol)
+{
+    // ld_stream_v4 with an L2 eviction policy (createpolicy value)
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {
     // read-only streaming load of 16 bytes that bypasses L1 allocation
@@ -216,6 +226,39 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
                  "r"(valid ? 4 : 0)
                  : "memory");
+}
+
+// The same copies with an L2 eviction policy (a createpolicy value, below).
+__device__ __forceinline__ void cp_async16_hint(void *dst, const void *src, bool valid, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(valid ? 16 : 0), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4_hint(void *dst, const void *src, bool valid, uint64_t pol)
+{
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2, %3;" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(valid ? 4 : 0), "l"(pol)
+                 : "memory");
+}
+
+// L2 eviction policies.  The last read of a weight in a launch (an expert's matrices and
+// scales by its last token chunk, the router's weights) is evict-first: the weight stream,
+// larger than L2, then displaces itself rather than the layer's small reused state
+// (activation codes, routing tables, partial sums, the kernels' code).
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

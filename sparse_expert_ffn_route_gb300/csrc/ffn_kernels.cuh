@@ -1,5 +1,5 @@
 // ffn_kernels.cuh -- the warp GEMV: grouped int4 x int8 expert FFN for few tokens per expert
-// (GEMV-shaped, HBM-bound), run for batches under 8 tokens and for reductions that are not
+// (GEMV-shaped, HBM-bound), run for batches under 4 tokens and for reductions that are not
 // multiples of 256 (the row GEMV of ffn_rows.cu takes the rest below the tensor-core
 // crossover) ["MoE 路由与专家流式加载" §1.3: gate/up/SiLU/down on the integer-dot path;
 // "colibri 开发演进实录" §2.2 K1: unsigned nibbles, dot(u - 8, q) = dot(u, q) - 8 * sum(q);
@@ -138,7 +138,7 @@ __device__ __forceinline__ int slot_of(int st, int u, int m, int c, int lane)
 // Issue the copies of one task into ring stage `st` (zero-fill outside the rows / slice).
 template <int NC, int RU, bool GU>
 __device__ __forceinline__ void issue_task(const FfnArgs &a, const Task &t, int st, uint4 *wbuf,
-                                           float *sbuf)
+                                           float *sbuf, uint64_t pol)
 {
     constexpr int NM = GU ? 2 : 1;
     const int lane = threadIdx.x & 31;
@@ -164,8 +164,8 @@ __device__ __forceinline__ void issue_task(const FfnArgs &a, const Task &t, int 
                 const bool ok = rv && li < sn;
                 const int ci = cb + (ok ? li : 0);
                 const int k = slot_of<NC, RU, NM>(st, u, m, c, lane);
-                cp_async16(wbuf + k, wm[m] + row * g.rowbytes + (size_t)ci * 16, ok);
-                cp_async4(sbuf + k, smat[m] + row * g.G + (ci >> 1), ok);
+                cp_async16_hint(wbuf + k, wm[m] + row * g.rowbytes + (size_t)ci * 16, ok, pol);
+                cp_async4_hint(sbuf + k, smat[m] + row * g.G + (ci >> 1), ok, pol);
             }
         }
     }
@@ -363,9 +363,13 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     cw.start(a, t_begin);
     Walker<GU> iw = cw;   // the next task to copy in
     int issued = t_begin;
+    // a slot's last token chunk (its chunks come in order) reads the weights for the last
+    // time in this launch: evict-first in L2
+    const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
     auto issue_next = [&](int st) {
         if (issued < t_end) {
-            issue_task<NC, RU, GU>(a, iw.t, st, wbuf, sbuf);
+            issue_task<NC, RU, GU>(a, iw.t, st, wbuf, sbuf,
+                                   iw.ntok <= iw.t.j0 + iw.tc ? pol_last : pol_again);
             if (++issued < t_end) iw.next(a);
         }
         cp_async_commit();   // possibly empty: keeps one group per task

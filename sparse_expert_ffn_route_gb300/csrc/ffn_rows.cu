@@ -128,12 +128,14 @@ __device__ __forceinline__ bool rw_wait_warp(uint64_t *bar, uint32_t parity, RwS
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
+// 3-D tiled TMA load with an L2 eviction policy (createpolicy value)
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                       uint32_t bar, uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -356,13 +358,15 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 arow = j >= 0 && j < t.nt ? act_row<GU>(a, t, j) : 0;
             }
         };
-        int task = lane == 0 ? atomicAdd(next, 1) : 0;
-        task = __shfl_sync(0xffffffffu, task, 0);
+        const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
+        // CTA b's first task is task b; the counter hands out the rest from gridDim.x on
+        const int grid = (int)gridDim.x;
+        int task = (int)blockIdx.x;
         // counter requests in flight (lane 0): the answers for tasks i+1 and, with at least
         // four tasks per CTA, i+2 (with fewer, the CTAs that start first would take them all)
-        const bool deep = total >= 4 * (int)gridDim.x;
-        int g1 = lane == 0 && task < total ? atomicAdd(next, 1) : total;
-        int g2 = lane == 0 && task < total && deep ? atomicAdd(next, 1) : total;
+        const bool deep = total >= 4 * grid;
+        int g1 = lane == 0 && task < total ? grid + atomicAdd(next, 1) : total;
+        int g2 = lane == 0 && task < total && deep ? grid + atomicAdd(next, 1) : total;
         Task t{};
         int arow = 0;
         decode(task, t, arow);
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 return false;
             }
             const int ntask = __shfl_sync(0xffffffffu, g, 0);
-            if (lane == 0 && ntask < total) g = atomicAdd(next, 1);
+            if (lane == 0 && ntask < total) g = grid + atomicAdd(next, 1);
             Task tn{};
             int narow = 0;
             decode(ntask, tn, narow);
@@ -395,8 +399,13 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             // coordinate advances with the stage)
             const CUtensorMap *map = &maps.act;
             // (gate/up: matrix m; down: the m-th 64-row block of the one matrix)
+            // z: the row coordinate of the nibble boxes (weight lanes; independent of the token
+            // rows, so those lanes' copies do not wait for the arow loads)
             int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
             const bool active = lane < 2 * NM + t.nt;
+            // weights and scales: the slot's last token chunk (the slot's chunks are taken in
+            // order) reads them for the last time in this launch, so evict-first
+            const uint64_t pol = lane < 2 * NM && ps->ntok[t.slot] <= t.j0 + kRwTok ? pol_last : pol_again;
             if (lane < NM) {
                 map = &maps.w[t.sh][GU ? lane : 0];
                 off = lane * kRwWBytes;
@@ -409,7 +418,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 dx = kRwLines * 4;
             } else {
                 off = NM * (kRwWBytes + kRwSBytes) + (lane - 2 * NM) * kRwTokBytes;
-                z = arow;
                 dy = kRwLines;
             }
             for (int s = 0; s < nst; ++s, ++k) {
@@ -433,8 +441,13 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 }
                 if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], bytes);
                 __syncwarp();
-                if (active)
-                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb);
+                // the weight and scale boxes first: they need no token row
+                if (lane < 2 * NM)
+                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb,
+                           pol);
+                else if (active)
+                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, arow,
+                           fb, pol);
             }
             task = ntask;
             t = tn;

@@ -80,10 +80,10 @@ __host__ __device__ inline Geo make_tc_geo(int kdim, int nrows, int matrices)
 constexpr int kRowBlock = 64;
 constexpr int kRowTok = 8;    // tokens per task at most
 constexpr int kRowTaskGateUp = kRowBlock, kRowTaskDown = 2 * kRowBlock;
-// Batches below this many tokens keep the warp GEMV: the row GEMV's whole-block tasks are then
-// too few per SM to hide the latency its sliced tasks hide (GLM decode layer, tokens/s, warp
-// vs row GEMV: T = 1 13.9k vs 12.8k, T = 4 26.7k vs 26.1k, T = 8 33.5k vs 35.1k).
-constexpr int kRowGemvMinT = 8;
+// Batches below this many tokens keep the warp GEMV: with 1-3 tokens the two kernels run the
+// GLM decode layer equally fast (tokens/s, warp vs row GEMV: T = 1 14.0k vs 13.8k, T = 2
+// 20.0k vs 19.8k), from 4 tokens on the row GEMV is ahead (T = 4 27.4k vs 28.5k).
+constexpr int kRowGemvMinT = 4;
 
 __host__ __device__ inline Geo make_rows_geo(int kdim, int nrows, int rows)
 {

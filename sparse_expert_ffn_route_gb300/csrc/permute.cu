@@ -23,34 +23,61 @@ namespace moe {
 
 namespace {
 
+// What the plan needs of the FFN kernels' task geometry (tasks_of / slot_cost in
+// ffn_tiles.cuh): the token chunk of a task, a power of two 2^lg, and the tasks per chunk
+// of tokens, [0] routed, [1] shared; so the device forms them with shifts.
 struct PlanParams {
     int T, n_shared, include_routed;
     int rowbase_routed;   // output row of routed pair 0
-    int tc_gu, tc_dn;
-    Geo geo_gu[2], geo_dn[2];   // [0] routed, [1] shared
+    int lg_gu, lg_dn;
+    int per_chunk_gu[2], per_chunk_dn[2];
 };
+
+// The four running sums of the plan: gate/up and down tasks, and their costs.
+struct PlanSums {
+    int gu, dn;
+    long long cgu, cdn;
+};
+__device__ __forceinline__ PlanSums operator+(const PlanSums &a, const PlanSums &b)
+{
+    return PlanSums{a.gu + b.gu, a.dn + b.dn, a.cgu + b.cgu, a.cdn + b.cdn};
+}
+__device__ __forceinline__ PlanSums operator-(const PlanSums &a, const PlanSums &b)
+{
+    return PlanSums{a.gu - b.gu, a.dn - b.dn, a.cgu - b.cgu, a.cdn - b.cdn};
+}
+__device__ __forceinline__ int shfl_up_v(int v, int off) { return __shfl_up_sync(0xffffffffu, v, off); }
+__device__ __forceinline__ PlanSums shfl_up_v(const PlanSums &v, int off)
+{
+    return PlanSums{__shfl_up_sync(0xffffffffu, v.gu, off), __shfl_up_sync(0xffffffffu, v.dn, off),
+                    __shfl_up_sync(0xffffffffu, v.cgu, off),
+                    __shfl_up_sync(0xffffffffu, v.cdn, off)};
+}
+
+// Inclusive scan over the lanes of a warp.
+template <typename V>
+__device__ __forceinline__ V warp_inclusive_scan(V v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const V o = shfl_up_v(v, off);
+        if (lane >= off) v = v + o;
+    }
+    return v;
+}
 
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).
 template <typename V>
 __device__ V block_exclusive_scan(V v, V *total, V *s_warp)
 {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-    V incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const V o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
+    const V incl = warp_inclusive_scan(v);
     if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        V w = lane < nw ? s_warp[lane] : V(0);
-        V wi = w;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const V o = __shfl_up_sync(0xffffffffu, wi, off);
-            if (lane >= off) wi += o;
-        }
+        const V w = lane < nw ? s_warp[lane] : V{};
+        const V wi = warp_inclusive_scan(w);
         if (lane < nw) s_warp[lane] = wi - w;   // exclusive prefix of warp totals
         if (lane == nw - 1) s_warp[32] = wi;
     }
@@ -61,70 +88,85 @@ __device__ V block_exclusive_scan(V v, V *total, V *s_warp)
     return res;
 }
 
-// Slot table + tile prefixes.  Reads offsets/uniq/n_uniq from global memory (written by
-// this CTA or by an earlier kernel).  Must be called by every thread of a block of at least
-// kMaxSlots threads... or any size: slots are strided.
-__device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const int32_t *uniq,
-                           const int32_t *n_uniq, FfnPlan *plan, int *s_warp)
+// One slot of the plan: its expert (-1 for a shared one), tokens and list heads, written to
+// the slot table; returns its task counts and costs.  Slots 0 .. ns-1 are the shared
+// experts (every token), then the routed experts in ascending id.
+// tasks_of and slot_cost for a chunk of 2^lg tokens and per_chunk tasks per chunk
+__device__ __forceinline__ void chunk_tasks(int per_chunk, int lg, int ntok, int &tasks,
+                                            long long &cost)
 {
-    __shared__ long long s_warp64[33];
+    tasks = 0;
+    cost = 0;
+    if (ntok <= 0) return;
+    const int tc = 1 << lg;
+    const int nch = (ntok + tc - 1) >> lg, nlast = ntok - ((nch - 1) << lg);
+    const int wlast = min(nlast <= 1 ? 1 : 1 << (32 - __clz(nlast - 1)), tc) + 3;   // task_weight
+    tasks = per_chunk * nch;
+    cost = (long long)per_chunk * ((long long)(nch - 1) * (tc + 3) + wlast);
+}
+
+__device__ __forceinline__ PlanSums plan_slot(const PlanParams &pp, int s, int e, int tokbase,
+                                              int ntok, FfnPlan *plan)
+{
+    const int sh = e < 0 ? 1 : 0;
+    plan->expert[s] = e;
+    plan->ntok[s] = ntok;
+    plan->tokbase[s] = tokbase;
+    plan->rowbase[s] = sh ? 0 : pp.rowbase_routed + tokbase;
+    PlanSums v;
+    chunk_tasks(pp.per_chunk_gu[sh], pp.lg_gu, ntok, v.gu, v.cgu);
+    chunk_tasks(pp.per_chunk_dn[sh], pp.lg_dn, ntok, v.dn, v.cdn);
+    return v;
+}
+
+__device__ __forceinline__ void plan_prefix(int s, const PlanSums &ex, FfnPlan *plan)
+{
+    plan->gu_prefix[s] = ex.gu;
+    plan->dn_prefix[s] = ex.dn;
+    plan->gu_cost[s] = ex.cgu;
+    plan->dn_cost[s] = ex.cdn;
+}
+
+// The plan's header and the totals after its last slot; zeroes the task counters.
+__device__ __forceinline__ void plan_header(int nslots, const PlanSums &tot, FfnPlan *plan)
+{
+    plan->n_slots = nslots;
+    plan_prefix(nslots, tot, plan);
+    plan->gu_tiles = tot.gu;
+    plan->dn_tiles = tot.dn;
+    plan->next[0] = plan->next[1] = 0;
+    plan->done[0] = plan->done[1] = 0;
+}
+
+// Slot table + tile prefixes by a whole block.  Reads offsets/uniq/n_uniq from global or
+// shared memory (written by this CTA or by an earlier kernel).  Slots are strided over the
+// threads; one block scan forms the four prefixes.
+__device__ void build_plan(const PlanParams &pp, const int32_t *offsets, const int32_t *uniq,
+                           const int32_t *n_uniq, FfnPlan *plan)
+{
+    __shared__ PlanSums s_ps[33];
     const int ns = pp.n_shared;
     const int nu = pp.include_routed ? *n_uniq : 0;
     const int nslots = ns + nu;
-    int base_gu = 0, base_dn = 0;
-    long long cbase_gu = 0, cbase_dn = 0;
+    PlanSums base{};
     for (int s0 = 0; s0 < nslots; s0 += blockDim.x) {
         const int s = s0 + threadIdx.x;
-        int gu = 0, dn = 0;
-        long long cgu = 0, cdn = 0;
+        PlanSums v{};
         if (s < nslots) {
-            int e, ntok, tokbase, rowbase, sh;
             if (s < ns) {
-                e = -1; ntok = pp.T; tokbase = 0; rowbase = 0; sh = 1;
+                v = plan_slot(pp, s, -1, 0, pp.T, plan);
             } else {
-                e = uniq[s - ns];
-                tokbase = offsets[e];
-                ntok = offsets[e + 1] - tokbase;
-                rowbase = pp.rowbase_routed + tokbase;
-                sh = 0;
+                const int e = uniq[s - ns];
+                const int tokbase = offsets[e];
+                v = plan_slot(pp, s, e, tokbase, offsets[e + 1] - tokbase, plan);
             }
-            plan->expert[s] = e;
-            plan->ntok[s] = ntok;
-            plan->tokbase[s] = tokbase;
-            plan->rowbase[s] = rowbase;
-            gu = tasks_of(pp.geo_gu[sh], ntok, pp.tc_gu);
-            dn = tasks_of(pp.geo_dn[sh], ntok, pp.tc_dn);
-            cgu = slot_cost(pp.geo_gu[sh], ntok, pp.tc_gu);
-            cdn = slot_cost(pp.geo_dn[sh], ntok, pp.tc_dn);
         }
-        int tot_gu, tot_dn;
-        const int ex_gu = block_exclusive_scan(gu, &tot_gu, s_warp);
-        const int ex_dn = block_exclusive_scan(dn, &tot_dn, s_warp);
-        long long ctot_gu, ctot_dn;
-        const long long cex_gu = block_exclusive_scan(cgu, &ctot_gu, s_warp64);
-        const long long cex_dn = block_exclusive_scan(cdn, &ctot_dn, s_warp64);
-        if (s < nslots) {
-            plan->gu_prefix[s] = base_gu + ex_gu;
-            plan->dn_prefix[s] = base_dn + ex_dn;
-            plan->gu_cost[s] = cbase_gu + cex_gu;
-            plan->dn_cost[s] = cbase_dn + cex_dn;
-        }
-        base_gu += tot_gu;
-        base_dn += tot_dn;
-        cbase_gu += ctot_gu;
-        cbase_dn += ctot_dn;
+        PlanSums tot;
+        const PlanSums ex = block_exclusive_scan(v, &tot, s_ps);
+        if (s < nslots) plan_prefix(s, base + ex, plan);
+        base = base + tot;
     }
-    if (threadIdx.x == 0) {
-        plan->n_slots = nslots;
-        plan->gu_prefix[nslots] = base_gu;
-        plan->dn_prefix[nslots] = base_dn;
-        plan->gu_cost[nslots] = cbase_gu;
-        plan->dn_cost[nslots] = cbase_dn;
-        plan->gu_tiles = base_gu;
-        plan->dn_tiles = base_dn;
-        plan->next[0] = plan->next[1] = 0;
-        plan->done[0] = plan->done[1] = 0;
-    }
+    if (threadIdx.x == 0) plan_header(nslots, base, plan);
 }
 
 // Shared-memory working set of the batch-union (E <= kMaxExperts).
@@ -280,10 +322,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams pp, const int32_t
                                                     const int32_t *uniq, const int32_t *n_uniq,
                                                     FfnPlan *plan)
 {
-    __shared__ int s_warp[33];
     pdl_wait();
     pdl_launch_dependents();
-    build_plan(pp, offsets, uniq, n_uniq, plan, s_warp);
+    build_plan(pp, offsets, uniq, n_uniq, plan);
 }
 
 // Batch-union of at most 1024 pairs by a block of 1024 threads, from the routing in shared
@@ -351,11 +392,139 @@ __device__ void permute_small_block(const int *s_ids, const int *s_keff, int T, 
     }
 }
 
+// Batch-union and plan of a batch of at most 256 pairs by the whole block (1024 threads, so
+// at least E + 1), in four block barriers and with short per-thread chains.  A kept pair's
+// place is its rank among the kept pairs' keys (expert << 8 | pair index): the lists come
+// out in ascending expert id and, within an expert, ascending pair index, i.e. ascending
+// token -- the order permute_small_block gives.  Same outputs as permute_small_block
+// followed by build_plan.  s_bits (kMaxExperts / 32 words) is zero on entry.
+constexpr int kSmallRouteMaxPairs = 256;
+
+struct SmallRouteSmem {
+    int *key, *sorted;    // [kSmallRouteMaxPairs]
+    unsigned *bits;       // [kMaxExperts / 32] experts present
+    int *uq, *start, *len;   // [kMaxExperts] unique experts, their list heads and lengths
+    PlanSums *ps;         // [32] warp totals of the plan scan
+};
+
+__device__ void route_small_block(const int *s_ids, const int *s_keff, int T, int K, int E,
+                                  const PermuteOut &o, int do_plan, const PlanParams &pp,
+                                  FfnPlan *plan, const SmallRouteSmem &sm)
+{
+    constexpr int kNone = 0x7fffffff;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int P = T * K, P4 = (P + 3) & ~3;
+    // keys of the kept pairs (padded to a multiple of 4 with kNone); experts present as bits
+    int key = kNone;
+    if (tid < P) {
+        const int t = tid / K, i = tid - t * K;
+        const int k = s_keff[t];
+        int bad = 0;
+        if (k < 0 || k > K) bad |= (i == 0) ? kErrBadKeff : 0;
+        if (i < max(0, min(K, k))) {
+            const int e = s_ids[tid];
+            if (e >= 0 && e < E) {
+                key = (e << 8) | tid;
+                atomicOr(&sm.bits[e >> 5], 1u << (e & 31));
+            } else {
+                bad |= kErrBadExpertId;
+            }
+        }
+        if (bad) atomicOr(o.err, bad);
+        if (o.pair_of && key == kNone) o.pair_of[tid] = -1;
+    }
+    if (tid < P4) sm.key[tid] = key;
+    __syncthreads();
+    // a kept pair's place: its rank among the keys
+    const bool valid = key != kNone;
+    if (valid) {
+        const int4 *k4 = reinterpret_cast<const int4 *>(sm.key);
+        int rank = 0;
+        for (int q = 0; q < P4 / 4; ++q) {
+            const int4 v = k4[q];
+            rank += (v.x < key ? 1 : 0) + (v.y < key ? 1 : 0) + (v.z < key ? 1 : 0) +
+                    (v.w < key ? 1 : 0);
+        }
+        sm.sorted[rank] = key >> 8;
+        o.tok[rank] = tid / K;
+        o.slot[rank] = tid;
+        if (o.pair_of) o.pair_of[tid] = rank;
+    }
+    const int nvalid = __syncthreads_count(valid);
+    // expert x: offsets[x] (kept pairs of lower experts), counts[x]; a present expert's
+    // place among the unique ones is the number of present experts below it
+    if (tid <= E) {
+        const int x = tid;
+        int lo = 0, hi = nvalid;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sm.sorted[mid] < x) lo = mid + 1;
+            else hi = mid;
+        }
+        o.offsets[x] = lo;
+        if (x < E) {
+            const unsigned word = sm.bits[x >> 5];
+            int c = 0;
+            if ((word >> (x & 31)) & 1u) {
+                int up = lo, top = nvalid;
+                while (up < top) {
+                    const int mid = (up + top) >> 1;
+                    if (sm.sorted[mid] <= x) up = mid + 1;
+                    else top = mid;
+                }
+                c = up - lo;
+                int u = __popc(word & ((1u << (x & 31)) - 1u));
+                for (int wi = 0; wi < (x >> 5); ++wi) u += __popc(sm.bits[wi]);
+                o.uniq[u] = x;
+                sm.uq[u] = x;
+                sm.start[u] = lo;
+                sm.len[u] = c;
+            }
+            o.counts[x] = c;
+        }
+    }
+    int nu = 0;
+    for (int wi = 0; wi < (E + 31) >> 5; ++wi) nu += __popc(sm.bits[wi]);
+    if (tid == 0) *o.n_uniq = nu;
+    if (!do_plan) return;
+    __syncthreads();
+    // plan: slot s by thread s; warp scans, then the warps' totals
+    const int ns = pp.n_shared;
+    const int nslots = ns + (pp.include_routed ? nu : 0);
+    PlanSums v{};
+    if (tid < nslots) {
+        if (tid < ns) v = plan_slot(pp, tid, -1, 0, pp.T, plan);
+        else v = plan_slot(pp, tid, sm.uq[tid - ns], sm.start[tid - ns], sm.len[tid - ns], plan);
+    }
+    const int nw = (nslots + 31) >> 5;
+    PlanSums incl{};
+    if (wid < nw) {
+        incl = warp_inclusive_scan(v);
+        if (lane == 31) sm.ps[wid] = incl;
+    }
+    __syncthreads();
+    if (tid < nslots) {
+        PlanSums ex = incl - v;
+        for (int w = 0; w < wid; ++w) ex = ex + sm.ps[w];
+        plan_prefix(tid, ex, plan);
+    }
+    if (tid == 0) {
+        PlanSums tot{};
+        for (int w = 0; w < nw; ++w) tot = tot + sm.ps[w];
+        plan_header(nslots, tot, plan);
+    }
+}
+
 // Decode-sized batch (T <= kRouteClusterMaxT, so T * K <= 1024 pairs): one warp per token
 // selects, then the block permutes and plans.  The routing and the lists' heads stay in
 // shared memory between the phases; the global outputs are written alongside.
-constexpr size_t kTailSmemBytes = kPermuteSmemBytes + sizeof(int) * (kRouteClusterMaxT * kMaxTopK) +
-                                  sizeof(int) * kRouteClusterMaxT + sizeof(int) * (1024 + kMaxExperts);
+// the routing arrays start on a 16-byte boundary after the batch-union's working set (the
+// small path reads keys as int4 and keeps 8-byte sums); every array below is a multiple of
+// 16 bytes long, so each starts aligned
+constexpr size_t kTailIdsOffset = (kPermuteSmemBytes + 15) & ~size_t(15);
+constexpr size_t kTailSmemBytes = kTailIdsOffset + sizeof(int) * (kRouteClusterMaxT * kMaxTopK) +
+                                  sizeof(int) * kRouteClusterMaxT + sizeof(int) * (1024 + kMaxExperts) +
+                                  sizeof(float) * kMaxExperts;
 
 __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restrict__ logits, int T,
                                                           SelectParams sp, int32_t *ids, float *w,
@@ -365,26 +534,61 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
 {
     extern __shared__ __align__(16) char tail_pool[];
     const PermuteSmem sm = carve_permute_smem(tail_pool);
-    int *s_ids = reinterpret_cast<int *>(tail_pool + kPermuteSmemBytes);
+    int *s_ids = reinterpret_cast<int *>(tail_pool + kTailIdsOffset);
     int *s_keff = s_ids + kRouteClusterMaxT * kMaxTopK;
     int *s_stage = s_keff + kRouteClusterMaxT;
     int *s_fill = s_stage + 1024;
-    pdl_wait();
-    pdl_launch_dependents();
+    float *s_bias = reinterpret_cast<float *>(s_fill + kMaxExperts);
     const int wid = threadIdx.x >> 5;
     const int E = sp.E, K = sp.K;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
+    static_assert((kRouteClusterMaxT * kMaxTopK * sizeof(int)) % 16 == 0 &&
+                      (kRouteClusterMaxT * sizeof(int)) % 16 == 0 &&
+                      (2 * kSmallRouteMaxPairs + kMaxExperts / 32) * sizeof(int) % 16 == 0 &&
+                      (2 * kSmallRouteMaxPairs + kMaxExperts / 32) * sizeof(int) +
+                              32 * sizeof(PlanSums) <= 1024 * sizeof(int),
+                  "tail shared-memory layout");
+    SmallRouteSmem srm;
+    srm.key = s_stage;
+    srm.sorted = s_stage + kSmallRouteMaxPairs;
+    srm.bits = reinterpret_cast<unsigned *>(s_stage + 2 * kSmallRouteMaxPairs);
+    srm.ps = reinterpret_cast<PlanSums *>(s_stage + 2 * kSmallRouteMaxPairs + kMaxExperts / 32);
+    srm.uq = sm.uniq;
+    srm.start = sm.base;
+    srm.len = sm.tot;
+    // the selection bias is a layer parameter, not an output of the router kernel: it is
+    // staged before the dependency wait
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_bias[e] = __ldcg(sp.bias + e);
+    if (threadIdx.x < kMaxExperts / 32) srm.bits[threadIdx.x] = 0u;
+    __syncthreads();
+    sp.bias = s_bias;
+    pdl_wait();
+    pdl_launch_dependents();
     for (int t = wid; t < T; t += 32) {
         const float *lrow = logits + (size_t)t * E;
         select_token(sp, [&](int e) { return lrow[e]; }, t, ids, w, keff, s_ids + t * K,
                      s_keff + t);
     }
     if (!do_permute) return;
+    const bool small = T * K <= kSmallRouteMaxPairs && pp.n_shared + E <= 1024;
+    if (!small)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
     __syncthreads();
+    if (small) {
+        route_small_block(s_ids, s_keff, T, K, E, o, do_plan, pp, plan, srm);
+        return;
+    }
     permute_small_block(s_ids, s_keff, T, K, E, o, sm, s_stage, s_fill);
     if (!do_plan) return;
     __syncthreads();
-    build_plan(pp, sm.off, sm.uniq, sm.nu, plan, sm.warp);
+    build_plan(pp, sm.off, sm.uniq, sm.nu, plan);
+}
+
+// log2 of a token chunk; every chunk the FFN paths configure is a power of two
+int log2_pow2(int tc)
+{
+    int lg = 0;
+    while ((1 << lg) < tc) ++lg;
+    return lg;
 }
 
 PlanParams plan_params(const FfnArgs &a)
@@ -394,11 +598,12 @@ PlanParams plan_params(const FfnArgs &a)
     pp.n_shared = a.n_shared;
     pp.include_routed = a.include_routed;
     pp.rowbase_routed = a.routed_rowbase;
-    pp.tc_gu = a.tc_gu;
-    pp.tc_dn = a.tc_dn;
+    pp.lg_gu = log2_pow2(a.tc_gu);
+    pp.lg_dn = log2_pow2(a.tc_dn);
     for (int i = 0; i < 2; ++i) {
-        pp.geo_gu[i] = a.geo_gu[i];
-        pp.geo_dn[i] = a.geo_dn[i];
+        const Geo &g = a.geo_gu[i], &d = a.geo_dn[i];
+        pp.per_chunk_gu[i] = (g.nrows + g.rb - 1) / g.rb * g.S;
+        pp.per_chunk_dn[i] = (d.nrows + d.rb - 1) / d.rb * d.S;
     }
     return pp;
 }

@@ -3,8 +3,9 @@
 // rounds of iterated argmax over the unchosen experts (ties to the lower id), optional
 // adaptive top-p over the kept gates, norm_topk_prob and routed_scaling_factor.
 //
-// Every decision is taken in fp32 with IEEE operations (__fdiv_rn, __fadd_rn, __fmul_rn):
-// given the same logits the warp reproduces the host oracle's choices and weights exactly.
+// Every decision is taken in fp32 with IEEE operations (__frcp_rn, __fdiv_rn, __fadd_rn,
+// __fmul_rn): given the same logits the warp reproduces the host oracle's choices and
+// weights exactly.
 #pragma once
 
 #include "device_util.cuh"
@@ -49,13 +50,14 @@ __device__ __forceinline__ uint32_t order_key(float v)
 // e = lane + 32j, one warp max-reduction finds the best value and one min-reduction the
 // lowest id holding it.  After the rounds lane k holds the k-th choice; top-p, the sums
 // (sequential, in the oracle's order) and the divisions then run on those lanes.
-template <typename LogitFn>
-__device__ void select_token(const SelectParams &p, LogitFn logit, int t,
-                             int32_t *__restrict__ ids, float *__restrict__ w,
-                             int32_t *__restrict__ keff, int *sm_ids = nullptr,
-                             int *sm_keff = nullptr)
+//
+// PL is the experts each lane holds (E <= 32 * PL); select_token below picks it from E.
+template <int PL, typename LogitFn>
+__device__ void select_token_pl(const SelectParams &p, LogitFn logit, int t,
+                                int32_t *__restrict__ ids, float *__restrict__ w,
+                                int32_t *__restrict__ keff, int *sm_ids, int *sm_keff)
 {
-    constexpr int kPerLane = kMaxExperts / 32;
+    constexpr int kPerLane = PL;
     constexpr unsigned kAll = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int E = p.E, K = p.K;
@@ -81,7 +83,9 @@ __device__ void select_token(const SelectParams &p, LogitFn logit, int t,
         sig[j] = 0.0f;
         key[j] = 0u;
         if (e < E) {
-            sig[j] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-lv[j])));
+            // 1 / (1 + e^-l) rounded once: the correctly rounded reciprocal is the
+            // correctly rounded quotient 1 / d
+            sig[j] = __frcp_rn(__fadd_rn(1.0f, expf(-lv[j])));
             key[j] = order_key(__fadd_rn(sig[j], bv[j]));
         }
     }
@@ -154,6 +158,18 @@ __device__ void select_token(const SelectParams &p, LogitFn logit, int t,
         if (sm_keff) *sm_keff = m;
     }
     __syncwarp();
+}
+
+template <typename LogitFn>
+__device__ __forceinline__ void select_token(const SelectParams &p, LogitFn logit, int t,
+                                             int32_t *__restrict__ ids, float *__restrict__ w,
+                                             int32_t *__restrict__ keff, int *sm_ids = nullptr,
+                                             int *sm_keff = nullptr)
+{
+    static_assert(kMaxExperts <= 32 * 16, "one warp holds at most 16 experts per lane");
+    if (p.E <= 32 * 4) select_token_pl<4>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
+    else if (p.E <= 32 * 8) select_token_pl<8>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
+    else select_token_pl<16>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
 }
 
 }  // namespace moe

@@ -64,9 +64,9 @@ def test_ffn_path_query(lib):
     assert moe.moe_ffn_uses_tensor_cores(glm, -1) == -1
     assert moe.moe_ffn_uses_tensor_cores(_cfg(top_k=9), 16) == -1
     # the kernel below the tensor path: the row GEMV when every reduction is a multiple of
-    # 256 inputs and the batch has 8 tokens or more, the warp GEMV otherwise
+    # 256 inputs and the batch has 4 tokens or more, the warp GEMV otherwise
     R, W, TC = moe.MOE_FFN_ROW_GEMV, moe.MOE_FFN_WARP_GEMV, moe.MOE_FFN_TENSOR
-    assert [moe.moe_ffn_path(glm, t) for t in (1, 4, 7, 8, 32, 256, 512)] == [W, W, W, R, R, R, TC]
+    assert [moe.moe_ffn_path(glm, t) for t in (1, 3, 4, 7, 8, 32, 256, 512)] == [W, W, R, R, R, R, R, TC]
     assert [moe.moe_ffn_path(a3b, t) for t in (16, 64, 65)] == [R, TC, TC]
     assert [moe.moe_ffn_path(tiny, t) for t in (1, 16, 65)] == [W, W, W]
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 32) == W

@@ -249,10 +249,14 @@ def _check_ffn(g, ref, perm):
                                   ref["xq"], ref["sx"])
 
 
-def test_expert_ffn_glm_full_width(moe):
-    """Full GLM-decode widths (H=6144, F=2048) at T=4 (the warp GEMV)."""
-    wl = synth.WORKLOADS["glm_decode"]
-    g, ref, perm = _ffn_both(moe, replace(wl, n_experts=48), 4)
+@pytest.mark.parametrize("T", [3, 4])
+def test_expert_ffn_glm_full_width(moe, T):
+    """Full GLM-decode widths (H=6144, F=2048) at the two sides of the warp / row GEMV
+    crossover: T=3 the warp GEMV (1024-input slices), T=4 the row GEMV."""
+    wl = replace(synth.WORKLOADS["glm_decode"], n_experts=48)
+    want = moe.MOE_FFN_WARP_GEMV if T < 4 else moe.MOE_FFN_ROW_GEMV
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == want
+    g, ref, perm = _ffn_both(moe, wl, T)
     _check_ffn(g, ref, perm)
 
 
