@@ -317,29 +317,36 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         sh->abort = 0;
         fence_mbar_init();
     }
-    pdl_wait();
+    // Early mode (gate/up with a shared expert whose x codes were written at least two
+    // launches back): the shared expert's tasks need neither the routing nor the plan, so
+    // the copy warp issues them before the dependency wait, while the route finishes; only
+    // the copy warp waits before it reads the plan.
+    const bool early = GU && a.shared_early && a.n_shared;
+    if (!early) pdl_wait();
     pdl_launch_dependents();
-    // the plan's slot table (written by the planner, which runs before this kernel)
     FfnPlan *plan = const_cast<FfnPlan *>(a.plan);
-    const int32_t *pre = GU ? plan->gu_prefix : plan->dn_prefix;
-    const int ns = plan->n_slots;
-    for (int i = threadIdx.x; i <= ns; i += blockDim.x) {
-        ps->prefix[i] = pre[i];
-        if (i < ns) {
-            ps->expert[i] = plan->expert[i];
-            ps->ntok[i] = plan->ntok[i];
-            ps->tokbase[i] = plan->tokbase[i];
-            ps->rowbase[i] = plan->rowbase[i];
+    // the plan's slot table (written by the planner, which runs before this kernel)
+    auto copy_plan = [&](int i0, int stride) {
+        const int32_t *pre = GU ? plan->gu_prefix : plan->dn_prefix;
+        const int ns = plan->n_slots;
+        for (int i = i0; i <= ns; i += stride) {
+            ps->prefix[i] = pre[i];
+            if (i < ns) {
+                ps->expert[i] = plan->expert[i];
+                ps->ntok[i] = plan->ntok[i];
+                ps->tokbase[i] = plan->tokbase[i];
+                ps->rowbase[i] = plan->rowbase[i];
+            }
         }
-    }
-    if (threadIdx.x == 0) ps->n_slots = ns;
+        if (i0 == 0) ps->n_slots = ns;
+    };
+    if (!early) copy_plan(threadIdx.x, blockDim.x);
     const float *gscale = GU ? a.xq.scale : a.hq.scale;
     const int nscale = GU ? a.T : a.plane_rows;
     const bool table = nscale <= kRwScaleTable;
     if (table)
         for (int i = threadIdx.x; i < nscale; i += blockDim.x) stab[i] = gscale[i];
     __syncthreads();
-    const int total = GU ? plan->gu_tiles : plan->dn_tiles;
     int32_t *next = &plan->next[GU ? 0 : 1];
     uint32_t k = 0;   // stages of this CTA so far
 
@@ -351,46 +358,12 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         // Lane L of the stage's one TMA instruction copies: L < NM nibbles of matrix L;
         // NM <= L < 2 NM scales of matrix L - NM; 2 NM <= L < 2 NM + nt the codes of token
         // L - 2 NM.
-        auto decode = [&](int task, Task &t, int &arow) {
-            if (task < total) {
-                t = rw_task<GU>(a, *ps, task);
-                const int j = lane - 2 * NM;
-                arow = j >= 0 && j < t.nt ? act_row<GU>(a, t, j) : 0;
-            }
-        };
         const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
-        // CTA b's first task is task b; the counter hands out the rest from gridDim.x on
-        const int grid = (int)gridDim.x;
-        int task = (int)blockIdx.x;
-        // counter requests in flight (lane 0): the answers for tasks i+1 and, with at least
-        // four tasks per CTA, i+2 (with fewer, the CTAs that start first would take them all)
-        const bool deep = total >= 4 * grid;
-        int g1 = lane == 0 && task < total ? grid + atomicAdd(next, 1) : total;
-        int g2 = lane == 0 && task < total && deep ? grid + atomicAdd(next, 1) : total;
-        Task t{};
-        int arow = 0;
-        decode(task, t, arow);
-        // Issues task `task`; g holds the answer of a request made one or two tasks ago and
-        // gets a new request.  The deep loop alternates g1 and g2, so no register waits on a
-        // request made in the same step.  False once the stop stage is issued or on a timeout.
-        auto step = [&](int &g) -> bool {
-            if (task >= total) {
-                // no more tasks: a stage without copies tells the compute warps to stop
-                const int slot = (int)(k % D);
-                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err)) return false;
-                if (lane == 0) {
-                    sh->hdr[slot].task = -1;
-                    mbar_arrive(&sh->full[slot]);
-                }
-                ++k;
-                return false;
-            }
-            const int ntask = __shfl_sync(0xffffffffu, g, 0);
-            if (lane == 0 && ntask < total) g = grid + atomicAdd(next, 1);
-            Task tn{};
-            int narow = 0;
-            decode(ntask, tn, narow);
-
+        // Issues every stage of task `task` (t; arow: this lane's token row).  `last`: the
+        // task is its slot's last token chunk (the slot's chunks are taken in order), whose
+        // weight and scale reads are the last in this launch, so evict-first.  False on a
+        // timeout.
+        auto issue = [&](int task, const Task &t, int arow, bool last) -> bool {
             const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
             const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
             const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
@@ -403,9 +376,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             // rows, so those lanes' copies do not wait for the arow loads)
             int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
             const bool active = lane < 2 * NM + t.nt;
-            // weights and scales: the slot's last token chunk (the slot's chunks are taken in
-            // order) reads them for the last time in this launch, so evict-first
-            const uint64_t pol = lane < 2 * NM && ps->ntok[t.slot] <= t.j0 + kRwTok ? pol_last : pol_again;
+            const uint64_t pol = lane < 2 * NM && last ? pol_last : pol_again;
             if (lane < NM) {
                 map = &maps.w[t.sh][GU ? lane : 0];
                 off = lane * kRwWBytes;
@@ -449,6 +420,80 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                     tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, arow,
                            fb, pol);
             }
+            return true;
+        };
+        const int grid = (int)gridDim.x;
+        // early mode: CTA b issues the shared expert's tasks b, b + grid, ... (slot 0, decoded
+        // without the plan: task = chunk * row blocks + block, as the plan numbers them)
+        int base = 0;   // the first task taken after the wait
+        bool failed = false;
+        if (early) {
+            const Geo &g = a.geo_gu[1];
+            const int nblk = (g.nrows + g.rb - 1) / g.rb;
+            base = nblk * ((a.T + kRwTok - 1) / kRwTok);
+            for (int task = (int)blockIdx.x; task < base; task += grid) {
+                Task ts{};
+                const int ch = task / nblk, blk = task - ch * nblk;
+                ts.slot = 0;
+                ts.e = -1;
+                ts.sh = 1;
+                ts.j0 = ch * kRwTok;
+                ts.nt = min(kRwTok, a.T - ts.j0);
+                ts.r0 = blk * g.rb;
+                ts.tokbase = 0;
+                ts.rowbase = ts.j0;
+                const int j = lane - 2 * NM;
+                if (!issue(task, ts, j >= 0 && j < ts.nt ? ts.j0 + j : 0, a.T <= ts.j0 + kRwTok)) {
+                    failed = true;
+                    break;
+                }
+            }
+            pdl_wait();
+            copy_plan(lane, 32);
+            __syncwarp();
+        }
+        // after a timeout no further task is taken (the stop stage below still goes out)
+        const int total = failed ? 0 : (GU ? plan->gu_tiles : plan->dn_tiles);
+        if (failed) base = 0;
+        auto decode = [&](int task, Task &t, int &arow) {
+            if (task < total) {
+                t = rw_task<GU>(a, *ps, task);
+                const int j = lane - 2 * NM;
+                arow = j >= 0 && j < t.nt ? act_row<GU>(a, t, j) : 0;
+            }
+        };
+        // CTA b's first task after the wait is task base + b; the counter hands out the rest
+        // from base + gridDim.x on
+        int task = base + (int)blockIdx.x;
+        // counter requests in flight (lane 0): the answers for tasks i+1 and, with at least
+        // four tasks per CTA, i+2 (with fewer, the CTAs that start first would take them all)
+        const bool deep = total - base >= 4 * grid;
+        int g1 = lane == 0 && task < total ? base + grid + atomicAdd(next, 1) : total;
+        int g2 = lane == 0 && task < total && deep ? base + grid + atomicAdd(next, 1) : total;
+        Task t{};
+        int arow = 0;
+        decode(task, t, arow);
+        // Issues task `task`; g holds the answer of a request made one or two tasks ago and
+        // gets a new request.  The deep loop alternates g1 and g2, so no register waits on a
+        // request made in the same step.  False once the stop stage is issued or on a timeout.
+        auto step = [&](int &g) -> bool {
+            if (task >= total) {
+                // no more tasks: a stage without copies tells the compute warps to stop
+                const int slot = (int)(k % D);
+                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err)) return false;
+                if (lane == 0) {
+                    sh->hdr[slot].task = -1;
+                    mbar_arrive(&sh->full[slot]);
+                }
+                ++k;
+                return false;
+            }
+            const int ntask = __shfl_sync(0xffffffffu, g, 0);
+            if (lane == 0 && ntask < total) g = base + grid + atomicAdd(next, 1);
+            Task tn{};
+            int narow = 0;
+            decode(ntask, tn, narow);
+            if (!issue(task, t, arow, ps->ntok[t.slot] <= t.j0 + kRwTok)) return false;
             task = ntask;
             t = tn;
             arow = narow;
@@ -507,7 +552,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             if (!ok) break;
         }
     }
-    // the last CTA to finish puts the counters back to zero for the next launch
+    // the last CTA to finish puts the counters back to zero for the next launch (after the
+    // planner, which zeroes them too: in early mode only the copy warp has waited so far)
+    if (early) pdl_wait();
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();

@@ -645,6 +645,7 @@ int moe_combine(const moe_config *cfg, const float *y_pairs, const int32_t *ids,
         a.plane_rows = T;
         a.slice_dn = 1;
         configure_ffn(a, workspace, L);
+        a.shared_early = 1;   // the plan kernel runs between the x quantisation and gate/up
         e = launch_quant_rows(x, T, cfg->hidden, cfg->hidden, a.xq, st);
         if (e == cudaSuccess) e = launch_plan(a, nullptr, nullptr, at<FfnPlan>(workspace, L.plan), st);
         if (e == cudaSuccess) e = run_ffn<StageScope>(a, T, 1, false, false, st);
@@ -725,6 +726,9 @@ int moe_layer_forward(const moe_config *cfg, const float *x, int T, const float 
     a.plane_rows = T * ns + T * cfg->top_k;
     a.slice_dn = 1;
     configure_ffn(a, workspace, L);
+    // decode route: the router kernel writes the x codes and the route tail runs between it
+    // and gate/up (the prefill route quantises x right before gate/up)
+    a.shared_early = T <= kRouteClusterMaxT ? 1 : 0;
 
     const bool ev = (flags & MOE_FLAG_STAGE_EVENTS) != 0;
     float *logits = at<float>(workspace, L.logits);

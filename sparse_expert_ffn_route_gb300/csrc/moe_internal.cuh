@@ -100,6 +100,9 @@ struct FfnArgs {
     Geo geo_gu[2], geo_dn[2];         // task geometry: [0] routed experts, [1] shared expert
     moe_ffn_probe probe;              // routed pairs only; row index = pair
     int routed_rowbase;               // output row of routed pair 0
+    // the row GEMV's gate/up may run the shared expert's tasks before its dependency wait:
+    // set only when the x codes come from a kernel at least two launches earlier
+    int shared_early;
 };
 
 // ---------------------------------------------------------------------------
