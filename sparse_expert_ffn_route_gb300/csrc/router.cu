@@ -3,12 +3,13 @@
 // ["MoE 路由与专家流式加载" §1.1, §1.2].
 //
 // Decode-sized batches (T <= kRouteClusterMaxT):
-//   router_cluster_kernel  one cluster of CS CTAs per 16 experts; CTA rank r holds the r-th
-//                          slice of H, each warp two experts x all tokens, so a lane keeps
-//                          its experts' router weights in registers and streams x (the eight
-//                          warps of a CTA read the same x slice, from L1 after the first).
-//                          The CS partial logits are summed in rank order through distributed
-//                          shared memory.  It also quantises x to int8 (the layer's activation
+//   router_cluster_kernel  up to 8 tokens: one cluster of CS CTAs per 16 experts; CTA rank r
+//                          holds the r-th slice of H, each warp two experts x all tokens, so
+//                          a lane keeps its experts' router weights in registers and streams
+//                          x from shared memory.
+//   router_tokens_kernel   more tokens: one cluster per 8 experts, tokens on the lanes (below).
+//                          Both sum the CS partial logits in rank order through distributed
+//                          shared memory and quantise x to int8 (the layer's activation
 //                          quantisation): cluster c takes tokens t = c (mod clusters), the
 //                          ranks' partial |x| maxima meet the same way.
 //   route_tail_kernel      (permute.cu) selection, batch-union and FFN plan in one CTA.
@@ -123,22 +124,100 @@ __global__ void __launch_bounds__(256, 2) router_logits_kernel(const float *__re
     }
 }
 
-// A warp of the cluster router forms XPW experts' partial logits (XPW = 1 or 2), 32 / XPW
-// tokens at a time: the 32 values of a pass are summed over the lanes by one reduce-scatter.
-// A cluster covers the 8 warps' experts.
+// A warp of router_cluster_kernel forms two experts' partial logits 16 tokens at a time: the
+// 32 values of a pass are summed over the lanes by one reduce-scatter.  A cluster covers the
+// 8 warps' 16 experts.
 constexpr int kMaxExpertsPerCluster = 16;
-constexpr int experts_per_cluster(int xpw) { return 8 * xpw; }
 constexpr int kRouteStageT = 32;   // tokens of x staged in shared memory at a time
-// Batches above this take one expert per warp: twice the clusters, and the same x slices read
-// by twice as many warps (at 32 tokens the router runs 1.3x faster; at 8 or fewer the two
-// forms time the same on a GB300).
-constexpr int kRouteXpw1MinT = 8;
+// Batches above this take router_tokens_kernel (GLM decode router + route tail, µs per call
+// on a GB300: T = 32 21.4 -> 18.8, T = 64 37.8 -> 33.5; at 8 or fewer tokens the per-expert
+// form is as fast).
+constexpr int kRouteTokensMinT = 8;
 
 size_t router_stage_bytes(int H, int cs) { return sizeof(float) * kRouteStageT * (H / cs); }
 
-// Decode-sized batches: logits of 8 * XPW experts x all T tokens per cluster, x quantisation.
-// MAXU bounds the float4 units of the H slice that one lane holds per expert.
-template <int MAXU, int XPW>
+// The end of both cluster routers, once s_part[t][j] holds this CTA's partial logits of the
+// cluster's kEPC experts over its slice of H: the |x| maxima of the tokens this cluster
+// quantises (t = c mod clusters), the logits of the tokens t = r (mod CS) summed over the
+// ranks in rank order through distributed shared memory, then the int8 codes of x.
+template <int kEPC>
+__device__ __forceinline__ void cluster_router_finish(cooperative_groups::cluster_group &cl,
+                                                      const float *__restrict__ x, int T, int H,
+                                                      int E, float *__restrict__ logits,
+                                                      const QuantRows &xq, int quant,
+                                                      float (*s_part)[kMaxExpertsPerCluster],
+                                                      float *s_amax, float *s_red)
+{
+    const int CS = (int)cl.num_blocks(), r = (int)cl.block_rank();
+    const int c = blockIdx.x / CS, ncl = gridDim.x / CS;
+    const int L = H / CS, k0 = r * L, nunit = L / 4;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    // |x| maximum of this slice for the tokens this cluster quantises
+    if (quant) {
+        for (int i = 0, t = c; t < T; ++i, t += ncl) {
+            float m = 0.0f;
+            for (int idx = tid; idx < nunit; idx += blockDim.x) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + k0 + idx * 4));
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) s_red[wid] = m;
+            __syncthreads();
+            if (tid == 0) {
+                float v = s_red[0];
+                for (int q = 1; q < 8; ++q) v = fmaxf(v, s_red[q]);
+                s_amax[i] = v;
+            }
+            __syncthreads();
+        }
+    }
+    cl.sync();
+
+    // logits of the tokens t = r (mod CS): the CS slices summed in rank order
+    const int mine = r < T ? (T - r + CS - 1) / CS : 0;
+    for (int pidx = tid; pidx < mine * kEPC; pidx += blockDim.x) {
+        const int t = r + (pidx / kEPC) * CS, j = pidx % kEPC;
+        const int e = c * kEPC + j;
+        if (e >= E) continue;
+        float sum = 0.0f;
+        for (int q = 0; q < CS; ++q) sum += *cl.map_shared_rank(&s_part[t][j], q);
+        logits[(size_t)t * E + e] = sum;
+    }
+    // int8 codes of this slice for the cluster's tokens (runs of 8 as [e0 e2 e4 e6|e1 e3 e5 e7],
+    // code sums per 32-element chunk), the row scale from rank 0
+    if (quant) {
+        for (int i = 0, t = c; t < T; ++i, t += ncl) {
+            float amax = 0.0f;
+            for (int q = 0; q < CS; ++q) amax = fmaxf(amax, *cl.map_shared_rank(&s_amax[i], q));
+            const float inv = quant_inv(amax);
+            const int runs = L / 8;
+            for (int base = 0; base < runs; base += blockDim.x) {
+                const int run = base + tid;
+                if (base + (tid & ~31) >= runs) break;   // whole warp past the end
+                int sum = 0;
+                if (run < runs) {
+                    const float *v = x + (size_t)t * H + k0 + run * 8;
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(v));
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(v + 4));
+                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    const uint2 pk = quant_pack8(xv, inv, sum);
+                    *reinterpret_cast<uint2 *>(xq.q + (size_t)t * xq.q_ld + k0 + run * 8) = pk;
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if ((lane & 3) == 0 && run < runs) xq.csum[(size_t)t * xq.c_ld + (k0 + run * 8) / 32] = sum;
+            }
+            if (r == 0 && tid == 0) xq.scale[t] = quant_scale(amax);
+        }
+    }
+    cl.sync();   // no CTA leaves while another still reads its shared memory
+}
+
+// Decode-sized batches of up to kRouteTokensMinT tokens: logits of 16 experts x all T tokens
+// per cluster, x quantisation.  MAXU bounds the float4 units of the H slice that one lane
+// holds per expert.
+template <int MAXU>
 __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__restrict__ x,
                                                                 const float *__restrict__ wr,
                                                                 int T, int H, int E,
@@ -148,13 +227,13 @@ __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__r
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     extern __shared__ __align__(16) char router_smem[];
-    constexpr int kEPC = experts_per_cluster(XPW), kTP = 32 / XPW;
+    constexpr int XPW = 2, kEPC = 8 * XPW, kTP = 32 / XPW;
     __shared__ float s_part[kRouteClusterMaxT][kMaxExpertsPerCluster];
     __shared__ float s_amax[kRouteClusterMaxT];
     __shared__ float s_red[8];
 
     const int CS = (int)cl.num_blocks(), r = (int)cl.block_rank();
-    const int c = blockIdx.x / CS, ncl = gridDim.x / CS;
+    const int c = blockIdx.x / CS;
     const int L = H / CS, k0 = r * L, nunit = L / 4;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int e0 = c * kEPC + XPW * wid;
@@ -224,66 +303,99 @@ __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__r
         }
         __syncthreads();   // before the next slice of x overwrites s_x
     }
-    // |x| maximum of this slice for the tokens this cluster quantises
-    if (quant) {
-        for (int i = 0, t = c; t < T; ++i, t += ncl) {
-            float m = 0.0f;
-            for (int idx = tid; idx < nunit; idx += blockDim.x) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + k0 + idx * 4));
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) s_red[wid] = m;
-            __syncthreads();
-            if (tid == 0) {
-                float v = s_red[0];
-                for (int q = 1; q < 8; ++q) v = fmaxf(v, s_red[q]);
-                s_amax[i] = v;
-            }
-            __syncthreads();
-        }
-    }
-    cl.sync();
+    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red);
+}
 
-    // logits of the tokens t = r (mod CS): the CS slices summed in rank order
-    const int mine = r < T ? (T - r + CS - 1) / CS : 0;
-    for (int pidx = tid; pidx < mine * kEPC; pidx += blockDim.x) {
-        const int t = r + (pidx / kEPC) * CS, j = pidx % kEPC;
-        const int e = c * kEPC + j;
-        if (e >= E) continue;
-        float sum = 0.0f;
-        for (int q = 0; q < CS; ++q) sum += *cl.map_shared_rank(&s_part[t][j], q);
-        logits[(size_t)t * E + e] = sum;
-    }
-    // int8 codes of this slice for the cluster's tokens (runs of 8 as [e0 e2 e4 e6|e1 e3 e5 e7],
-    // code sums per 32-element chunk), the row scale from rank 0
-    if (quant) {
-        for (int i = 0, t = c; t < T; ++i, t += ncl) {
-            float amax = 0.0f;
-            for (int q = 0; q < CS; ++q) amax = fmaxf(amax, *cl.map_shared_rank(&s_amax[i], q));
-            const float inv = quant_inv(amax);
-            const int runs = L / 8;
-            for (int base = 0; base < runs; base += blockDim.x) {
-                const int run = base + tid;
-                if (base + (tid & ~31) >= runs) break;   // whole warp past the end
-                int sum = 0;
-                if (run < runs) {
-                    const float *v = x + (size_t)t * H + k0 + run * 8;
-                    const float4 a = __ldg(reinterpret_cast<const float4 *>(v));
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(v + 4));
-                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    const uint2 pk = quant_pack8(xv, inv, sum);
-                    *reinterpret_cast<uint2 *>(xq.q + (size_t)t * xq.q_ld + k0 + run * 8) = pk;
-                }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if ((lane & 3) == 0 && run < runs) xq.csum[(size_t)t * xq.c_ld + (k0 + run * 8) / 32] = sum;
-            }
-            if (r == 0 && tid == 0) xq.scale[t] = quant_scale(amax);
+
+// Batches of more than kRouteTokensMinT tokens: the same clusters (CS ranks over H, 8 experts
+// per cluster), with tokens on the lanes instead.  Warp w of rank r takes the w-th eighth of
+// the rank's H slice for all 8 experts and 32 tokens at a time (lane = token): a lane reads its
+// token's x from L2 once and the experts' router weights as shared-memory broadcasts, so no
+// lane re-reads x from shared memory per expert (the per-expert form of router_cluster_kernel
+// is bound by shared-memory bandwidth there).  A lane's sum runs over its eighth in k order;
+// the eight warps' sums are added in warp order, the ranks' in rank order.
+__global__ void __launch_bounds__(256, 2) router_tokens_kernel(const float *__restrict__ x,
+                                                               const float *__restrict__ wr,
+                                                               int T, int H, int E,
+                                                               float *__restrict__ logits,
+                                                               QuantRows xq, int quant)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    constexpr int kEPC = 8;
+    extern __shared__ __align__(16) char router_smem[];
+    __shared__ float s_part[kRouteClusterMaxT][kMaxExpertsPerCluster];
+    __shared__ float s_tp[8][32][kEPC + 1];   // the warps' partial sums (padded rows)
+    __shared__ float s_amax[kRouteClusterMaxT];
+    __shared__ float s_red[8];
+
+    const int CS = (int)cl.num_blocks(), r = (int)cl.block_rank();
+    const int c = blockIdx.x / CS;
+    const int L = H / CS, k0 = r * L;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int e0 = c * kEPC;
+    const int nq = L / 32;           // float4 units of a warp's eighth of the slice
+    const int kw = wid * (L / 8);    // its first element within the slice
+
+    // the cluster's router weights for this slice, [expert][L] in shared memory; a layer
+    // parameter, so copied (evict-first in L2: read once per call) before the dependency wait
+    float4 *s_w = reinterpret_cast<float4 *>(router_smem);
+    {
+        const uint64_t pol = l2_policy_evict_first();
+        const int units = L / 4;
+        for (int idx = tid; idx < kEPC * units; idx += blockDim.x) {
+            const int j = idx / units, u = idx - j * units;
+            const int e = e0 + j;
+            cp_async16_hint(s_w + idx, wr + (size_t)(e < E ? e : 0) * H + k0 + u * 4, e < E, pol);
         }
+        cp_async_commit();
     }
-    cl.sync();   // no CTA leaves while another still reads its shared memory
+    pdl_wait();
+    pdl_launch_dependents();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    const float4 *sw = s_w + kw / 4;
+    for (int t0 = 0; t0 < T; t0 += 32) {
+        const int t = t0 + lane;
+        const bool tv = t < T;
+        const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)(tv ? t : 0) * H + k0 + kw);
+        float acc[kEPC];
+#pragma unroll
+        for (int j = 0; j < kEPC; ++j) acc[j] = 0.0f;
+        for (int q0 = 0; q0 < nq; q0 += 8) {
+            float4 xv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                xv[i] = tv && q0 + i < nq ? __ldg(xr + q0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (q0 + i < nq) {
+#pragma unroll
+                    for (int j = 0; j < kEPC; ++j) {
+                        const float4 w4 = sw[j * (L / 4) + q0 + i];
+                        acc[j] = fmaf(xv[i].x, w4.x, acc[j]);
+                        acc[j] = fmaf(xv[i].y, w4.y, acc[j]);
+                        acc[j] = fmaf(xv[i].z, w4.z, acc[j]);
+                        acc[j] = fmaf(xv[i].w, w4.w, acc[j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kEPC; ++j) s_tp[wid][lane][j] = acc[j];
+        __syncthreads();
+        {
+            // thread (token tok, expert j): the eight warps' sums in warp order
+            const int tok = tid >> 3, j = tid & 7;
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) sum += s_tp[w][tok][j];
+            if (t0 + tok < T) s_part[t0 + tok][j] = sum;
+        }
+        __syncthreads();   // before the next pass overwrites s_tp
+    }
+    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red);
 }
 
 __global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ part, int S,
@@ -337,25 +449,24 @@ cudaError_t launch_router_logits(const moe_config &c, const float *x, const floa
     if (T <= kRouteClusterMaxT) {
         const int cs = route_cluster_size(H);
         const int units = (H / cs / 4 + 31) / 32;   // float4 units per lane and expert
-        // one expert per warp (twice the clusters) once a warp's pass holds enough tokens
-        const int xpw = T > kRouteXpw1MinT ? 1 : 2;
-        const int epc = 8 * xpw;
-        const dim3 grid(cs * ((E + epc - 1) / epc));
         const QuantRows q = xq ? *xq : QuantRows{};
         const int quant = xq ? 1 : 0;
+        // tokens on the lanes once a pass holds enough of them
+        if (T > kRouteTokensMinT) {
+            const dim3 grid(cs * ((E + 7) / 8));
+            const size_t smem = sizeof(float) * 8 * (H / cs);
+            return launch_kernel(router_tokens_kernel, grid, dim3(256), smem, st, cs, x, wr, T, H, E,
+                                 scratch, q, quant);
+        }
+        const dim3 grid(cs * ((E + 15) / 16));
         const size_t smem = router_stage_bytes(H, cs);
         auto go = [&](auto kernel) {
             return launch_kernel(kernel, grid, dim3(256), smem, st, cs, x, wr, T, H, E, scratch,
                                  q, quant);
         };
-        if (xpw == 1) {
-            if (units <= 2) return go(router_cluster_kernel<2, 1>);
-            if (units <= 4) return go(router_cluster_kernel<4, 1>);
-            return go(router_cluster_kernel<8, 1>);
-        }
-        if (units <= 2) return go(router_cluster_kernel<2, 2>);
-        if (units <= 4) return go(router_cluster_kernel<4, 2>);
-        return go(router_cluster_kernel<8, 2>);
+        if (units <= 2) return go(router_cluster_kernel<2>);
+        if (units <= 4) return go(router_cluster_kernel<4>);
+        return go(router_cluster_kernel<8>);
     }
     const int S = router_splits(c, T);
     *splits = S;
