@@ -86,8 +86,31 @@ struct Walker {
             else hi = mid;
         }
         enter(a, lo);
-        // local index = (chunk * S + slice) * nblk + block
-        const int local = task - prefix[lo];
+        locate(task - prefix[lo]);
+    }
+
+    // Task `task` of the shared expert, slot 0, without the plan: every token, list head 0,
+    // output rows from 0.  Walking stays inside the slot (next() is only called while
+    // another task of the range follows).
+    __device__ void start_shared(const FfnArgs &a, int task)
+    {
+        tc = GU ? a.tc_gu : a.tc_dn;
+        t.slot = 0;
+        t.e = -1;
+        t.sh = 1;
+        const Geo &g = GU ? a.geo_gu[1] : a.geo_dn[1];
+        rb = g.rb;
+        nblk = (g.nrows + g.rb - 1) / g.rb;
+        S = g.S;
+        ntok = a.T;
+        t.tokbase = 0;
+        t.rowbase = 0;
+        locate(task);
+    }
+
+    // the slot's local task index = (chunk * S + slice) * nblk + block
+    __device__ __forceinline__ void locate(int local)
+    {
         const int cs = local / nblk;
         blk = local - cs * nblk;
         const int ch = cs / S;
@@ -341,7 +364,8 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     constexpr int D = ring_depth<NC, RU, GU>();
     constexpr int SL = ring_slots<NC, RU, GU>();
     extern __shared__ uint4 ffn_ring[];
-    pdl_wait();
+    const bool early = GU && a.shared_early && a.n_shared;
+    if (!early) pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     uint4 *wbuf = ffn_ring + (size_t)wid * D * SL * 32;
@@ -350,92 +374,106 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
 
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    const int n_slots = a.plan->n_slots;
-    const long long C = (GU ? a.plan->gu_cost : a.plan->dn_cost)[n_slots];
-    if (C <= 0) return;
-    const int t_begin = task_at<GU>(a, C * gw / nw);
-    const int t_end = gw + 1 == nw ? (GU ? a.plan->gu_tiles : a.plan->dn_tiles)
-                                   : task_at<GU>(a, C * (gw + 1) / nw);
-    if (t_begin >= t_end) return;
     const QuantRows &src = GU ? a.xq : a.hq;
-
-    Walker<GU> cw;   // the task being computed
-    cw.start(a, t_begin);
-    Walker<GU> iw = cw;   // the next task to copy in
-    int issued = t_begin;
     // a slot's last token chunk (its chunks come in order) reads the weights for the last
     // time in this launch: evict-first in L2
     const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
-    auto issue_next = [&](int st) {
-        if (issued < t_end) {
-            issue_task<NC, RU, GU>(a, iw.t, st, wbuf, sbuf,
-                                   iw.ntok <= iw.t.j0 + iw.tc ? pol_last : pol_again);
-            if (++issued < t_end) iw.next(a);
-        }
-        cp_async_commit();   // possibly empty: keeps one group per task
-    };
-#pragma unroll
-    for (int k = 0; k < D - 1; ++k) issue_next(k);
-
     uint32_t act[TC][NC][8];
     int csum8[TC][NC];   // -8 x the chunk's code sum
     float ascale[TC];
-    int cur_slot = -1, cur_j0 = -1, cur_s = -1;
 
-    for (int task = t_begin, it = 0; task < t_end; ++task, ++it) {
-        issue_next((it + D - 1) % D);
-        cp_async_wait<D - 1>();   // this task's copies (group `it`) have landed
-        if (task > t_begin) cw.next(a);
-        const Task &t = cw.t;
-        const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+    // Runs tasks [t_begin, t_end) through this warp's ring; `shared`: the range lies in the
+    // shared expert's slot and is walked without the plan.
+    auto run = [&](int t_begin, int t_end, bool shared) {
+        Walker<GU> cw;   // the task being computed
+        if (shared) cw.start_shared(a, t_begin);
+        else cw.start(a, t_begin);
+        Walker<GU> iw = cw;   // the next task to copy in
+        int issued = t_begin;
+        auto issue_next = [&](int st) {
+            if (issued < t_end) {
+                issue_task<NC, RU, GU>(a, iw.t, st, wbuf, sbuf,
+                                       iw.ntok <= iw.t.j0 + iw.tc ? pol_last : pol_again);
+                if (++issued < t_end) iw.next(a);
+            }
+            cp_async_commit();   // possibly empty: keeps one group per task
+        };
+#pragma unroll
+        for (int k = 0; k < D - 1; ++k) issue_next(k);
 
-        // activations of this lane's chunks for the task's tokens (kept across tasks)
-        if (t.slot != cur_slot || t.j0 != cur_j0 || t.s != cur_s) {
-            cur_slot = t.slot;
-            cur_j0 = t.j0;
-            cur_s = t.s;
-            const int lpr = lpr_of<NC>(g);
-            const int gl = lane % lpr, cb = t.s * g.sch, sn = min(g.sch, g.kdim / 32 - cb);
+        int cur_slot = -1, cur_j0 = -1, cur_s = -1;
+        for (int task = t_begin, it = 0; task < t_end; ++task, ++it) {
+            issue_next((it + D - 1) % D);
+            cp_async_wait<D - 1>();   // this task's copies (group `it`) have landed
+            if (task > t_begin) cw.next(a);
+            const Task &t = cw.t;
+            const Geo &g = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+            // activations of this lane's chunks for the task's tokens (kept across tasks)
+            if (t.slot != cur_slot || t.j0 != cur_j0 || t.s != cur_s) {
+                cur_slot = t.slot;
+                cur_j0 = t.j0;
+                cur_s = t.s;
+                const int lpr = lpr_of<NC>(g);
+                const int gl = lane % lpr, cb = t.s * g.sch, sn = min(g.sch, g.kdim / 32 - cb);
 #pragma unroll
-            for (int j = 0; j < TC; ++j) {
-                int row = 0;
-                ascale[j] = 0.0f;
-                if (j < t.nt) {
-                    if (GU) row = t.sh ? t.j0 + j : a.tok[t.tokbase + t.j0 + j];
-                    else row = t.rowbase + j;
-                    ascale[j] = src.scale[row];
-                }
+                for (int j = 0; j < TC; ++j) {
+                    int row = 0;
+                    ascale[j] = 0.0f;
+                    if (j < t.nt) {
+                        if (GU) row = t.sh ? t.j0 + j : a.tok[t.tokbase + t.j0 + j];
+                        else row = t.rowbase + j;
+                        ascale[j] = src.scale[row];
+                    }
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const int li = gl + c * lpr, ci = cb + li;
-                    if (j < t.nt && li < sn) {
-                        const uint4 *p = reinterpret_cast<const uint4 *>(
-                            src.q + (size_t)row * src.q_ld + (size_t)ci * 32);
-                        const uint4 v0 = p[0], v1 = p[1];
-                        act[j][c][0] = v0.x; act[j][c][1] = v0.y; act[j][c][2] = v0.z; act[j][c][3] = v0.w;
-                        act[j][c][4] = v1.x; act[j][c][5] = v1.y; act[j][c][6] = v1.z; act[j][c][7] = v1.w;
-                        csum8[j][c] = -8 * src.csum[(size_t)row * src.c_ld + ci];
-                    } else {
+                    for (int c = 0; c < NC; ++c) {
+                        const int li = gl + c * lpr, ci = cb + li;
+                        if (j < t.nt && li < sn) {
+                            const uint4 *p = reinterpret_cast<const uint4 *>(
+                                src.q + (size_t)row * src.q_ld + (size_t)ci * 32);
+                            const uint4 v0 = p[0], v1 = p[1];
+                            act[j][c][0] = v0.x; act[j][c][1] = v0.y; act[j][c][2] = v0.z; act[j][c][3] = v0.w;
+                            act[j][c][4] = v1.x; act[j][c][5] = v1.y; act[j][c][6] = v1.z; act[j][c][7] = v1.w;
+                            csum8[j][c] = -8 * src.csum[(size_t)row * src.c_ld + ci];
+                        } else {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) act[j][c][q] = 0;
-                        csum8[j][c] = 0;
+                            for (int q = 0; q < 8; ++q) act[j][c][q] = 0;
+                            csum8[j][c] = 0;
+                        }
                     }
                 }
             }
-        }
 
-        // the chunk's real token count picks the variant, so padding costs little
-        const int st = it % D;
-        if (t.nt == 1 || TC == 1)
-            run_task<NC, TC, RU, 1, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
-        else if (t.nt == 2 || TC == 2)
-            run_task<NC, TC, RU, (TC >= 2 ? 2 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
-        else if (t.nt <= 4 || TC == 4)
-            run_task<NC, TC, RU, (TC >= 4 ? 4 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
-        else
-            run_task<NC, TC, RU, TC, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+            // the chunk's real token count picks the variant, so padding costs little
+            const int st = it % D;
+            if (t.nt == 1 || TC == 1)
+                run_task<NC, TC, RU, 1, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+            else if (t.nt == 2 || TC == 2)
+                run_task<NC, TC, RU, (TC >= 2 ? 2 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+            else if (t.nt <= 4 || TC == 4)
+                run_task<NC, TC, RU, (TC >= 4 ? 4 : 1), GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+            else
+                run_task<NC, TC, RU, TC, GU, PROBE>(a, t, g, st, wbuf, sbuf, act, csum8, ascale);
+        }
+        cp_async_wait<0>();
+    };
+
+    // Early mode (gate/up of a call whose x codes were written at least two launches back):
+    // the shared expert's tasks, a contiguous share per warp, run before the dependency wait.
+    long long c0 = 0;   // the routed tasks' share of the cost starts here
+    if (early) {
+        const int n_sh = tasks_of(a.geo_gu[1], a.T, a.tc_gu);
+        const int s_begin = (int)(n_sh * gw / nw), s_end = (int)(n_sh * (gw + 1) / nw);
+        if (s_begin < s_end) run(s_begin, s_end, true);
+        pdl_wait();
+        c0 = (GU ? a.plan->gu_cost : a.plan->dn_cost)[1];
     }
-    cp_async_wait<0>();
+    const int n_slots = a.plan->n_slots;
+    const long long C = (GU ? a.plan->gu_cost : a.plan->dn_cost)[n_slots];
+    if (C <= c0) return;
+    const int t_begin = task_at<GU>(a, c0 + (C - c0) * gw / nw);
+    const int t_end = gw + 1 == nw ? (GU ? a.plan->gu_tiles : a.plan->dn_tiles)
+                                   : task_at<GU>(a, c0 + (C - c0) * (gw + 1) / nw);
+    if (t_begin < t_end) run(t_begin, t_end, false);
 }
 
 typedef void (*FfnKernel)(const FfnArgs);
