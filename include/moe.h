@@ -45,8 +45,10 @@
  *     max(F, Fs)/16 and (T*(K+1) + 513) * H/64 below 1e9.  Inputs must be finite.
  *   - Alignment: weight, activation and output tensors 16 bytes; index arrays,
  *     bias and routing weights 4 bytes; the workspace 256 bytes.
- *   - The workspace's first 256 bytes hold a device error word: zero them
- *     once before the workspace is first used (e.g. allocate it zeroed).
+ *   - The workspace's first 256 bytes hold a device error word and a counter
+ *     that the kernels return to zero themselves: zero them once before the
+ *     workspace is first used (e.g. allocate it zeroed).  moe_check_errors
+ *     zeroes them again after it reports an error.
  *   - Determinism: every output is a deterministic function of the inputs
  *     (no floating-point atomics; reductions run in a fixed order).
  */

@@ -671,7 +671,8 @@ int moe_check_errors(void *workspace, size_t workspace_bytes, void *stream)
     int32_t flag = 0;
     cudaError_t e = cudaStreamSynchronize(st);
     if (e == cudaSuccess) e = cudaMemcpy(&flag, workspace, 4, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess && flag) e = cudaMemsetAsync(workspace, 0, 4, st);
+    // the error word and the route tail's ticket (a launch stopped midway may leave it set)
+    if (e == cudaSuccess && flag) e = cudaMemsetAsync(workspace, 0, 256, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "error check");
     if (flag & kErrBadExpertId) return fail(MOE_ERR_DEVICE, "an expert id outside [0, n_experts) was skipped");

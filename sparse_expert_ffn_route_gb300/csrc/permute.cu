@@ -526,6 +526,14 @@ constexpr size_t kTailSmemBytes = kTailIdsOffset + sizeof(int) * (kRouteClusterM
                                   sizeof(int) * kRouteClusterMaxT + sizeof(int) * (1024 + kMaxExperts) +
                                   sizeof(float) * kMaxExperts;
 
+// Batches of more than kTailOneCtaMaxT tokens select over several CTAs, kTailTokensPerCta
+// tokens each (one warp per token: one SM's 32 warps selecting 64 tokens took 12 µs); the
+// last CTA to finish, by a ticket in the workspace's first 256 bytes, reads every token's
+// choice back and builds the batch-union and the plan.
+constexpr int kTailOneCtaMaxT = 32;
+constexpr int kTailTokensPerCta = 8;
+constexpr int kTailTicketOffset = 24;   // ints into the workspace's first 256 bytes
+
 __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restrict__ logits, int T,
                                                           SelectParams sp, int32_t *ids, float *w,
                                                           int32_t *keff, int do_permute,
@@ -563,12 +571,33 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     sp.bias = s_bias;
     pdl_wait();
     pdl_launch_dependents();
-    for (int t = wid; t < T; t += 32) {
+    const int G = (int)gridDim.x;
+    const int tb = G > 1 ? (int)blockIdx.x * kTailTokensPerCta : 0;
+    const int te = G > 1 ? min(T, tb + kTailTokensPerCta) : T;
+    for (int t = tb + wid; t < te; t += 32) {
         const float *lrow = logits + (size_t)t * E;
         select_token(sp, [&](int e) { return lrow[e]; }, t, ids, w, keff, s_ids + t * K,
                      s_keff + t);
     }
     if (!do_permute) return;
+    if (G > 1) {
+        __shared__ int s_last;
+        __syncthreads();   // this CTA's choices are written
+        if (threadIdx.x == 0) {
+            __threadfence();
+            int32_t *ticket = o.err + kTailTicketOffset;
+            s_last = atomicAdd(ticket, 1) == G - 1;
+            if (s_last) {
+                *ticket = 0;   // back to zero for the next call
+                __threadfence();
+            }
+        }
+        __syncthreads();
+        if (!s_last) return;
+        // every token's choice (the other CTAs' through L2)
+        for (int i = threadIdx.x; i < T * K; i += blockDim.x) s_ids[i] = __ldcg(ids + i);
+        for (int i = threadIdx.x; i < T; i += blockDim.x) s_keff[i] = __ldcg(keff + i);
+    }
     const bool small = T * K <= kSmallRouteMaxPairs && pp.n_shared + E <= 1024;
     if (!small)
         for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
@@ -632,7 +661,8 @@ cudaError_t launch_route_tail(const moe_config &c, const float *logits, const fl
     const PermuteOut o = perm ? *perm : PermuteOut{};
     const PlanParams pp = plan_args ? plan_params(*plan_args) : PlanParams{};
     FfnPlan *plan = plan_args ? const_cast<FfnPlan *>(plan_args->plan) : nullptr;
-    return launch_kernel(route_tail_kernel, dim3(1), dim3(1024), kTailSmemBytes, st, 1, logits, T,
+    const int grid = T > kTailOneCtaMaxT ? (T + kTailTokensPerCta - 1) / kTailTokensPerCta : 1;
+    return launch_kernel(route_tail_kernel, dim3(grid), dim3(1024), kTailSmemBytes, st, 1, logits, T,
                          select_params(c, bias), ids, w, keff, perm ? 1 : 0, o,
                          (perm && plan_args) ? 1 : 0, pp, plan);
 }
