@@ -157,6 +157,23 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+PATH_NAMES = {0: "warp GEMV", 1: "tcgen05 grouped GEMM", 2: "row GEMV"}
+
+
+def stage_path(cfg, T: int, stage: str) -> int:
+    """The kernel that runs an FFN stage ("gate_up" or "down")."""
+    import sparse_expert_ffn_route_gb300 as moe
+    return moe.moe_ffn_path(cfg, T) if stage == "gate_up" else moe.moe_ffn_path_down(cfg, T)
+
+
+def ffn_kernel_name(cfg, T: int) -> str:
+    import sparse_expert_ffn_route_gb300 as moe
+    gu, dn = moe.moe_ffn_path(cfg, T), moe.moe_ffn_path_down(cfg, T)
+    if gu == dn:
+        return PATH_NAMES.get(gu, "?")
+    return "%s (gate/up) + %s (down)" % (PATH_NAMES.get(gu, "?"), PATH_NAMES.get(dn, "?"))
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch recorded by an ncu capture of this kernel (profiles/), or None
     when the kernel's source changed since the capture."""
@@ -310,7 +327,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = hbm_peak()
     achieved = tot_bytes[dom] / (st[dom][0] / 1e3) / 1e9
     traffic = recorded_traffic("ffn_" + dom, "%s_T%d" % (wl.name, T))
-    if moe.moe_ffn_uses_tensor_cores(cfg, T) == 1:
+    if stage_path(cfg, T, dom) == moe.MOE_FFN_TENSOR:
         # a dense contraction: tensor-pipe roofline on the useful FLOPs (the stage also holds
         # the x-code gather launch, so this is a lower bound on the GEMM kernel's own rate)
         tot_flops = {"gate_up": 0.0, "down": 0.0}
@@ -465,8 +482,7 @@ def run_ours(args, world, rank, local):
                    "routed_scaling_factor": wl.routed_scaling_factor, "top_p": wl.top_p,
                    "unique_experts_mean": round(float(np.mean([s[0] for s in stats])), 1),
                    "batches_rotated": N_BATCHES,
-                   "ffn_kernel": {moe.MOE_FFN_WARP_GEMV: "warp GEMV", moe.MOE_FFN_TENSOR: "tcgen05 grouped GEMM",
-                                  moe.MOE_FFN_ROW_GEMV: "row GEMV"}.get(moe.moe_ffn_path(cfg, T), "?"),
+                   "ffn_kernel": ffn_kernel_name(cfg, T),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights"
                          % (np.mean([algorithmic_bytes(wl, T, *s)["layer"] for s in stats]) / 1e9),
                    "parallelism": "dp%d (replicas, no collective)" % world},
@@ -567,9 +583,8 @@ def measure_layer(moe, wl, T, routed, shared, dev, steps, warmup, peak, rank=0):
     dom = max(("gate_up", "down"), key=lambda s_: st[s_][0])
     gbs = tot[dom] / (st[dom][0] / 1e3) / 1e9
     traffic = recorded_traffic("ffn_" + dom, "%s_T%d" % (wl.name, T))
-    path = {moe.MOE_FFN_WARP_GEMV: "warp GEMV", moe.MOE_FFN_TENSOR: "tcgen05 grouped GEMM",
-            moe.MOE_FFN_ROW_GEMV: "row GEMV"}.get(moe.moe_ffn_path(cfg, T), "?")
-    if moe.moe_ffn_uses_tensor_cores(cfg, T) == 1:
+    path = ffn_kernel_name(cfg, T)
+    if stage_path(cfg, T, dom) == moe.MOE_FFN_TENSOR:
         tpeak, tkind = tensor_peak()
         tf = fl[dom] / (st[dom][0] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": "ffn_" + dom, "achieved": round(tf, 1), "peak": tpeak,

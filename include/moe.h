@@ -207,17 +207,20 @@ int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls
  * GEMV into a dense contraction once tokens per expert grow.] */
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
 
-/* Which grouped expert-FFN kernel a call with T tokens runs (host-side, no
- * device work): MOE_FFN_TENSOR when moe_ffn_uses_tensor_cores says so;
- * otherwise MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when
- * hidden, d_ff and d_ff_shared are multiples of 256 and T >= 4, else
- * MOE_FFN_WARP_GEMV.
+/* Which grouped expert-FFN kernel a call with T tokens runs for gate/up
+ * (moe_ffn_path) and for down (moe_ffn_path_down) (host-side, no device
+ * work): MOE_FFN_TENSOR when moe_ffn_uses_tensor_cores says so -- except
+ * gate/up of a narrow layer (d_ff and d_ff_shared under 1024, hidden 1024 or
+ * more) with 64 tokens or fewer, which takes the row GEMV; otherwise
+ * MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when hidden, d_ff
+ * and d_ff_shared are multiples of 256 and T >= 4, else MOE_FFN_WARP_GEMV.
  * Returns -1 for an invalid config or T < 0.
  * ["colibri 开发演进实录" §2.2 K1/K1b: the integer dot both GEMV kernels run.] */
 #define MOE_FFN_WARP_GEMV 0
 #define MOE_FFN_TENSOR    1
 #define MOE_FFN_ROW_GEMV  2
 int moe_ffn_path(const moe_config *cfg, int T);
+int moe_ffn_path_down(const moe_config *cfg, int T);
 
 /* Router ["MoE 路由与专家流式加载" §1.1, §1.2].
  *   x [T][H] fp32, w_router [E][H] fp32, bias [E] fp32 (selection only).

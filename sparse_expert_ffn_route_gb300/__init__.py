@@ -13,4 +13,5 @@ from .binding import (EXPORTS, LIBRARY_PATH, MOE_ERR_ALIGN, MOE_ERR_ARG, MOE_ERR
                       moe_permute, moe_route, moe_route_noalloc, moe_stage_times,
                       moe_workspace_size, moe_ffn_uses_tensor_cores,
                       moe_route_lookahead, moe_topk_hits, moe_quantize_int4_gs64, moe_quantize_int3_g64,
-                      moe_selftest_wait_timeout, moe_layer_forward_host, moe_ffn_path)
+                      moe_selftest_wait_timeout, moe_layer_forward_host, moe_ffn_path,
+                      moe_ffn_path_down)

@@ -39,7 +39,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "
            "moe_route_noalloc", "moe_ffn_uses_tensor_cores", "moe_route_lookahead",
            "moe_topk_hits", "moe_quantize_int4_gs64", "moe_quantize_int3_g64",
            "moe_selftest_wait_timeout",
-           "moe_layer_forward_host", "moe_ffn_path")
+           "moe_layer_forward_host", "moe_ffn_path", "moe_ffn_path_down")
 
 
 class MoeError(RuntimeError):
@@ -101,6 +101,8 @@ def load_library():
     L.moe_ffn_uses_tensor_cores.restype = i32
     L.moe_ffn_path.argtypes = [vp, i32]
     L.moe_ffn_path.restype = i32
+    L.moe_ffn_path_down.argtypes = [vp, i32]
+    L.moe_ffn_path_down.restype = i32
     L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_route_lookahead.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.moe_topk_hits.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
@@ -153,9 +155,14 @@ def moe_ffn_uses_tensor_cores(cfg: MoeConfig, T: int) -> int:
 
 
 def moe_ffn_path(cfg: MoeConfig, T: int) -> int:
-    """The grouped expert-FFN kernel a call with T tokens runs: MOE_FFN_WARP_GEMV,
-    MOE_FFN_TENSOR or MOE_FFN_ROW_GEMV; -1 for an invalid config or T."""
+    """The grouped expert-FFN kernel a call with T tokens runs for gate/up:
+    MOE_FFN_WARP_GEMV, MOE_FFN_TENSOR or MOE_FFN_ROW_GEMV; -1 for an invalid config or T."""
     return int(load_library().moe_ffn_path(ctypes.byref(cfg), T))
+
+
+def moe_ffn_path_down(cfg: MoeConfig, T: int) -> int:
+    """The same for the down projection."""
+    return int(load_library().moe_ffn_path_down(ctypes.byref(cfg), T))
 
 
 def alloc_workspace(cfg: MoeConfig, max_tokens: int, device="cuda") -> torch.Tensor:

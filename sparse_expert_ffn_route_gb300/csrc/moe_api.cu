@@ -208,7 +208,7 @@ void configure_ffn(FfnArgs &a, void *ws, const WsLayout &L)
 {
     ffn_configure(a);
     a.xq.bf16 = nullptr;
-    a.hq.bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.hbf) : nullptr;
+    a.hq.bf16 = a.tensor_dn ? at<__nv_bfloat16>(ws, L.hbf) : nullptr;
     a.x_bf16 = a.tensor ? at<__nv_bfloat16>(ws, L.xbf) : nullptr;
     a.h_bf16 = a.hq.bf16;
 }
@@ -512,15 +512,21 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T)
     return ffn_use_tensor_cores(query_args(*cfg, T)) ? 1 : 0;
 }
 
-int moe_ffn_path(const moe_config *cfg, int T)
+// the paths ffn_configure picks (the row GEMV's shape conditions hold for the operands'
+// 16-byte alignment of every call that passes validation: weights are checked, the workspace
+// regions are aligned)
+static int ffn_path_of(const moe_config *cfg, int T, bool down)
 {
     const int tc = moe_ffn_uses_tensor_cores(cfg, T);
-    if (tc != 0) return tc;
-    // the row GEMV's shape conditions; the operands' 16-byte alignment holds for every call
-    // that passes validation (weights are checked, the workspace regions are aligned)
-    return T >= kRowGemvMinT && ffn_rows_supported(query_args(*cfg, T)) ? MOE_FFN_ROW_GEMV
-                                                                         : MOE_FFN_WARP_GEMV;
+    if (tc < 0) return tc;
+    const FfnArgs a = query_args(*cfg, T);
+    if (tc) return down || !ffn_split_paths(a) ? MOE_FFN_TENSOR : MOE_FFN_ROW_GEMV;
+    return T >= kRowGemvMinT && ffn_rows_supported(a) ? MOE_FFN_ROW_GEMV : MOE_FFN_WARP_GEMV;
 }
+
+int moe_ffn_path(const moe_config *cfg, int T) { return ffn_path_of(cfg, T, false); }
+
+int moe_ffn_path_down(const moe_config *cfg, int T) { return ffn_path_of(cfg, T, true); }
 
 int moe_route(const moe_config *cfg, const float *x, const float *w_router, const float *bias,
               int T, int32_t *ids, float *w, int32_t *keff, void *workspace,

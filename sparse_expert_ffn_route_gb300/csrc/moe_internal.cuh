@@ -92,8 +92,8 @@ struct FfnArgs {
     float *gpart, *upart;             // [S_gate/up][plane_rows][hstride] partial gate / up
     int plane_rows;                   // output rows of the call (shared rows + routed pairs)
     int slice_gu, slice_dn;           // rows cut into 1024-input slices
-    int tensor;                       // the tcgen05 path (ffn_tc.cu) runs gate/up and down
-    int rows;                         // the row GEMV (ffn_rows.cu) runs gate/up and down
+    int tensor, tensor_dn;            // the tcgen05 path (ffn_tc.cu) runs gate/up / down
+    int rows, rows_dn;                // the row GEMV (ffn_rows.cu) runs gate/up / down
     __nv_bfloat16 *x_bf16;            // [rows][H] the codes of x per output row as bf16 (tensor path)
     __nv_bfloat16 *h_bf16;            // [rows][hstride] the codes of h as bf16 (tensor path)
     int tc_gu, tc_dn;                 // token chunk per task
@@ -177,6 +177,8 @@ cudaError_t launch_ffn_tc(bool gate_up, const FfnArgs &a, cudaStream_t st);
 // row GEMV (ffn_rows.cu): reductions that are multiples of 256 inputs, 16-byte aligned
 // operands; one pass over each 64-row weight block per chunk of up to 16 tokens
 bool ffn_rows_supported(const FfnArgs &a);
+// a narrow decode-route layer whose gate/up takes the row GEMV and down the tensor path
+bool ffn_split_paths(const FfnArgs &a);
 cudaError_t launch_ffn_rows(bool gate_up, const FfnArgs &a, cudaStream_t st);
 cudaError_t launch_ffn_down(const FfnArgs &a, cudaStream_t st);
 // pair_of (nullable) gives each (t, i) its list position directly; without it the position
