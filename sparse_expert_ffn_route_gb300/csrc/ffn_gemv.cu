@@ -87,14 +87,25 @@ bool ffn_use_tensor_cores(const FfnArgs &a)
     return U > 0.0 && (double)a.T * a.K / U >= 10.0;
 }
 
-// On a narrow layer in the decode route the tensor path runs down only: gate/up, whose
-// reduction over H is long, is faster on the row GEMV, while down's short reduction over d_ff
-// makes one-stage row-GEMV tasks (A3B-style layer, T = 64: gate/up 38.7 µs on the row GEMV
-// against 48.6 on the tensor path, down 41.2 against 31.1).
+// Where the tensor path takes a layer, it runs down only in two cases.  On a narrow layer in
+// the decode route: gate/up, whose reduction over H is long, is faster on the row GEMV, while
+// down's short reduction over d_ff makes one-stage row-GEMV tasks (A3B-style layer, T = 64:
+// gate/up 38.7 µs on the row GEMV against 48.6 on the tensor path, down 41.2 against 31.1).
+// Past the decode route, on wide layers, down crosses to the tensor path at fewer tokens
+// per expert than gate/up: between 10 and kSplitMaxPerExpert expected tokens per routed
+// expert gate/up stays on the row GEMV (wide layer, T = 512, 10.7 per expert: gate/up 2.86 ms
+// on the row GEMV against 3.32 on the tensor path, down 2.33 against 1.76).
+constexpr double kSplitMaxPerExpert = 14.0;
+
 bool ffn_split_paths(const FfnArgs &a)
 {
-    return a.T <= kRouteClusterMaxT && a.H >= 1024 && a.F < 1024 && (!a.n_shared || a.Fs < 1024) &&
-           a.T >= kRowGemvMinT && ffn_rows_supported(a);
+    if (a.T < kRowGemvMinT || !ffn_rows_supported(a)) return false;
+    const bool narrow = a.H < 1024 || a.F < 1024;
+    if (a.T <= kRouteClusterMaxT)
+        return a.H >= 1024 && a.F < 1024 && (!a.n_shared || a.Fs < 1024);
+    if (narrow) return false;
+    const double U = a.E * (1.0 - pow(1.0 - (double)a.K / a.E, (double)a.T));
+    return U > 0.0 && (double)a.T * a.K / U < kSplitMaxPerExpert;
 }
 
 void ffn_configure(FfnArgs &a)

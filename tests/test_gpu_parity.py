@@ -199,6 +199,19 @@ def test_expert_ffn_exact_accumulators(moe, name, T):
     _check_ffn(g, ref, perm)
 
 
+def test_expert_ffn_exact_accumulators_split_paths(moe):
+    """A wide layer past the decode route at about 12 tokens per routed expert: gate/up on the
+    row GEMV, down on the tensor path (the paths are chosen per projection)."""
+    from dataclasses import replace
+    wl = replace(synth.WORKLOADS["wide"], name="split_mid", hidden=1024, d_ff=1024,
+                 d_ff_shared=1024, n_experts=64)
+    T = 96
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_ROW_GEMV
+    assert moe.moe_ffn_path_down(moe_cfg(wl), T) == moe.MOE_FFN_TENSOR
+    g, ref, perm = _ffn_both(moe, wl, T)
+    _check_ffn(g, ref, perm)
+
+
 @pytest.mark.parametrize("T", [24, 64])
 def test_expert_ffn_exact_accumulators_row_gemv(moe, T):
     """Row GEMV (decode-sized batch, reductions in multiples of 256) on a mid-sized shape:
