@@ -12,7 +12,9 @@
 //      ascending in token.
 // plan_kernel: slot table and tile prefix sums of the FFN kernels.
 // route_tail_kernel: decode-sized batches -- selection from the final router logits
-// (router_select.cuh), the batch-union and the plan, all in one CTA of 1024 threads.
+// (router_select.cuh), the batch-union and the plan, in one CTA of 1024 threads (above 32
+// tokens the selection spreads over one CTA per 8 tokens and the last one goes on alone);
+// up to 256 pairs the batch-union ranks the pairs' keys with the whole block.
 #include "device_util.cuh"
 #include "ffn_tiles.cuh"
 #include "launch.cuh"

@@ -12,7 +12,9 @@
 //                          shared memory and quantise x to int8 (the layer's activation
 //                          quantisation): cluster c takes tokens t = c (mod clusters), the
 //                          ranks' partial |x| maxima meet the same way.
-//   route_tail_kernel      (permute.cu) selection, batch-union and FFN plan in one CTA.
+//   route_tail_kernel      (permute.cu) selection, batch-union and FFN plan: one CTA up to
+//                          32 tokens; beyond, the selection over one CTA per 8 tokens and the
+//                          rest in the last of them.
 // Larger batches:
 //   router_logits_kernel   fp32 x . W_router^T, tiled 128 tokens x 64 experts, split along
 //                          H so that the grid covers the GPU; partial sums to [S][T][E].
