@@ -201,8 +201,9 @@ int moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, int polls
  * d_ff_shared in multiples of 512: on narrow ones (hidden or d_ff under 1024)
  * every batch of 32 tokens or more, otherwise batches beyond the decode route
  * (T > 64) whose expected tokens per routed expert T*K/U (U = E*(1-(1-K/E)^T),
- * the distinct experts of uniform routing) is at least 10.  Returns -1 for an
- * invalid config or T < 0.
+ * the distinct experts of uniform routing) is at least 10.  1 means the tensor
+ * path runs at least the down projection (moe_ffn_path / moe_ffn_path_down tell
+ * each projection's kernel).  Returns -1 for an invalid config or T < 0.
  * ["MoE 路由与专家流式加载" §1.3: the expert FFN turns from a weight-streaming
  * GEMV into a dense contraction once tokens per expert grow.] */
 int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
@@ -211,7 +212,9 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
  * (moe_ffn_path) and for down (moe_ffn_path_down) (host-side, no device
  * work): MOE_FFN_TENSOR when moe_ffn_uses_tensor_cores says so -- except
  * gate/up of a narrow layer (d_ff and d_ff_shared under 1024, hidden 1024 or
- * more) with 64 tokens or fewer, which takes the row GEMV; otherwise
+ * more) with 64 tokens or fewer, and gate/up of a wide layer beyond 64 tokens
+ * with under 14 expected tokens per routed expert, which take the row GEMV
+ * where its shape conditions hold; otherwise
  * MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when hidden, d_ff
  * and d_ff_shared are multiples of 256 and T >= 4, else MOE_FFN_WARP_GEMV.
  * Returns -1 for an invalid config or T < 0.
