@@ -401,12 +401,14 @@ __device__ void permute_small_block(const int *s_ids, const int *s_keff, int T, 
 // token -- the order permute_small_block gives.  Same outputs as permute_small_block
 // followed by build_plan.  s_bits (kMaxExperts / 32 words) is zero on entry.
 constexpr int kSmallRouteMaxPairs = 256;
+constexpr int kPlanByCountMinT = 16;
 
 struct SmallRouteSmem {
     int *key, *sorted;    // [kSmallRouteMaxPairs]
     unsigned *bits;       // [kMaxExperts / 32] experts present
     int *uq, *start, *len;   // [kMaxExperts] unique experts, their list heads and lengths
     PlanSums *ps;         // [32] warp totals of the plan scan
+    int *c, *lo;          // [kMaxExperts] per expert: kept pairs, first list entry
 };
 
 __device__ void route_small_block(const int *s_ids, const int *s_keff, int T, int K, int E,
@@ -416,6 +418,8 @@ __device__ void route_small_block(const int *s_ids, const int *s_keff, int T, in
     constexpr int kNone = 0x7fffffff;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int P = T * K, P4 = (P + 3) & ~3;
+    int *sm_c = sm.c, *sm_lo = sm.lo;   // per expert: kept pairs, first list entry
+    const bool by_count = do_plan && T > kPlanByCountMinT;
     // keys of the kept pairs (padded to a multiple of 4 with kNone); experts present as bits
     int key = kNone;
     if (tid < P) {
@@ -478,11 +482,15 @@ __device__ void route_small_block(const int *s_ids, const int *s_keff, int T, in
                 int u = __popc(word & ((1u << (x & 31)) - 1u));
                 for (int wi = 0; wi < (x >> 5); ++wi) u += __popc(sm.bits[wi]);
                 o.uniq[u] = x;
-                sm.uq[u] = x;
-                sm.start[u] = lo;
-                sm.len[u] = c;
+                sm_lo[x] = lo;
+                if (!by_count) {
+                    sm.uq[u] = x;
+                    sm.start[u] = lo;
+                    sm.len[u] = c;
+                }
             }
             o.counts[x] = c;
+            sm_c[x] = c;
         }
     }
     int nu = 0;
@@ -490,6 +498,28 @@ __device__ void route_small_block(const int *s_ids, const int *s_keff, int T, in
     if (tid == 0) *o.n_uniq = nu;
     if (!do_plan) return;
     __syncthreads();
+    // Above kPlanByCountMinT tokens the plan's routed slots go by descending token count
+    // (ties by id): the FFN kernels hand out tasks in slot order, so the longest come first
+    // and the shortest close the launch (GLM decode T = 32: gate/up and down each 2.4 µs
+    // shorter; at 8 and 16 tokens the ranking costs more than it saves, and the slots stay
+    // in ascending id).
+    if (by_count && tid < E && ((sm.bits[tid >> 5] >> (tid & 31)) & 1u)) {
+        const int x = tid, c = sm_c[x];
+        int v = 0;
+        for (int wi = 0; wi < (E + 31) >> 5; ++wi) {
+            unsigned w = sm.bits[wi];
+            while (w) {
+                const int y = wi * 32 + __ffs(w) - 1;
+                w &= w - 1;
+                const int cy = sm_c[y];
+                v += (cy > c || (cy == c && y < x)) ? 1 : 0;
+            }
+        }
+        sm.uq[v] = x;
+        sm.start[v] = sm_lo[x];
+        sm.len[v] = c;
+    }
+    if (by_count) __syncthreads();
     // plan: slot s by thread s; warp scans, then the warps' totals
     const int ns = pp.n_shared;
     const int nslots = ns + (pp.include_routed ? nu : 0);
@@ -563,6 +593,8 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     srm.bits = reinterpret_cast<unsigned *>(s_stage + 2 * kSmallRouteMaxPairs);
     srm.ps = reinterpret_cast<PlanSums *>(s_stage + 2 * kSmallRouteMaxPairs + kMaxExperts / 32);
     srm.uq = sm.uniq;
+    srm.c = sm.cnt;
+    srm.lo = sm.off;
     srm.start = sm.base;
     srm.len = sm.tot;
     // the selection bias is a layer parameter, not an output of the router kernel: it is
