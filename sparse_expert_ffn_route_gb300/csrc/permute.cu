@@ -643,7 +643,22 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     permute_small_block(s_ids, s_keff, T, K, E, o, sm, s_stage, s_fill);
     if (!do_plan) return;
     __syncthreads();
-    build_plan(pp, sm.off, sm.uniq, sm.nu, plan);
+    // the plan's routed slots by descending token count (ties by id), as on the small path
+    // above kPlanByCountMinT tokens (GLM decode T = 64: 90.9k -> 93.4k tokens/s; A3B T = 64
+    // 699k -> 722k)
+    const int nu = *sm.nu;
+    int *order = sm.base;
+    if ((int)threadIdx.x < nu) {
+        const int x = sm.uniq[threadIdx.x], c = sm.off[x + 1] - sm.off[x];
+        int v = 0;
+        for (int u = 0; u < nu; ++u) {
+            const int y = sm.uniq[u], cy = sm.off[y + 1] - sm.off[y];
+            v += (cy > c || (cy == c && y < x)) ? 1 : 0;
+        }
+        order[v] = x;
+    }
+    __syncthreads();
+    build_plan(pp, sm.off, order, sm.nu, plan);
 }
 
 // log2 of a token chunk; every chunk the FFN paths configure is a power of two
