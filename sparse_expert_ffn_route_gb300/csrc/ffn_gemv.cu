@@ -136,8 +136,9 @@ void ffn_configure(FfnArgs &a)
     }
     if (a.tensor || a.rows) return;   // both projections are set (the split pairs row GEMV + tensor)
     const int fmax = sh && a.Fs > a.F ? a.Fs : a.F;
-    const bool sgu = small && a.slice_gu && a.H > 32 * kSliceChunks;
-    const bool sdn = small && a.slice_dn && fmax > 32 * kSliceChunks &&
+    const bool slice = small && a.T >= kSliceMinT;
+    const bool sgu = slice && a.slice_gu && a.H > 32 * kSliceChunks;
+    const bool sdn = slice && a.slice_dn && fmax > 32 * kSliceChunks &&
                      fmax <= 32 * kSliceChunks * kMaxCombinePlanes;
     a.slice_gu = sgu ? 1 : 0;
     a.slice_dn = sdn ? 1 : 0;

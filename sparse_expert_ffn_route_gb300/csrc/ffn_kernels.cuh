@@ -1,5 +1,5 @@
 // ffn_kernels.cuh -- the warp GEMV: grouped int4 x int8 expert FFN for few tokens per expert
-// (GEMV-shaped, HBM-bound), run for batches under 4 tokens and for reductions that are not
+// (GEMV-shaped, HBM-bound), run for batches under 3 tokens and for reductions that are not
 // multiples of 256 (the row GEMV of ffn_rows.cu takes the rest below the tensor-core
 // crossover) ["MoE 路由与专家流式加载" §1.3: gate/up/SiLU/down on the integer-dot path;
 // "colibri 开发演进实录" §2.2 K1: unsigned nibbles, dot(u - 8, q) = dot(u, q) - 8 * sum(q);

@@ -80,10 +80,19 @@ __host__ __device__ inline Geo make_tc_geo(int kdim, int nrows, int matrices)
 constexpr int kRowBlock = 64;
 constexpr int kRowTok = 8;    // tokens per task at most
 constexpr int kRowTaskGateUp = kRowBlock, kRowTaskDown = 2 * kRowBlock;
-// Batches below this many tokens keep the warp GEMV: with 1-3 tokens the two kernels run the
-// GLM decode layer equally fast (tokens/s, warp vs row GEMV: T = 1 14.0k vs 13.8k, T = 2
-// 20.0k vs 19.8k), from 4 tokens on the row GEMV is ahead (T = 4 27.4k vs 28.5k).
-constexpr int kRowGemvMinT = 4;
+// Batches below this many tokens keep the warp GEMV.  Measured on the GLM decode layer
+// (tokens/s, warp vs row GEMV): T = 1 14.4k vs 13.8k, T = 2 20.2k vs 20.2k, T = 3 24.1k vs
+// 25.6k; with one token a 64-row task over the whole reduction is too coarse (about two per
+// CTA), from three on the row GEMV's shared activation rows pay.
+constexpr int kRowGemvMinT = 3;
+// Warp-GEMV rows are cut into kSliceChunks-chunk slices only in batches of at least this
+// many tokens.  With one or two tokens whole rows are faster (tokens/s, sliced vs whole:
+// GLM decode T = 1 14.5k vs 15.9k, T = 2 20.2k vs 22.7k; wide layer T = 1 12.3k vs 13.6k;
+// A3B-style T = 1 28.8k vs 30.5k): no partial-sum planes for the h quantisation and the
+// combine to add up.  With more tokens (where the warp GEMV only runs for reductions the row
+// GEMV does not take) a slice keeps each lane at one chunk, so the activations of 4 tokens
+// fit the registers and an expert's weights are streamed once per 4 tokens, not per token.
+constexpr int kSliceMinT = 3;
 
 __host__ __device__ inline Geo make_rows_geo(int kdim, int nrows, int rows)
 {

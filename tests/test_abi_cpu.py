@@ -64,14 +64,14 @@ def test_ffn_path_query(lib):
     assert moe.moe_ffn_uses_tensor_cores(glm, -1) == -1
     assert moe.moe_ffn_uses_tensor_cores(_cfg(top_k=9), 16) == -1
     # the kernel below the tensor path: the row GEMV when every reduction is a multiple of
-    # 256 inputs and the batch has 4 tokens or more, the warp GEMV otherwise
+    # 256 inputs and the batch has 3 tokens or more, the warp GEMV otherwise
     R, W, TC = moe.MOE_FFN_ROW_GEMV, moe.MOE_FFN_WARP_GEMV, moe.MOE_FFN_TENSOR
-    assert [moe.moe_ffn_path(glm, t) for t in (1, 3, 4, 7, 8, 32, 256, 512)] == [W, W, R, R, R, R, R, TC]
+    assert [moe.moe_ffn_path(glm, t) for t in (1, 2, 3, 4, 8, 32, 256, 512)] == [W, W, R, R, R, R, R, TC]
     # the narrow A3B-style layer: in the decode route (T <= 64) gate/up on the row GEMV and
     # down on the tensor path from 32 tokens on; past it both on the tensor path
     assert [moe.moe_ffn_path(a3b, t) for t in (16, 31, 32, 64, 65)] == [R, R, R, R, TC]
     assert [moe.moe_ffn_path_down(a3b, t) for t in (16, 31, 32, 64, 65)] == [R, R, TC, TC, TC]
-    assert [moe.moe_ffn_path_down(glm, t) for t in (1, 4, 32, 512)] == [W, R, R, TC]
+    assert [moe.moe_ffn_path_down(glm, t) for t in (1, 2, 3, 32, 512)] == [W, W, R, R, TC]
     assert moe.moe_ffn_path_down(glm, -1) == -1
     assert [moe.moe_ffn_path(tiny, t) for t in (1, 16, 65)] == [W, W, W]
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 32) == W

@@ -263,12 +263,12 @@ def _check_ffn(g, ref, perm):
                                   ref["xq"], ref["sx"])
 
 
-@pytest.mark.parametrize("T", [3, 4])
+@pytest.mark.parametrize("T", [2, 3])
 def test_expert_ffn_glm_full_width(moe, T):
     """Full GLM-decode widths (H=6144, F=2048) at the two sides of the warp / row GEMV
-    crossover: T=3 the warp GEMV (1024-input slices), T=4 the row GEMV."""
+    crossover: T=2 the warp GEMV (whole rows), T=3 the row GEMV."""
     wl = replace(synth.WORKLOADS["glm_decode"], n_experts=48)
-    want = moe.MOE_FFN_WARP_GEMV if T < 4 else moe.MOE_FFN_ROW_GEMV
+    want = moe.MOE_FFN_WARP_GEMV if T < 3 else moe.MOE_FFN_ROW_GEMV
     assert moe.moe_ffn_path(moe_cfg(wl), T) == want
     g, ref, perm = _ffn_both(moe, wl, T)
     _check_ffn(g, ref, perm)
@@ -356,7 +356,8 @@ def test_layer_forward(moe, name, T):
         assert near == 0
 
 
-@pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 32, [0, 13, 31]),
+@pytest.mark.parametrize("name,T,sample", [("glm_decode", 1, [0]), ("glm_decode", 2, [0, 1]),
+                                           ("glm_decode", 32, [0, 13, 31]),
                                            ("glm_decode", 128, [0, 77, 127]),
                                            ("wide", 64, [0, 40]), ("prefill", 4096, [0, 2047, 4095])])
 def test_layer_forward_full_size_sampled(moe, name, T, sample):
