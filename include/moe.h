@@ -26,7 +26,9 @@
  *     synchronise, except moe_layer_forward with MOE_FLAG_SYNC_CHECK.
  *     Kernels are launched with programmatic dependent launch: a kernel may
  *     start while the previous work on the stream finishes, and the router
- *     reads w_router and bias before it waits for that work.  Weights and
+ *     reads w_router and bias before it waits for that work (the down
+ *     projection likewise starts reading its weights before the h
+ *     quantisation ahead of it ends).  Weights and
  *     bias are parameters: do not write them with the kernel enqueued just
  *     before a call on the same stream (an event, a copy or a host sync in
  *     between orders such a write).

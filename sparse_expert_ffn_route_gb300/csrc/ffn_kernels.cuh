@@ -365,7 +365,12 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     constexpr int SL = ring_slots<NC, RU, GU>();
     extern __shared__ uint4 ffn_ring[];
     const bool early = GU && a.shared_early && a.n_shared;
-    if (!early) pdl_wait();
+    // Down: the plan and the weights are older than the h codes (the planner ran at least
+    // three launches back, the h quantisation is the launch just before), so each warp sends
+    // its first D-1 tasks' weight copies before the dependency wait and only its reads of the
+    // codes wait.
+    const bool early_w = !GU;
+    if (!early && !early_w) pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     uint4 *wbuf = ffn_ring + (size_t)wid * D * SL * 32;
@@ -383,8 +388,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     float ascale[TC];
 
     // Runs tasks [t_begin, t_end) through this warp's ring; `shared`: the range lies in the
-    // shared expert's slot and is walked without the plan.
-    auto run = [&](int t_begin, int t_end, bool shared) {
+    // shared expert's slot and is walked without the plan; `wait`: the dependency wait comes
+    // after the first copies.
+    auto run = [&](int t_begin, int t_end, bool shared, bool wait) {
         Walker<GU> cw;   // the task being computed
         if (shared) cw.start_shared(a, t_begin);
         else cw.start(a, t_begin);
@@ -400,6 +406,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
         };
 #pragma unroll
         for (int k = 0; k < D - 1; ++k) issue_next(k);
+        if (wait) pdl_wait();
 
         int cur_slot = -1, cur_j0 = -1, cur_s = -1;
         for (int task = t_begin, it = 0; task < t_end; ++task, ++it) {
@@ -463,17 +470,23 @@ __global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_consta
     if (early) {
         const int n_sh = tasks_of(a.geo_gu[1], a.T, a.tc_gu);
         const int s_begin = (int)(n_sh * gw / nw), s_end = (int)(n_sh * (gw + 1) / nw);
-        if (s_begin < s_end) run(s_begin, s_end, true);
+        if (s_begin < s_end) run(s_begin, s_end, true, false);
         pdl_wait();
         c0 = (GU ? a.plan->gu_cost : a.plan->dn_cost)[1];
     }
     const int n_slots = a.plan->n_slots;
     const long long C = (GU ? a.plan->gu_cost : a.plan->dn_cost)[n_slots];
-    if (C <= c0) return;
+    // every warp passes the dependency wait once, so that the launch never ends before the
+    // work it depends on
+    if (C <= c0) {
+        if (early_w) pdl_wait();
+        return;
+    }
     const int t_begin = task_at<GU>(a, c0 + (C - c0) * gw / nw);
     const int t_end = gw + 1 == nw ? (GU ? a.plan->gu_tiles : a.plan->dn_tiles)
                                    : task_at<GU>(a, c0 + (C - c0) * (gw + 1) / nw);
-    if (t_begin < t_end) run(t_begin, t_end, false);
+    if (t_begin < t_end) run(t_begin, t_end, false, early_w);
+    else if (early_w) pdl_wait();
 }
 
 typedef void (*FfnKernel)(const FfnArgs);
