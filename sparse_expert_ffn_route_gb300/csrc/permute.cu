@@ -12,9 +12,10 @@
 //      ascending in token.
 // plan_kernel: slot table and tile prefix sums of the FFN kernels.
 // route_tail_kernel: decode-sized batches -- selection from the final router logits
-// (router_select.cuh), the batch-union and the plan, in one CTA of 1024 threads (above 32
-// tokens the selection spreads over one CTA per 8 tokens and the last one goes on alone);
-// up to 256 pairs the batch-union ranks the pairs' keys with the whole block.
+// (router_select.cuh), the batch-union and the plan, in one CTA (above 32 tokens the
+// selection spreads over one CTA per 8 tokens of 1024 threads and the last one goes on
+// alone); up to 256 pairs the batch-union ranks the pairs' keys with the whole block, which
+// then has only the threads its phases need.
 #include "device_util.cuh"
 #include "ffn_tiles.cuh"
 #include "launch.cuh"
@@ -394,8 +395,8 @@ __device__ void permute_small_block(const int *s_ids, const int *s_keff, int T, 
     }
 }
 
-// Batch-union and plan of a batch of at most 256 pairs by the whole block (1024 threads, so
-// at least E + 1), in four block barriers and with short per-thread chains.  A kept pair's
+// Batch-union and plan of a batch of at most 256 pairs by the whole block (at least E + 1,
+// n_shared + E and T * K threads), in four block barriers and with short per-thread chains.  A kept pair's
 // place is its rank among the kept pairs' keys (expert << 8 | pair index): the lists come
 // out in ascending expert id and, within an expert, ascending pair index, i.e. ascending
 // token -- the order permute_small_block gives.  Same outputs as permute_small_block
@@ -608,7 +609,7 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     const int G = (int)gridDim.x;
     const int tb = G > 1 ? (int)blockIdx.x * kTailTokensPerCta : 0;
     const int te = G > 1 ? min(T, tb + kTailTokensPerCta) : T;
-    for (int t = tb + wid; t < te; t += 32) {
+    for (int t = tb + wid; t < te; t += (int)(blockDim.x >> 5)) {
         const float *lrow = logits + (size_t)t * E;
         select_token(sp, [&](int e) { return lrow[e]; }, t, ids, w, keff, s_ids + t * K,
                      s_keff + t);
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
         for (int i = threadIdx.x; i < T * K; i += blockDim.x) s_ids[i] = __ldcg(ids + i);
         for (int i = threadIdx.x; i < T; i += blockDim.x) s_keff[i] = __ldcg(keff + i);
     }
-    const bool small = T * K <= kSmallRouteMaxPairs && pp.n_shared + E <= 1024;
+    const bool small = T * K <= kSmallRouteMaxPairs && pp.n_shared + E <= (int)blockDim.x;
     if (!small)
         for (int e = threadIdx.x; e < E; e += blockDim.x) sm.cnt[e] = 0;
     __syncthreads();
@@ -659,6 +660,19 @@ __global__ void __launch_bounds__(1024) route_tail_kernel(const float *__restric
     }
     __syncthreads();
     build_plan(pp, sm.off, order, sm.nu, plan);
+}
+
+// Threads of the route tail: 1024, except for one CTA whose pairs take the small path, which
+// gets the threads its phases use (a warp per token, a thread per pair, per expert + 1 and
+// per plan slot): every block-wide phase is run by all of the block's warps, so a GLM decode
+// batch of one token (E = 256) takes 288 threads instead of 1024.
+int tail_threads(const moe_config &c, int T, int grid, const PlanParams &pp)
+{
+    const int P = T * c.top_k, E = c.n_experts;
+    if (grid != 1 || P > kSmallRouteMaxPairs) return 1024;
+    int need = max(max(E + 1, pp.n_shared + E), max((P + 3) & ~3, 32 * T));
+    need = (need + 31) & ~31;
+    return need < 1024 ? need : 1024;
 }
 
 // log2 of a token chunk; every chunk the FFN paths configure is a power of two
@@ -711,7 +725,8 @@ cudaError_t launch_route_tail(const moe_config &c, const float *logits, const fl
     const PlanParams pp = plan_args ? plan_params(*plan_args) : PlanParams{};
     FfnPlan *plan = plan_args ? const_cast<FfnPlan *>(plan_args->plan) : nullptr;
     const int grid = T > kTailOneCtaMaxT ? (T + kTailTokensPerCta - 1) / kTailTokensPerCta : 1;
-    return launch_kernel(route_tail_kernel, dim3(grid), dim3(1024), kTailSmemBytes, st, 1, logits, T,
+    return launch_kernel(route_tail_kernel, dim3(grid), dim3(tail_threads(c, T, grid, pp)),
+                         kTailSmemBytes, st, 1, logits, T,
                          select_params(c, bias), ids, w, keff, perm ? 1 : 0, o,
                          (perm && plan_args) ? 1 : 0, pp, plan);
 }
