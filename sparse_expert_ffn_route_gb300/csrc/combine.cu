@@ -31,13 +31,19 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
     pdl_wait();
     pdl_launch_dependents();
     const int t = blockIdx.y;
-    const int k = max(0, min(K, keff[t]));
-    if (threadIdx.x < k) {
+    // the token's K entries are read alongside keff (not behind it): one round trip fewer
+    // before the pairs' rows can be loaded
+    const int kt = keff[t];
+    if (threadIdx.x < K) {
         const int i = threadIdx.x;
         const int e = ids[(size_t)t * K + i];
+        const float wi = w[(size_t)t * K + i];
+        const int pk = pair_of ? pair_of[(size_t)t * K + i] : -1;
         int pair = -1;
-        if (pair_of) {
-            pair = pair_of[(size_t)t * K + i];
+        if (i >= max(0, min(K, kt))) {
+            // not kept: no pair
+        } else if (pair_of) {
+            pair = pk;
         } else if (e >= 0 && e < E) {
             int lo = offsets[e], hi = offsets[e + 1];   // first entry >= t
             const int end = hi;
@@ -49,8 +55,9 @@ __global__ void __launch_bounds__(kCThreads) combine_kernel(
             if (lo < end && tok[lo] == t) pair = lo;
         }
         s_pair[i] = pair;   // -1: (t, i) has no pair (inconsistent routing); it adds nothing
-        s_w[i] = w[(size_t)t * K + i];
+        s_w[i] = wi;
     }
+    const int k = max(0, min(K, kt));
     __syncthreads();
     const int c = (blockIdx.x * kCThreads + threadIdx.x) * 4;
     if (c >= H) return;

@@ -141,14 +141,17 @@ size_t router_stage_bytes(int H, int cs) { return sizeof(float) * kRouteStageT *
 // The end of both cluster routers, once s_part[t][j] holds this CTA's partial logits of the
 // cluster's kEPC experts over its slice of H: the |x| maxima of the tokens this cluster
 // quantises (t = c mod clusters), the logits of the tokens t = r (mod CS) summed over the
-// ranks in rank order through distributed shared memory, then the int8 codes of x.
+// ranks in rank order through distributed shared memory, then the int8 codes of x.  xs, when
+// not null, holds this rank's slice of every token's x in shared memory ([T][L/4] float4s),
+// which is then read instead of global memory.
 template <int kEPC>
 __device__ __forceinline__ void cluster_router_finish(cooperative_groups::cluster_group &cl,
                                                       const float *__restrict__ x, int T, int H,
                                                       int E, float *__restrict__ logits,
                                                       const QuantRows &xq, int quant,
                                                       float (*s_part)[kMaxExpertsPerCluster],
-                                                      float *s_amax, float *s_red)
+                                                      float *s_amax, float *s_red,
+                                                      const float4 *xs)
 {
     const int CS = (int)cl.num_blocks(), r = (int)cl.block_rank();
     const int c = blockIdx.x / CS, ncl = gridDim.x / CS;
@@ -159,7 +162,8 @@ __device__ __forceinline__ void cluster_router_finish(cooperative_groups::cluste
         for (int i = 0, t = c; t < T; ++i, t += ncl) {
             float m = 0.0f;
             for (int idx = tid; idx < nunit; idx += blockDim.x) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + k0 + idx * 4));
+                const float4 v = xs ? xs[(size_t)t * nunit + idx]
+                                    : __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + k0 + idx * 4));
                 m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
             }
 #pragma unroll
@@ -200,8 +204,9 @@ __device__ __forceinline__ void cluster_router_finish(cooperative_groups::cluste
                 int sum = 0;
                 if (run < runs) {
                     const float *v = x + (size_t)t * H + k0 + run * 8;
-                    const float4 a = __ldg(reinterpret_cast<const float4 *>(v));
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(v + 4));
+                    const float4 a = xs ? xs[(size_t)t * nunit + 2 * run] : __ldg(reinterpret_cast<const float4 *>(v));
+                    const float4 b = xs ? xs[(size_t)t * nunit + 2 * run + 1]
+                                        : __ldg(reinterpret_cast<const float4 *>(v + 4));
                     const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     const uint2 pk = quant_pack8(xv, inv, sum);
                     *reinterpret_cast<uint2 *>(xq.q + (size_t)t * xq.q_ld + k0 + run * 8) = pk;
@@ -305,7 +310,9 @@ __global__ void __launch_bounds__(256, 2) router_cluster_kernel(const float *__r
         }
         __syncthreads();   // before the next slice of x overwrites s_x
     }
-    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red);
+    // at most kRouteTokensMinT tokens, i.e. one stage: s_x still holds every token's slice
+    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red,
+                                T <= kRouteStageT ? s_x : nullptr);
 }
 
 
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(256, 2) router_tokens_kernel(const float *__re
         }
         __syncthreads();   // before the next pass overwrites s_tp
     }
-    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red);
+    cluster_router_finish<kEPC>(cl, x, T, H, E, logits, xq, quant, s_part, s_amax, s_red, nullptr);
 }
 
 __global__ void __launch_bounds__(256) router_select_kernel(const float *__restrict__ part, int S,
