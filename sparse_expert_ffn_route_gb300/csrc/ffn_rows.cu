@@ -322,7 +322,12 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     // the copy warp issues them before the dependency wait, while the route finishes; only
     // the copy warp waits before it reads the plan.
     const bool early = GU && a.shared_early && a.n_shared;
-    if (!early) pdl_wait();
+    // Down: the plan (written at least three launches back) and the weights are older than
+    // the h codes, so the slot table is read, and the copy warp arms the first ring stages of
+    // the CTA's first task and sends their weight and scale boxes, before the dependency
+    // wait; the token boxes and the h scales follow it.
+    const bool early_dn = !GU;
+    if (!early && !early_dn) pdl_wait();
     pdl_launch_dependents();
     FfnPlan *plan = const_cast<FfnPlan *>(a.plan);
     // the plan's slot table (written by the planner, which runs before this kernel)
@@ -344,11 +349,92 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     const float *gscale = GU ? a.xq.scale : a.hq.scale;
     const int nscale = GU ? a.T : a.plane_rows;
     const bool table = nscale <= kRwScaleTable;
+    int32_t *next = &plan->next[GU ? 0 : 1];
+    uint32_t k = 0;      // stages of this CTA so far
+    uint32_t kpre = 0;   // (down, copy warp) stages armed and sent weights before the wait
+    const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
+    // (copy warp) Issues every stage of task `task` (t; arow: this lane's token row).  `last`:
+    // the task is its slot's last token chunk (the slot's chunks are taken in order), whose
+    // weight and scale reads are the last in this launch, so evict-first.  `weights_only`:
+    // arm the task's first (at most D) stages and send only their weight and scale boxes;
+    // the stages below kpre were so armed, and get only their token boxes.  False on a
+    // timeout.
+    auto issue = [&](int task, const Task &t, int arow, bool last, bool weights_only) -> bool {
+        const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
+        const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
+        const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
+        const uint32_t bytes = NM * (kRwWBytes + kRwSBytes) + t.nt * kRwTokBytes;
+        // this lane's box: map, shared-memory offset, coordinates (the line or group
+        // coordinate advances with the stage)
+        const CUtensorMap *map = &maps.act;
+        // (gate/up: matrix m; down: the m-th 64-row block of the one matrix)
+        // z: the row coordinate of the nibble boxes (weight lanes; independent of the token
+        // rows, so those lanes' copies do not wait for the arow loads)
+        int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
+        const bool active = lane < 2 * NM + t.nt;
+        const uint64_t pol = lane < 2 * NM && last ? pol_last : pol_again;
+        if (lane < NM) {
+            map = &maps.w[t.sh][GU ? lane : 0];
+            off = lane * kRwWBytes;
+            z = wrow + (GU ? 0 : lane * kRowBlock);
+            dy = kRwLines;
+        } else if (lane < 2 * NM) {
+            map = &maps.s[t.sh][GU ? lane - NM : 0];
+            off = NM * kRwWBytes + (lane - NM) * kRwSBytes;
+            y = wrow + (GU ? 0 : (lane - NM) * kRowBlock);
+            dx = kRwLines * 4;
+        } else {
+            off = NM * (kRwWBytes + kRwSBytes) + (lane - 2 * NM) * kRwTokBytes;
+            dy = kRwLines;
+        }
+        const int smax = weights_only ? min(nst, D) : nst;
+        for (int s = 0; s < smax; ++s, ++k) {
+            const bool armed = !weights_only && k < kpre;
+            const int slot = (int)(k % D);
+            if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
+                return false;
+            const uint32_t fb = smem_u32(&sh->full[slot]);
+            if (s == 0 && !armed) {
+                RwHdr &h = sh->hdr[slot];
+                if (lane == 0) {
+                    h.task = task;
+                    h.e = t.e;
+                    h.r0 = t.r0;
+                    h.j0 = t.j0;
+                    h.nt = t.nt;
+                    h.rowbase = t.rowbase;
+                    h.tokbase = t.tokbase;
+                }
+                if (lane >= 2 * NM && lane < 2 * NM + kRwTok) h.arow[lane - 2 * NM] = arow;
+                __syncwarp();
+            }
+            if (lane == 0 && !armed) mbar_arrive_expect_tx(&sh->full[slot], bytes);
+            __syncwarp();
+            // the weight and scale boxes first: they need no token row
+            if (lane < 2 * NM && !armed)
+                tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb,
+                       pol);
+            else if (active && lane >= 2 * NM && !weights_only)
+                tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, arow,
+                       fb, pol);
+        }
+        return true;
+    };
+    if (early_dn) {
+        __syncthreads();   // the slot table and the barriers' initialisation
+        if (warp == kRwWarps && (int)blockIdx.x < plan->dn_tiles) {
+            const Task t = rw_task<GU>(a, *ps, (int)blockIdx.x);
+            const int j = lane - 2 * NM;
+            const int arow = j >= 0 && j < t.nt ? act_row<GU>(a, t, j) : 0;
+            issue((int)blockIdx.x, t, arow, ps->ntok[t.slot] <= t.j0 + kRwTok, true);
+            kpre = k;
+            k = 0;   // the task is issued again from its first stage: token boxes only below kpre
+        }
+        pdl_wait();
+    }
     if (table)
         for (int i = threadIdx.x; i < nscale; i += blockDim.x) stab[i] = gscale[i];
     __syncthreads();
-    int32_t *next = &plan->next[GU ? 0 : 1];
-    uint32_t k = 0;   // stages of this CTA so far
 
     if (warp == kRwWarps) {
         // ------------------------------- copy warp ------------------------------------
@@ -358,70 +444,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         // Lane L of the stage's one TMA instruction copies: L < NM nibbles of matrix L;
         // NM <= L < 2 NM scales of matrix L - NM; 2 NM <= L < 2 NM + nt the codes of token
         // L - 2 NM.
-        const uint64_t pol_last = l2_policy_evict_first(), pol_again = l2_policy_evict_normal();
-        // Issues every stage of task `task` (t; arow: this lane's token row).  `last`: the
-        // task is its slot's last token chunk (the slot's chunks are taken in order), whose
-        // weight and scale reads are the last in this launch, so evict-first.  False on a
-        // timeout.
-        auto issue = [&](int task, const Task &t, int arow, bool last) -> bool {
-            const Geo &geo = GU ? a.geo_gu[t.sh] : a.geo_dn[t.sh];
-            const int nst = (geo.kdim + kRwInputs - 1) / kRwInputs;
-            const int wrow = (t.sh ? 0 : t.e * geo.nrows) + t.r0;
-            const uint32_t bytes = NM * (kRwWBytes + kRwSBytes) + t.nt * kRwTokBytes;
-            // this lane's box: map, shared-memory offset, coordinates (the line or group
-            // coordinate advances with the stage)
-            const CUtensorMap *map = &maps.act;
-            // (gate/up: matrix m; down: the m-th 64-row block of the one matrix)
-            // z: the row coordinate of the nibble boxes (weight lanes; independent of the token
-            // rows, so those lanes' copies do not wait for the arow loads)
-            int off = 0, x = 0, y = 0, z = 0, dx = 0, dy = 0;
-            const bool active = lane < 2 * NM + t.nt;
-            const uint64_t pol = lane < 2 * NM && last ? pol_last : pol_again;
-            if (lane < NM) {
-                map = &maps.w[t.sh][GU ? lane : 0];
-                off = lane * kRwWBytes;
-                z = wrow + (GU ? 0 : lane * kRowBlock);
-                dy = kRwLines;
-            } else if (lane < 2 * NM) {
-                map = &maps.s[t.sh][GU ? lane - NM : 0];
-                off = NM * kRwWBytes + (lane - NM) * kRwSBytes;
-                y = wrow + (GU ? 0 : (lane - NM) * kRowBlock);
-                dx = kRwLines * 4;
-            } else {
-                off = NM * (kRwWBytes + kRwSBytes) + (lane - 2 * NM) * kRwTokBytes;
-                dy = kRwLines;
-            }
-            for (int s = 0; s < nst; ++s, ++k) {
-                const int slot = (int)(k % D);
-                if (k >= (uint32_t)D && !rw_wait_warp(&sh->empty[slot], ((k / D) - 1) & 1, sh, a.err))
-                    return false;
-                const uint32_t fb = smem_u32(&sh->full[slot]);
-                if (s == 0) {
-                    RwHdr &h = sh->hdr[slot];
-                    if (lane == 0) {
-                        h.task = task;
-                        h.e = t.e;
-                        h.r0 = t.r0;
-                        h.j0 = t.j0;
-                        h.nt = t.nt;
-                        h.rowbase = t.rowbase;
-                        h.tokbase = t.tokbase;
-                    }
-                    if (lane >= 2 * NM && lane < 2 * NM + kRwTok) h.arow[lane - 2 * NM] = arow;
-                    __syncwarp();
-                }
-                if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], bytes);
-                __syncwarp();
-                // the weight and scale boxes first: they need no token row
-                if (lane < 2 * NM)
-                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, z, fb,
-                           pol);
-                else if (active)
-                    tma_3d(smem_u32(ring + (size_t)slot * SB + off), map, x + s * dx, y + s * dy, arow,
-                           fb, pol);
-            }
-            return true;
-        };
         const int grid = (int)gridDim.x;
         // early mode: CTA b issues the shared expert's tasks b, b + grid, ... (slot 0, decoded
         // without the plan: task = chunk * row blocks + block, as the plan numbers them)
@@ -443,7 +465,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
                 ts.tokbase = 0;
                 ts.rowbase = ts.j0;
                 const int j = lane - 2 * NM;
-                if (!issue(task, ts, j >= 0 && j < ts.nt ? ts.j0 + j : 0, a.T <= ts.j0 + kRwTok)) {
+                if (!issue(task, ts, j >= 0 && j < ts.nt ? ts.j0 + j : 0, a.T <= ts.j0 + kRwTok, false)) {
                     failed = true;
                     break;
                 }
@@ -493,7 +515,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             Task tn{};
             int narow = 0;
             decode(ntask, tn, narow);
-            if (!issue(task, t, arow, ps->ntok[t.slot] <= t.j0 + kRwTok)) return false;
+            if (!issue(task, t, arow, ps->ntok[t.slot] <= t.j0 + kRwTok, false)) return false;
             task = ntask;
             t = tn;
             arow = narow;
