@@ -218,7 +218,7 @@ int moe_ffn_uses_tensor_cores(const moe_config *cfg, int T);
  * with under 14 expected tokens per routed expert, which take the row GEMV
  * where its shape conditions hold; otherwise
  * MOE_FFN_ROW_GEMV (one weight pass per 8 tokens, TMA-fed) when hidden, d_ff
- * and d_ff_shared are multiples of 256 and T >= 4, else MOE_FFN_WARP_GEMV.
+ * and d_ff_shared are multiples of 256 and T >= 3, else MOE_FFN_WARP_GEMV.
  * Returns -1 for an invalid config or T < 0.
  * ["colibri 开发演进实录" §2.2 K1/K1b: the integer dot both GEMV kernels run.] */
 #define MOE_FFN_WARP_GEMV 0
