@@ -74,6 +74,8 @@ def test_ffn_path_query(lib):
     assert [moe.moe_ffn_path_down(glm, t) for t in (1, 2, 3, 32, 512)] == [W, W, R, R, TC]
     assert moe.moe_ffn_path_down(glm, -1) == -1
     assert [moe.moe_ffn_path(tiny, t) for t in (1, 16, 65)] == [W, W, W]
+    # reductions that are not multiples of 256 keep the warp GEMV at any decode batch
+    assert moe.moe_ffn_path(_cfg(hidden=1088, d_ff=1088, n_shared=0, d_ff_shared=0), 8) == W
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=640), 32) == W
     assert moe.moe_ffn_path(_cfg(hidden=6144, d_ff=2048, d_ff_shared=768), 32) == R
     assert moe.moe_ffn_path(glm, -1) == -1 and moe.moe_ffn_path(_cfg(top_k=9), 16) == -1

@@ -199,6 +199,20 @@ def test_expert_ffn_exact_accumulators(moe, name, T):
     _check_ffn(g, ref, perm)
 
 
+def test_expert_ffn_exact_accumulators_sliced_warp_gemv(moe):
+    """The warp GEMV on 1024-input slices: reductions that are not multiples of 256 (hidden and
+    d_ff 1088: a full slice and a ragged one of 2 chunks) keep the row GEMV out, and 8 tokens
+    are past the whole-row batches, so gate/up ends in slice planes that the h quantisation
+    adds in slice order ["colibri 开发演进实录" §2.2 K1b, per-group int32 dot]."""
+    from dataclasses import replace
+    wl = replace(synth.WORKLOADS["tiny"], name="sliced", hidden=1088, d_ff=1088, n_shared=0,
+                 d_ff_shared=0, n_experts=16, top_k=4)
+    T = 8
+    assert moe.moe_ffn_path(moe_cfg(wl), T) == moe.MOE_FFN_WARP_GEMV
+    g, ref, perm = _ffn_both(moe, wl, T)
+    _check_ffn(g, ref, perm)
+
+
 def test_expert_ffn_exact_accumulators_split_paths(moe):
     """A wide layer past the decode route at about 12 tokens per routed expert: gate/up on the
     row GEMV, down on the tensor path (the paths are chosen per projection)."""
