@@ -30,9 +30,9 @@
 // the task (rows x matrices x tokens) at once by a reduce-scatter (V-1 shuffles in all, lane
 // l ends with one total); with fewer lanes per row, each by a shuffle tree.  gate/up tasks
 // carry both matrices and end with h = SiLU(sx*gate) * (sx*up); down tasks end with
-// y = sh * acc.  When the rows are sliced (decode-sized batches), a task ends with its
-// slice's partial sums instead: sx*gate and sx*up into per-slice planes that the h
-// quantisation adds up in slice order, and sh*acc into the slice's plane of y that the
+// y = sh * acc.  When the rows are sliced (decode-route batches of 3 tokens or more), a task
+// ends with its slice's partial sums instead: sx*gate and sx*up into per-slice planes that
+// the h quantisation adds up in slice order, and sh*acc into the slice's plane of y that the
 // combine adds up in slice order.
 #pragma once
 
