@@ -52,15 +52,29 @@ __device__ __forceinline__ uint32_t order_key(float v)
 // (sequential, in the oracle's order) and the divisions then run on those lanes.
 //
 // PL is the experts each lane holds (E <= 32 * PL); select_token below picks it from E.
+// select_from_scores takes over once the lane holds its experts' gates and choice keys.
+template <int PL>
+__device__ void select_from_scores(const SelectParams &p, const float (&sig)[PL],
+                                   uint32_t (&key)[PL], int t, int32_t *__restrict__ ids,
+                                   float *__restrict__ w, int32_t *__restrict__ keff,
+                                   int *sm_ids, int *sm_keff);
+
+// The sigmoid gate of a logit, 1 / (1 + e^-l) rounded once (the correctly rounded
+// reciprocal is the correctly rounded quotient 1 / d), and its choice key.
+__device__ __forceinline__ void score_expert(float l, float bias, float &sig, uint32_t &key)
+{
+    sig = __frcp_rn(__fadd_rn(1.0f, expf(-l)));
+    key = order_key(__fadd_rn(sig, bias));
+}
+
 template <int PL, typename LogitFn>
 __device__ void select_token_pl(const SelectParams &p, LogitFn logit, int t,
                                 int32_t *__restrict__ ids, float *__restrict__ w,
                                 int32_t *__restrict__ keff, int *sm_ids, int *sm_keff)
 {
     constexpr int kPerLane = PL;
-    constexpr unsigned kAll = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const int E = p.E, K = p.K;
+    const int E = p.E;
 
     // every logit and bias of this lane is loaded before any of them is used, so the loads
     // overlap instead of queueing behind each other's arithmetic
@@ -82,14 +96,41 @@ __device__ void select_token_pl(const SelectParams &p, LogitFn logit, int t,
         const int e = lane + 32 * j;
         sig[j] = 0.0f;
         key[j] = 0u;
-        if (e < E) {
-            // 1 / (1 + e^-l) rounded once: the correctly rounded reciprocal is the
-            // correctly rounded quotient 1 / d
-            sig[j] = __frcp_rn(__fadd_rn(1.0f, expf(-lv[j])));
-            key[j] = order_key(__fadd_rn(sig[j], bv[j]));
-        }
+        if (e < E) score_expert(lv[j], bv[j], sig[j], key[j]);
     }
+    select_from_scores<PL>(p, sig, key, t, ids, w, keff, sm_ids, sm_keff);
+}
 
+// The same selection from gates and keys already in shared memory (sig_s[e], key_s[e] for the
+// token's E experts, from score_expert).
+template <int PL>
+__device__ void select_token_staged_pl(const SelectParams &p, const float *sig_s,
+                                       const uint32_t *key_s, int t, int32_t *__restrict__ ids,
+                                       float *__restrict__ w, int32_t *__restrict__ keff,
+                                       int *sm_ids, int *sm_keff)
+{
+    const int lane = threadIdx.x & 31;
+    float sig[PL];
+    uint32_t key[PL];
+#pragma unroll
+    for (int j = 0; j < PL; ++j) {
+        const int e = lane + 32 * j;
+        sig[j] = e < p.E ? sig_s[e] : 0.0f;
+        key[j] = e < p.E ? key_s[e] : 0u;
+    }
+    select_from_scores<PL>(p, sig, key, t, ids, w, keff, sm_ids, sm_keff);
+}
+
+template <int PL>
+__device__ void select_from_scores(const SelectParams &p, const float (&sig)[PL],
+                                   uint32_t (&key)[PL], int t, int32_t *__restrict__ ids,
+                                   float *__restrict__ w, int32_t *__restrict__ keff,
+                                   int *sm_ids, int *sm_keff)
+{
+    constexpr int kPerLane = PL;
+    constexpr unsigned kAll = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int K = p.K;
     int my_id = -1;       // lane k < K: the k-th chosen expert
     float my_g = 0.0f;    // and its gate (the unbiased sigmoid)
     for (int k = 0; k < K; ++k) {
@@ -170,6 +211,16 @@ __device__ __forceinline__ void select_token(const SelectParams &p, LogitFn logi
     if (p.E <= 32 * 4) select_token_pl<4>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
     else if (p.E <= 32 * 8) select_token_pl<8>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
     else select_token_pl<16>(p, logit, t, ids, w, keff, sm_ids, sm_keff);
+}
+
+__device__ __forceinline__ void select_token_staged(const SelectParams &p, const float *sig_s,
+                                                    const uint32_t *key_s, int t, int32_t *ids,
+                                                    float *w, int32_t *keff, int *sm_ids,
+                                                    int *sm_keff)
+{
+    if (p.E <= 32 * 4) select_token_staged_pl<4>(p, sig_s, key_s, t, ids, w, keff, sm_ids, sm_keff);
+    else if (p.E <= 32 * 8) select_token_staged_pl<8>(p, sig_s, key_s, t, ids, w, keff, sm_ids, sm_keff);
+    else select_token_staged_pl<16>(p, sig_s, key_s, t, ids, w, keff, sm_ids, sm_keff);
 }
 
 }  // namespace moe
